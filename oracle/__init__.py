@@ -1,0 +1,232 @@
+"""CPU oracle for paged attention over a q8 KV cache.
+
+TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+never calls it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``q8_oracle.c`` (plain C: fp32 scalar quantizer, fp64
+attention); this module only compiles it with gcc and marshals numpy arrays.
+Each function cites the page passage it follows:
+
+* ``q8_quantize_rows`` / ``kv_store`` -- "shared/attention_kit.py"
+  (``quantize_q8``) for the format, "shared/kernels/qk_quant_triton.py"
+  (``_norm_rope_quant``) for rounding half away from zero, "attention_impl.py"
+  (``_store_kvcache_nhd``) for the scatter by slot.
+* ``paged_attention`` -- "attention_impl.py" (``_cache_seq``, ``_sdpa_one``,
+  ``_prefill_torch_from_cache``) and "triton_turboquant_unified_attention.py"
+  (causal limit ``seq_offset <= context_len + query_pos``, GQA row mapping).
+* ``attention_partial`` / ``merge_partials`` -- the split-KV segments of
+  "triton_turboquant_unified_attention.py" (3D kernel) and the log-sum-exp
+  merge ``_merge_lse_`` of "shared/attention_kit.py", in natural-log form.
+
+Parity status of each function (what pins it) is listed in the design notes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q8_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# fp-contract=off: no fused multiply-add, so both hosts (x86-64 here, aarch64
+# on the GPU machine) round every operation the same way.
+CFLAGS = ["-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off", "-fno-fast-math",
+          "-fPIC", "-shared", "-pthread", "-Wall", "-Wextra"]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``q8_oracle.c`` into ``_build/liboracle.so`` (gcc)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        lib.or_f32_to_f16_rne.argtypes = [f32]
+        lib.or_f32_to_f16_rne.restype = ctypes.c_uint16
+        lib.or_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.or_f16_to_f32.restype = f32
+        lib.or_q8_quantize_group.argtypes = [P, P, P]
+        lib.or_q8_quantize_group.restype = None
+        lib.or_q8_quantize_rows.argtypes = [P, i64, i32, P, P]
+        lib.or_q8_quantize_rows.restype = None
+        lib.or_kv_store.argtypes = [P, P, P, i64, i32, i32, P, P, P, P, i64, i32]
+        lib.or_kv_store.restype = i64
+        lib.or_paged_attention.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
+                                           P, P, i32, P, i32, f32, P, i64, P, P, i32]
+        lib.or_paged_attention.restype = ctypes.c_int
+        lib.or_attention_partial.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
+                                             P, P, i32, P, i32, f32, i32, i32, i64, i64,
+                                             P, P, P]
+        lib.or_attention_partial.restype = ctypes.c_int
+        lib.or_merge_partials.argtypes = [i32, P, P, P, i32, P, P]
+        lib.or_merge_partials.restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+# --------------------------------------------------------------------------- formats
+
+def f32_to_f16_bits(x: float) -> int:
+    """binary32 -> binary16 bits, round to nearest even (IEEE definition)."""
+    return int(_load().or_f32_to_f16_rne(ctypes.c_float(x)))
+
+
+def f16_bits_to_f32(h: int) -> float:
+    return float(_load().or_f16_to_f32(ctypes.c_uint16(h)))
+
+
+# --------------------------------------------------------------------------- q8
+
+def q8_quantize_group(x: np.ndarray) -> tuple[np.ndarray, int]:
+    """One group of 32 fp32 values -> (int8 codes [32], fp16 scale bits)."""
+    x = _c(np.asarray(x, dtype=np.float32), np.float32)
+    if x.shape != (32,):
+        raise ValueError("a q8 group has 32 channels")
+    codes = np.empty(32, np.int8)
+    scale = np.empty(1, np.uint16)
+    _load().or_q8_quantize_group(_ptr(x), _ptr(codes), _ptr(scale))
+    return codes, int(scale[0])
+
+
+def q8_quantize_rows(x_bf16_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """bf16 rows (uint16 bit patterns) [..., D] -> codes int8 [..., D],
+    scales fp16 bits uint16 [..., D/32]."""
+    x = _c(x_bf16_bits, np.uint16)
+    d = x.shape[-1]
+    if d % 32:
+        raise ValueError("D must be a multiple of 32")
+    n = x.size // d
+    codes = np.empty(x.shape, np.int8)
+    scales = np.empty((*x.shape[:-1], d // 32), np.uint16)
+    _load().or_q8_quantize_rows(_ptr(x), n, d, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_scale) -> int:
+    """Quantize and scatter [N, Hk, D] bf16 rows into HND caches, in place.
+
+    Caches: codes [num_blocks, Hk, bs, D] int8, scales [num_blocks, Hk, bs, D/32]
+    uint16 (fp16 bits).  Returns the number of skipped out-of-range slots."""
+    key = _c(key_bits, np.uint16)
+    value = _c(value_bits, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    for a in (k_cache, v_cache):
+        if not (a.flags.c_contiguous and a.dtype == np.int8):
+            raise TypeError("code caches must be contiguous int8")
+    for a in (k_scale, v_scale):
+        if not (a.flags.c_contiguous and a.dtype == np.uint16):
+            raise TypeError("scale caches must be contiguous uint16")
+    n, hk, d = key.shape
+    num_blocks, hk2, bs, d2 = k_cache.shape
+    if (hk2, d2) != (hk, d) or value.shape != key.shape or slots.shape != (n,):
+        raise ValueError("shape mismatch")
+    return int(_load().or_kv_store(_ptr(key), _ptr(value), _ptr(slots), n, hk, d,
+                                   _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
+                                   _ptr(v_scale), num_blocks, bs))
+
+
+# --------------------------------------------------------------------------- attention
+
+def _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
+               block_table):
+    q = _c(q_bits, np.uint16)
+    kc, vc = _c(k_cache, np.int8), _c(v_cache, np.int8)
+    ks, vs = _c(k_scale, np.uint16), _c(v_scale, np.uint16)
+    cu = _c(cu_seqlens_q, np.int32)
+    sl = _c(seq_lens, np.int32)
+    bt = _c(block_table, np.int32)
+    T, hq, d = q.shape
+    num_blocks, hk, bs, d2 = kc.shape
+    if d2 != d or vc.shape != kc.shape or hq % hk:
+        raise ValueError("shape mismatch")
+    S = sl.shape[0]
+    if cu.shape != (S + 1,) or bt.ndim != 2 or bt.shape[0] != S:
+        raise ValueError("metadata shape mismatch")
+    keep = (q, kc, ks, vc, vs, cu, sl, bt)
+    args = [_ptr(q), T, hq, hk, d, _ptr(kc), _ptr(ks), _ptr(vc), _ptr(vs), num_blocks, bs,
+            _ptr(cu), _ptr(sl), S, _ptr(bt), bt.shape[1]]
+    return keep, args, T, hq, d
+
+
+def paged_attention(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
+                    block_table, softmax_scale: float, rows=None, n_threads: int = 0):
+    """fp64 causal paged attention.  Returns (out [n, D] float64, lse [n] float64)
+    for the rows ``rows`` (row = token * Hq + q head), all T*Hq rows if None."""
+    keep, args, T, hq, d = _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale,
+                                      cu_seqlens_q, seq_lens, block_table)
+    if rows is None:
+        n = T * hq
+        rows_arr, rows_ptr = None, None
+    else:
+        rows_arr = _c(np.asarray(rows, dtype=np.int64), np.int64)
+        n = rows_arr.shape[0]
+        rows_ptr = _ptr(rows_arr)
+    out = np.empty((n, d), np.float64)
+    lse = np.empty(n, np.float64)
+    err = _load().or_paged_attention(*args, ctypes.c_float(softmax_scale), rows_ptr, n,
+                                     _ptr(out), _ptr(lse), n_threads)
+    del keep
+    if err:
+        raise RuntimeError("oracle: invalid metadata (block table, seq_lens or cu_seqlens_q)")
+    return out, lse
+
+
+def attention_partial(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
+                      block_table, softmax_scale: float, token: int, head: int, lo: int,
+                      hi: int):
+    """Partial triple (m, l, acc[D]) of one row over the visible keys in [lo, hi)."""
+    keep, args, T, hq, d = _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale,
+                                      cu_seqlens_q, seq_lens, block_table)
+    m = np.empty(1, np.float64)
+    l = np.empty(1, np.float64)
+    acc = np.empty(d, np.float64)
+    err = _load().or_attention_partial(*args, ctypes.c_float(softmax_scale), token, head,
+                                       lo, hi, _ptr(m), _ptr(l), _ptr(acc))
+    del keep
+    if err:
+        raise RuntimeError("oracle: invalid metadata")
+    return float(m[0]), float(l[0]), acc
+
+
+def merge_partials(m, l, acc):
+    """Merge partial triples over disjoint key sets -> (out [D], lse)."""
+    m = _c(np.asarray(m, np.float64), np.float64)
+    l = _c(np.asarray(l, np.float64), np.float64)
+    acc = _c(np.asarray(acc, np.float64), np.float64)
+    n, d = acc.shape
+    out = np.empty(d, np.float64)
+    lse = np.empty(1, np.float64)
+    _load().or_merge_partials(n, _ptr(m), _ptr(l), _ptr(acc), d, _ptr(out), _ptr(lse))
+    return out, float(lse[0])

@@ -1,0 +1,436 @@
+/*
+ * Plain CPU oracle for paged attention over a q8 KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  It shares nothing with the
+ * CUDA library: no header, no helper, no table.
+ *
+ * Sources (pages, cited by title and section):
+ *  - "shared/attention_kit.py" (WanGP attention kit): the q8 format
+ *    (`quantize_q8`, `dequantize_q8_into`: int8 data, one FP16 scale per
+ *    32 channels, scale = max|x|/127 clamped at 1e-8) and the two-set
+ *    log-sum-exp merge `_merge_lse_`.
+ *  - "shared/kernels/qk_quant_triton.py" (`_norm_rope_quant`): rounding half
+ *    away from zero before the int8 cast.
+ *  - "attention_impl.py" (fastkernels-b200, `_store_kvcache_nhd`,
+ *    `StoreKVCache`): scatter by slot, slot < 0 skipped,
+ *    block = slot // block_size, offset = slot % block_size; the torch SDPA
+ *    reference paths `_cache_seq`, `_sdpa_one`, `_prefill_torch_from_cache`:
+ *    paged gather, GQA by repeat_interleave, causal mask k_pos <= q_pos with
+ *    key_offset = k_len - q_len.
+ *  - "triton_turboquant_unified_attention.py" (vLLM unified kernel): the
+ *    seq_lens / query_start_loc meaning, the causal limit
+ *    seq_offset <= context_len + query_pos, the 3D split-KV segments and the
+ *    (max, expsum, acc) partial triples merged by the online-softmax rule.
+ *
+ * Precision: quantization takes its decisions in fp32, as the q8 pages do
+ * (`x.float()`, then fp32 divide, round, clamp, FP16 store).  Attention is
+ * fp64 over the exactly dequantized values code * (double)scale.
+ *
+ * Readings where the pages are silent or disagree (each is listed in the
+ * design notes):
+ *  - rounding is exact round-half-away-from-zero of the fp32 quotient
+ *    (C `roundf`), not "+0.5*sign then truncate";
+ *  - the divisor is the fp32 scale before its FP16 rounding;
+ *  - the scale floor is 1e-8 (fp32), and FP16 conversion is round to nearest
+ *    even;
+ *  - the LSE is the natural log of sum_j exp(scale * q.k_j);
+ *  - caches are HND: codes [num_blocks, Hk, block_size, D] int8, scales
+ *    [num_blocks, Hk, block_size, D/32] fp16.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define OR_GROUP 32
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 bit pattern -> value.  bf16 is the upper half of an IEEE binary32. */
+static float or_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* binary16 bit pattern -> value (exact; every binary16 is a binary32). */
+float or_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) & 1u;
+    uint32_t exp = (uint32_t)(h >> 10) & 0x1fu;
+    uint32_t man = (uint32_t)h & 0x3ffu;
+    float mag;
+    if (exp == 0) {
+        mag = ldexpf((float)man, -24);            /* zero or subnormal: man * 2^-24 */
+    } else if (exp == 31) {
+        mag = man ? NAN : INFINITY;
+    } else {
+        mag = ldexpf((float)(man | 0x400u), (int)exp - 25); /* 1.man * 2^(exp-15) */
+    }
+    return sign ? -mag : mag;
+}
+
+/*
+ * binary32 -> binary16, round to nearest, ties to even (IEEE 754 default).
+ * Written from the definition: find the two neighbouring binary16 values and
+ * pick the nearer, the even one on a tie.  Overflow past the largest finite
+ * binary16 (65504) rounds to infinity exactly when the value is at or above
+ * 65520, the midpoint between 65504 and 2^16.
+ */
+uint16_t or_f32_to_f16_rne(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    float a = fabsf(x);
+    if (isnan(x)) return (uint16_t)(sign | 0x7e00u);
+    if (a >= 65520.0f) return (uint16_t)(sign | 0x7c00u);   /* rounds to inf */
+    /* binary16 step (ulp) at a: 2^(e-10) for normal a in [2^e, 2^(e+1)),
+     * 2^-24 for subnormal a < 2^-14. */
+    int e;
+    if (a < ldexpf(1.0f, -14)) {
+        e = -14;
+    } else {
+        (void)frexpf(a, &e);   /* a = m * 2^e, m in [0.5, 1) */
+        e -= 1;                /* a in [2^e, 2^(e+1)) */
+    }
+    double ulp = ldexp(1.0, e - 10);
+    double q = (double)a / ulp;          /* exact: a has 24 bits, ulp a power of two */
+    double lo = floor(q);
+    double rem = q - lo;
+    double n;
+    if (rem > 0.5) n = lo + 1.0;
+    else if (rem < 0.5) n = lo;
+    else n = (fmod(lo, 2.0) == 0.0) ? lo : lo + 1.0;
+    double r = n * ulp;                  /* the rounded magnitude, exact */
+    /* encode r */
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -14)) {
+        uint16_t man = (uint16_t)(r / ldexp(1.0, -24));
+        return (uint16_t)(sign | man);
+    }
+    int re;
+    double m = frexp(r, &re);            /* r = m * 2^re, m in [0.5, 1) */
+    int exp16 = re - 1 + 15;             /* r = 1.f * 2^(re-1) */
+    if (exp16 >= 31) return (uint16_t)(sign | 0x7c00u);
+    uint16_t man = (uint16_t)((m * 2.0 - 1.0) * 1024.0);
+    return (uint16_t)(sign | ((uint16_t)exp16 << 10) | man);
+}
+
+/* ------------------------------------------------------------------------ */
+/* q8 quantization of one group of 32 channels                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * q8 format ("shared/attention_kit.py", `quantize_q8`):
+ *   amax  = max |x| over the group                        (fp32)
+ *   s32   = max(amax / 127, 1e-8)                         (fp32 divide, clamp_min)
+ *   code  = clamp(round_half_away(x / s32), -127, 127)    (fp32 divide)
+ *   scale = fp16(s32), round to nearest even
+ * Rounding half away from zero follows "shared/kernels/qk_quant_triton.py"
+ * (`_norm_rope_quant`), taken exactly (C roundf).
+ */
+void or_q8_quantize_group(const float *x, int8_t *codes, uint16_t *scale_bits)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < OR_GROUP; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float s32 = amax / 127.0f;
+    if (s32 < 1e-8f) s32 = 1e-8f;
+    for (int i = 0; i < OR_GROUP; ++i) {
+        float r = roundf(x[i] / s32);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        codes[i] = (int8_t)r;
+    }
+    *scale_bits = or_f32_to_f16_rne(s32);
+}
+
+/* Quantize rows of bf16 values: x [n_rows, d] -> codes [n_rows, d],
+ * scales [n_rows, d/32]. */
+void or_q8_quantize_rows(const uint16_t *x_bf16, int64_t n_rows, int32_t d,
+                         int8_t *codes, uint16_t *scales)
+{
+    float buf[OR_GROUP];
+    int32_t groups = d / OR_GROUP;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int32_t g = 0; g < groups; ++g) {
+            const uint16_t *src = x_bf16 + r * d + (int64_t)g * OR_GROUP;
+            for (int i = 0; i < OR_GROUP; ++i) buf[i] = or_bf16_to_f32(src[i]);
+            or_q8_quantize_group(buf, codes + r * d + (int64_t)g * OR_GROUP,
+                                 scales + r * groups + g);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* kv_store: quantize and scatter by slot                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * key, value: [n_tokens, hk, d] bf16 bits, contiguous.
+ * Caches (HND): codes [num_blocks, hk, bs, d] int8; scales
+ * [num_blocks, hk, bs, d/32] fp16 bits.
+ * Scatter ("attention_impl.py", `_store_kvcache_nhd`): slot < 0 is skipped;
+ * block = slot / bs, offset = slot % bs.  A slot at or beyond
+ * num_blocks * bs is skipped and counted in the return value.
+ */
+int64_t or_kv_store(const uint16_t *key, const uint16_t *value,
+                    const int64_t *slot_mapping, int64_t n_tokens, int32_t hk,
+                    int32_t d, int8_t *k_cache, uint16_t *k_scale,
+                    int8_t *v_cache, uint16_t *v_scale, int64_t num_blocks,
+                    int32_t bs)
+{
+    int64_t bad = 0;
+    int32_t groups = d / OR_GROUP;
+    for (int64_t n = 0; n < n_tokens; ++n) {
+        int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * bs) { ++bad; continue; }
+        int64_t block = slot / bs;
+        int64_t offset = slot % bs;
+        for (int32_t h = 0; h < hk; ++h) {
+            int64_t row = (block * hk + h) * bs + offset;     /* HND row */
+            const uint16_t *ks = key + (n * hk + h) * (int64_t)d;
+            const uint16_t *vs = value + (n * hk + h) * (int64_t)d;
+            or_q8_quantize_rows(ks, 1, d, k_cache + row * d, k_scale + row * groups);
+            or_q8_quantize_rows(vs, 1, d, v_cache + row * d, v_scale + row * groups);
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged attention in fp64                                                   */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *q;          /* [T, hq, d] bf16 bits */
+    int32_t T, hq, hk, d;
+    const int8_t *k_cache;
+    const uint16_t *k_scale;
+    const int8_t *v_cache;
+    const uint16_t *v_scale;
+    int64_t num_blocks;
+    int32_t bs;
+    const int32_t *cu_seqlens_q;    /* [S+1] */
+    const int32_t *seq_lens;        /* [S] */
+    int32_t S;
+    const int32_t *block_table;     /* [S, bt_stride] */
+    int32_t bt_stride;
+    double softmax_scale;
+} or_problem;
+
+/* HND row of key j of kv head h of sequence s, through the block table
+ * ("attention_impl.py", `_cache_seq`: page j / bs, offset j % bs), or -1
+ * when the table entry is missing or out of range. */
+static int64_t or_kv_row(const or_problem *p, int32_t s, int32_t h, int64_t j)
+{
+    int64_t page = j / p->bs;
+    int64_t off = j % p->bs;
+    if (page >= p->bt_stride) return -1;
+    int64_t blk = p->block_table[(int64_t)s * p->bt_stride + page];
+    if (blk < 0 || blk >= p->num_blocks) return -1;
+    return (blk * p->hk + h) * p->bs + off;
+}
+
+/* Dequantized channel c of an HND row: code * scale, exact in fp64
+ * ("shared/attention_kit.py", `dequantize_q8_into`). */
+static double or_dequant(const or_problem *p, const int8_t *cache,
+                         const uint16_t *scale, int64_t row, int32_t c)
+{
+    int32_t groups = p->d / OR_GROUP;
+    double code = (double)cache[row * p->d + c];
+    double sc = (double)or_f16_to_f32(scale[row * groups + c / OR_GROUP]);
+    return code * sc;
+}
+
+/* Sequence of token t: the s with cu[s] <= t < cu[s+1] (linear scan). */
+static int32_t or_seq_of_token(const or_problem *p, int32_t t)
+{
+    for (int32_t s = 0; s < p->S; ++s)
+        if (p->cu_seqlens_q[s] <= t && t < p->cu_seqlens_q[s + 1]) return s;
+    return -1;
+}
+
+/*
+ * Attention of one (token t, q head h) over the visible keys j in [lo, hi):
+ * visible means j <= context_len + i, context_len = seq_len - q_len,
+ * i = t - cu[s] ("triton_turboquant_unified_attention.py", causal mask;
+ * "attention_impl.py", `_sdpa_one` with key_offset = k_len - q_len).
+ * GQA: q head h reads kv head h / (hq / hk).
+ * Returns the partial triple (m, l, acc): m = max score, l = sum exp(s - m),
+ * acc = sum exp(s - m) * v.  An empty range gives m = -inf, l = 0, acc = 0.
+ * scores: scratch of at least hi - lo doubles.
+ */
+static int or_partial(const or_problem *p, int32_t t, int32_t h, int64_t lo,
+                      int64_t hi, double *scores, double *m_out, double *l_out,
+                      double *acc)
+{
+    int err = 0;
+    int32_t s = or_seq_of_token(p, t);
+    if (s < 0) return 1;
+    int32_t q_len = p->cu_seqlens_q[s + 1] - p->cu_seqlens_q[s];
+    int64_t ctx = (int64_t)p->seq_lens[s] - q_len;
+    int64_t i = t - p->cu_seqlens_q[s];
+    int64_t last = ctx + i;                     /* last visible key */
+    if (ctx < 0) return 1;
+    if (hi > last + 1) hi = last + 1;
+    int32_t kvh = h / (p->hq / p->hk);
+    const uint16_t *qrow = p->q + ((int64_t)t * p->hq + h) * p->d;
+    for (int32_t c = 0; c < p->d; ++c) acc[c] = 0.0;
+    if (hi <= lo) { *m_out = -INFINITY; *l_out = 0.0; return 0; }
+    double m = -INFINITY;
+    for (int64_t j = lo; j < hi; ++j) {
+        int64_t row = or_kv_row(p, s, kvh, j);
+        double dot = 0.0;
+        if (row < 0) err = 1;
+        else
+            for (int32_t c = 0; c < p->d; ++c)
+                dot += (double)or_bf16_to_f32(qrow[c]) *
+                       or_dequant(p, p->k_cache, p->k_scale, row, c);
+        scores[j - lo] = p->softmax_scale * dot;
+        if (scores[j - lo] > m) m = scores[j - lo];
+    }
+    double l = 0.0;
+    for (int64_t j = lo; j < hi; ++j) {
+        int64_t row = or_kv_row(p, s, kvh, j);
+        double w = exp(scores[j - lo] - m);
+        l += w;
+        if (row >= 0)
+            for (int32_t c = 0; c < p->d; ++c)
+                acc[c] += w * or_dequant(p, p->v_cache, p->v_scale, row, c);
+    }
+    *m_out = m;
+    *l_out = l;
+    return err;
+}
+
+/*
+ * Merge of partial triples over disjoint key sets (the online-softmax rule of
+ * the split-KV segments, and "shared/attention_kit.py" `_merge_lse_` in
+ * natural-log form):
+ *   M = max_k m_k;  w_k = exp(m_k - M)  (0 for an empty part);
+ *   out = sum_k w_k acc_k / sum_k w_k l_k;  lse = M + ln sum_k w_k l_k.
+ */
+void or_merge_partials(int32_t n, const double *m, const double *l,
+                       const double *acc, int32_t d, double *out, double *lse)
+{
+    double M = -INFINITY;
+    for (int32_t k = 0; k < n; ++k) if (m[k] > M) M = m[k];
+    double L = 0.0;
+    for (int32_t c = 0; c < d; ++c) out[c] = 0.0;
+    for (int32_t k = 0; k < n; ++k) {
+        if (m[k] == -INFINITY) continue;
+        double w = exp(m[k] - M);
+        L += w * l[k];
+        for (int32_t c = 0; c < d; ++c) out[c] += w * acc[(int64_t)k * d + c];
+    }
+    for (int32_t c = 0; c < d; ++c) out[c] /= L;
+    *lse = M + log(L);
+}
+
+typedef struct {
+    const or_problem *p;
+    const int64_t *rows;     /* row r = token * hq + head */
+    int64_t n_rows;
+    int64_t next;            /* shared work counter */
+    pthread_mutex_t lock;
+    double *out, *lse;
+    int64_t max_keys;
+    int errors;
+} or_job;
+
+static void *or_worker(void *arg)
+{
+    or_job *job = (or_job *)arg;
+    const or_problem *p = job->p;
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(job->max_keys + 1));
+    double *acc = (double *)malloc(sizeof(double) * (size_t)p->d);
+    int errors = 0;
+    for (;;) {
+        pthread_mutex_lock(&job->lock);
+        int64_t k = job->next++;
+        pthread_mutex_unlock(&job->lock);
+        if (k >= job->n_rows) break;
+        int64_t r = job->rows ? job->rows[k] : k;
+        int32_t t = (int32_t)(r / p->hq), h = (int32_t)(r % p->hq);
+        double m, l;
+        errors |= or_partial(p, t, h, 0, job->max_keys, scores, &m, &l, acc);
+        /* one part: out = acc / l, lse = m + ln l */
+        or_merge_partials(1, &m, &l, acc, p->d, job->out + k * p->d, job->lse + k);
+    }
+    pthread_mutex_lock(&job->lock);
+    job->errors |= errors;
+    pthread_mutex_unlock(&job->lock);
+    free(scores);
+    free(acc);
+    return NULL;
+}
+
+/*
+ * Full attention for the listed rows (row = token * hq + q head; rows == NULL
+ * means all T * hq rows in order).  out [n_rows, d] and lse [n_rows] fp64.
+ * n_threads <= 0 uses every online core.  Returns 0, or 1 when a row's
+ * metadata was invalid (its result is then meaningless).
+ */
+int or_paged_attention(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
+                       int32_t d, const int8_t *k_cache, const uint16_t *k_scale,
+                       const int8_t *v_cache, const uint16_t *v_scale,
+                       int64_t num_blocks, int32_t bs, const int32_t *cu_seqlens_q,
+                       const int32_t *seq_lens, int32_t S,
+                       const int32_t *block_table, int32_t bt_stride,
+                       float softmax_scale, const int64_t *rows, int64_t n_rows,
+                       double *out, double *lse, int32_t n_threads)
+{
+    or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
+                    num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
+                    bt_stride, (double)softmax_scale};
+    if (!rows) n_rows = (int64_t)T * hq;
+    int64_t max_keys = 1;
+    for (int32_t s = 0; s < S; ++s) if (seq_lens[s] > max_keys) max_keys = seq_lens[s];
+    or_job job;
+    job.p = &p; job.rows = rows; job.n_rows = n_rows; job.next = 0;
+    job.out = out; job.lse = lse; job.max_keys = max_keys; job.errors = 0;
+    pthread_mutex_init(&job.lock, NULL);
+    if (n_threads <= 0) n_threads = (int32_t)sysconf(_SC_NPROCESSORS_ONLN);
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 512) n_threads = 512;
+    pthread_t tids[512];
+    for (int32_t i = 0; i < n_threads; ++i) pthread_create(&tids[i], NULL, or_worker, &job);
+    for (int32_t i = 0; i < n_threads; ++i) pthread_join(tids[i], NULL);
+    pthread_mutex_destroy(&job.lock);
+    return job.errors;
+}
+
+/*
+ * Partial triple of one row over keys [lo, hi) (split-KV segment), for the
+ * merge identities.  acc [d].
+ */
+int or_attention_partial(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
+                         int32_t d, const int8_t *k_cache, const uint16_t *k_scale,
+                         const int8_t *v_cache, const uint16_t *v_scale,
+                         int64_t num_blocks, int32_t bs,
+                         const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                         int32_t S, const int32_t *block_table, int32_t bt_stride,
+                         float softmax_scale, int32_t token, int32_t head,
+                         int64_t lo, int64_t hi, double *m, double *l, double *acc)
+{
+    or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
+                    num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
+                    bt_stride, (double)softmax_scale};
+    int64_t n = hi > lo ? hi - lo : 1;
+    double *scores = (double *)malloc(sizeof(double) * (size_t)n);
+    int err = or_partial(&p, token, head, lo, hi, scores, m, l, acc);
+    free(scores);
+    return err;
+}

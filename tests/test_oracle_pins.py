@@ -1,0 +1,425 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests re-types the oracle's formulas.  Each one checks the
+oracle against something else: values worked out by hand from the pages'
+definitions (tests/golden), a library routine (numpy's IEEE fp16 conversion,
+torch's fp64 scaled_dot_product_attention and logsumexp), closed forms,
+invariants, or one part of the oracle against another (split against joint).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_attention_int8_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q8_hand_examples.txt")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _load_golden():
+    cases = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, xs, codes, bits = [p.strip() for p in line.split(";")]
+        x = np.array([float(v) for v in xs.split(",")], np.float32)
+        c = np.array([int(v) for v in codes.split(",")], np.int8)
+        cases.append((name, x, c, int(bits, 16)))
+    return cases
+
+
+def _f16_bits_numpy(x: np.ndarray) -> np.ndarray:
+    return np.asarray(x, np.float32).astype(np.float16).view(np.uint16)
+
+
+def _bf16_bits(x: torch.Tensor) -> np.ndarray:
+    return inputs.bf16_bits(x.to(torch.bfloat16))
+
+
+def _rand_cache(rng, num_blocks, hk, bs, d, scale_lo=0.005, scale_hi=0.05):
+    kc = rng.integers(-127, 128, size=(num_blocks, hk, bs, d), dtype=np.int8)
+    vc = rng.integers(-127, 128, size=(num_blocks, hk, bs, d), dtype=np.int8)
+    ks = _f16_bits_numpy(rng.uniform(scale_lo, scale_hi, size=(num_blocks, hk, bs, d // 32)))
+    vs = _f16_bits_numpy(rng.uniform(scale_lo, scale_hi, size=(num_blocks, hk, bs, d // 32)))
+    return kc, ks, vc, vs
+
+
+def _dequant(codes, scales):
+    """Reference dequantization with numpy (fp64): value = code * fp16 scale."""
+    s = scales.view(np.float16).astype(np.float64)
+    return codes.astype(np.float64) * np.repeat(s, 32, axis=-1)
+
+
+def _problem(rng, q_lens, seq_lens, hq, hk, d, bs, spare=3, q_scale=1.0):
+    S = len(seq_lens)
+    pages = [(L + bs - 1) // bs for L in seq_lens]
+    num_blocks = sum(pages) + spare
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    bt = np.full((S, max(pages)), -1, np.int32)
+    pos = 0
+    for s, n in enumerate(pages):
+        bt[s, :n] = perm[pos:pos + n]
+        pos += n
+    cu = np.zeros(S + 1, np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    T = int(cu[-1])
+    q = _bf16_bits(torch.from_numpy(rng.standard_normal((T, hq, d)) * q_scale))
+    kc, ks, vc, vs = _rand_cache(rng, num_blocks, hk, bs, d)
+    return dict(q=q, kc=kc, ks=ks, vc=vc, vs=vs, cu=cu, sl=np.array(seq_lens, np.int32),
+                bt=bt, hq=hq, hk=hk, d=d, bs=bs)
+
+
+def _run(p, scale, rows=None):
+    return oracle.paged_attention(p["q"], p["kc"], p["ks"], p["vc"], p["vs"], p["cu"],
+                                  p["sl"], p["bt"], scale, rows=rows, n_threads=4)
+
+
+def _gather(p, codes, scales, s, L):
+    """Logical [L, Hk, D] fp64 of sequence s (numpy gather through the table)."""
+    bs = p["bs"]
+    j = np.arange(L)
+    blk = p["bt"][s, j // bs]
+    off = j % bs
+    deq = _dequant(codes, scales)                 # [nb, hk, bs, d]
+    return deq[blk, :, off, :]                     # [L, hk, d]
+
+
+# ----------------------------------------------------------------------------- number formats
+
+def test_f16_conversion_matches_ieee_round_to_nearest_even():
+    rng = np.random.default_rng(11)
+    vals = [rng.standard_normal(4000) * 10.0 ** rng.integers(-9, 5, 4000)]
+    # exact midpoints between neighbouring fp16 values (ties), normal and subnormal
+    h = np.arange(0, 0x7bff, 7, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    vals.append(((lo + hi) / 2).astype(np.float32))
+    vals.append(np.array([0.0, -0.0, 1e-8, 2.98e-8, 2.9802322e-08, 5.96e-8, 6.1e-5,
+                          65504.0, 65519.99, 65520.0, 65536.0, 1e30, -65520.0,
+                          np.float32(1) / np.float32(127)], np.float32))
+    x = np.concatenate([np.asarray(v, np.float32) for v in vals])
+    x = np.concatenate([x, -x])
+    got = np.array([oracle.f32_to_f16_bits(float(v)) for v in x], np.uint16)
+    np.testing.assert_array_equal(got, _f16_bits_numpy(x))
+
+
+def test_f16_decode_matches_ieee_for_every_finite_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = np.isfinite(bits.view(np.float16))
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_bits_to_f32(int(b)) for b in bits[finite]], np.float32)
+    np.testing.assert_array_equal(got, ref[finite])
+
+
+# ----------------------------------------------------------------------------- q8 quantizer
+
+@pytest.mark.parametrize("case", _load_golden(), ids=lambda c: c[0])
+def test_q8_hand_examples(case):
+    name, x, codes, bits = case
+    got_codes, got_bits = oracle.q8_quantize_group(x)
+    np.testing.assert_array_equal(got_codes, codes)
+    assert got_bits == bits
+
+
+def test_q8_rounding_is_half_away_not_half_even_nor_add_half_truncate():
+    # 0.5 - 2^-25: exact rounding gives 0; "+0.5 then truncate" in fp32 gives 1
+    # (0.5 - 2^-25 + 0.5 rounds up to 1.0), and half-even would also give 0.
+    x = np.zeros(32, np.float32)
+    x[0] = 127.0
+    x[1] = np.float32(0.5) - np.float32(2.0 ** -25)
+    x[2] = 2.5
+    codes, _ = oracle.q8_quantize_group(x)
+    assert codes[1] == 0
+    assert codes[2] == 3  # half-even would give 2
+
+
+def _random_groups(rng, n):
+    groups = []
+    for i in range(n):
+        kind = i % 5
+        if kind == 0:
+            g = rng.standard_normal(32)
+        elif kind == 1:   # one outlier over tiny values
+            g = rng.standard_normal(32) * 1e-3
+            g[rng.integers(32)] = rng.choice([-1, 1]) * rng.uniform(10, 1000)
+        elif kind == 2:   # values on tie points of a scale-one grid
+            g = rng.integers(-126, 127, 32) + 0.5
+            g[0] = 127.0
+        elif kind == 3:   # widely varying magnitudes
+            g = rng.standard_normal(32) * 10.0 ** rng.uniform(-6, 4)
+        else:             # bf16-representable values, as the kernels see them
+            g = torch.from_numpy(rng.standard_normal(32) * 3).to(torch.bfloat16).float().numpy()
+        groups.append(np.asarray(g, np.float32))
+    return groups
+
+
+def test_q8_invariants_on_random_groups():
+    rng = np.random.default_rng(5)
+    for x in _random_groups(rng, 600):
+        codes, bits = oracle.q8_quantize_group(x)
+        c = codes.astype(np.int64)
+        amax = float(np.max(np.abs(x)))
+        s16 = float(np.array([bits], np.uint16).view(np.float16)[0])
+        assert np.all(np.abs(c) <= 127)
+        assert not np.any(c == -128)
+        # the element of largest magnitude maps to +-127
+        k = int(np.argmax(np.abs(x)))
+        if amax > 0:
+            assert c[k] == (127 if x[k] > 0 else -127)
+        # rounding error against the fp32 scale: at most half a step (plus the
+        # quotient's own rounding), never more
+        s32 = max(amax / 127.0, 1e-8)
+        err = np.abs(x.astype(np.float64) - c * s32)
+        assert np.all(err <= 0.5 * s32 * (1 + 1e-6) + 1e-30)
+        # round trip through the stored fp16 scale
+        rt = np.abs(x.astype(np.float64) - c * s16)
+        assert np.all(rt <= 0.5 * s32 * (1 + 1e-6) + 127 * abs(s32 - s16) + 1e-30)
+        # the fp16 scale is the nearest fp16 of the fp32 scale: within half an ulp
+        assert abs(s16 - s32) <= 2.0 ** -11 * s32 + 2.0 ** -25
+
+
+def test_q8_groups_are_32_consecutive_channels():
+    # Four groups with very different magnitudes: each group's scale depends on
+    # its own 32 channels only, so each group's maximum maps to 127.
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(32) * m for m in (1e-3, 1.0, 50.0, 1e-6)])
+    bits = _bf16_bits(torch.from_numpy(x)).reshape(1, 128)
+    codes, scales = oracle.q8_quantize_rows(bits)
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()[0]
+    for g in range(4):
+        part = xb[32 * g:32 * g + 32]
+        one_codes, one_bits = oracle.q8_quantize_group(part)
+        np.testing.assert_array_equal(codes[0, 32 * g:32 * g + 32], one_codes)
+        assert scales[0, g] == one_bits
+        assert np.max(np.abs(codes[0, 32 * g:32 * g + 32].astype(int))) == 127
+
+
+# ----------------------------------------------------------------------------- kv_store scatter
+
+def _small_store_problem(seed=0, hk=2, d=64, bs=16):
+    spec = inputs.Spec("pin", seed, hq=2 * hk, hk=hk, d=d, bs=bs, n_prefill=2, prefill_qlen=5,
+                       prefix_lens=(3, 40), n_decode=3, decode_lens=(1, 50), pad_frac=0.2,
+                       spare_blocks=4)
+    return inputs.make_workload(spec)
+
+
+def test_kv_store_skips_padding_and_leaves_canary_elsewhere():
+    w = _small_store_problem()
+    k, v, slots = w.all_key_value()
+    kc, ks, vc, vs = [t.numpy() for t in inputs.empty_cache(w.num_blocks, 2, 16, 64)]
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    bad = oracle.kv_store(inputs.bf16_bits(k), inputs.bf16_bits(v), slots.numpy(), kc, ks, vc, vs)
+    assert bad == 0
+    written = np.zeros(w.num_blocks * 16, bool)
+    written[slots.numpy()[slots.numpy() >= 0]] = True
+    # slot -> (block, offset) in HND: a written slot holds no canary, an
+    # unwritten one holds only canary
+    codes_by_slot = kc.transpose(0, 2, 1, 3).reshape(w.num_blocks * 16, -1)
+    scales_by_slot = ks.transpose(0, 2, 1, 3).reshape(w.num_blocks * 16, -1)
+    assert np.all(codes_by_slot[~written] == -128)
+    assert np.all(scales_by_slot[~written] == 0xFFFF)
+    assert not np.any(codes_by_slot[written] == -128)
+    assert (slots.numpy() < 0).sum() > 0  # padding rows were present and skipped
+
+
+def test_kv_store_out_of_range_slot_is_reported_not_written():
+    kc, ks, vc, vs = [t.numpy() for t in inputs.empty_cache(2, 1, 16, 32)]
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    key = _bf16_bits(torch.ones(3, 1, 32))
+    bad = oracle.kv_store(key, key, np.array([5, 32, -1], np.int64), kc, ks, vc, vs)
+    assert bad == 1
+    assert np.all(kc.reshape(32, 32)[np.arange(32) != 5] == -128)
+
+
+def test_store_then_gather_is_independent_of_physical_placement():
+    # The same rows stored under two different block tables read back equal
+    # through each table: placement is invisible to a reader of the logical cache.
+    w1 = _small_store_problem(seed=1)
+    logical = []
+    rng = np.random.default_rng(9)
+    perm = rng.permutation(w1.num_blocks).astype(np.int32)
+    bt2 = np.where(w1.block_table.numpy() >= 0, perm[np.maximum(w1.block_table.numpy(), 0)], -1)
+    k, v, slots = w1.all_key_value()
+    slots = slots.numpy()
+    bs = 16
+    slots2 = np.where(slots >= 0, perm[np.maximum(slots, 0) // bs] * bs + np.maximum(slots, 0) % bs, -1)
+    for table, sl in ((w1.block_table.numpy(), slots), (bt2, slots2)):
+        kc, ks, vc, vs = [t.numpy() for t in inputs.empty_cache(w1.num_blocks, 2, bs, 64)]
+        ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+        oracle.kv_store(inputs.bf16_bits(k), inputs.bf16_bits(v), sl, kc, ks, vc, vs)
+        p = dict(bt=table, bs=bs)
+        logical.append([_gather(p, kc, ks, s, int(L)) for s, L in enumerate(w1.seq_lens.tolist())]
+                       + [_gather(p, vc, vs, s, int(L)) for s, L in enumerate(w1.seq_lens.tolist())])
+    for a, b in zip(*logical):
+        np.testing.assert_array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------- attention
+
+def test_attention_matches_torch_sdpa_fp64_brute_force():
+    """Tiny mixed batch against torch's scaled_dot_product_attention in float64
+    (explicit causal mask with key offset k_len - q_len, repeat_interleave of
+    kv heads), as the torch reference paths of "attention_impl.py" set it up;
+    LSE against torch.logsumexp of the masked scores."""
+    rng = np.random.default_rng(21)
+    hq, hk, d, bs = 6, 2, 64, 16
+    q_lens = [5, 1, 3, 1, 17]
+    seq_lens = [5, 40, 19, 1, 50]
+    p = _problem(rng, q_lens, seq_lens, hq, hk, d, bs)
+    scale = 0.125
+    out, lse = _run(p, scale)
+    out = out.reshape(-1, hq, d)
+    lse = lse.reshape(-1, hq)
+    qf = torch.from_numpy(p["q"].view(np.int16)).view(torch.bfloat16).double()
+    for s in range(len(q_lens)):
+        L, ql = seq_lens[s], q_lens[s]
+        K = torch.from_numpy(_gather(p, p["kc"], p["ks"], s, L))          # [L, hk, d]
+        V = torch.from_numpy(_gather(p, p["vc"], p["vs"], s, L))
+        K = K.repeat_interleave(hq // hk, dim=1).transpose(0, 1)          # [hq, L, d]
+        V = V.repeat_interleave(hq // hk, dim=1).transpose(0, 1)
+        Q = qf[p["cu"][s]:p["cu"][s + 1]].transpose(0, 1)                  # [hq, ql, d]
+        mask = torch.arange(L)[None, :] <= (L - ql + torch.arange(ql))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            Q[None], K[None], V[None], attn_mask=mask, scale=scale)[0].transpose(0, 1)
+        scores = (Q @ K.transpose(1, 2)) * scale
+        ref_lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1).transpose(0, 1)
+        np.testing.assert_allclose(out[p["cu"][s]:p["cu"][s + 1]], ref.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[p["cu"][s]:p["cu"][s + 1]], ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_one_visible_key_gives_that_value_and_its_score():
+    # "attention_impl.py" single-token path: a one-key softmax is exactly 1.
+    rng = np.random.default_rng(2)
+    p = _problem(rng, [1, 1], [1, 1], 4, 2, 64, 16)
+    out, lse = _run(p, 0.2)
+    qf = torch.from_numpy(p["q"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    for s in range(2):
+        K = _gather(p, p["kc"], p["ks"], s, 1)[0]
+        V = _gather(p, p["vc"], p["vs"], s, 1)[0]
+        for h in range(4):
+            r = s * 4 + h
+            np.testing.assert_allclose(out[r], V[h // 2], rtol=0, atol=1e-15)
+            # the softmax scale is an fp32 argument: 0.2 means float32(0.2)
+            assert abs(lse[r] - float(np.float32(0.2)) * float(np.dot(qf[s, h], K[h // 2]))) < 1e-12
+
+
+def test_zero_query_gives_mean_value_and_log_count():
+    rng = np.random.default_rng(4)
+    p = _problem(rng, [1, 4], [33, 20], 4, 2, 64, 16, q_scale=0.0)
+    out, lse = _run(p, 0.3)
+    out = out.reshape(-1, 4, 64)
+    lse = lse.reshape(-1, 4)
+    # decode row: 33 visible keys; prefill rows i = 0..3 see 16 + i + 1 keys
+    for t, (s, n) in enumerate([(0, 33), (1, 17), (1, 18), (1, 19), (1, 20)]):
+        V = _gather(p, p["vc"], p["vs"], s, n)
+        for h in range(4):
+            np.testing.assert_allclose(out[t, h], V[:, h // 2].mean(0), rtol=0, atol=1e-12)
+            assert abs(lse[t, h] - math.log(n)) < 1e-12
+
+
+def test_identical_keys_and_constant_values():
+    # all keys equal -> uniform weights, lse = s + ln n; values constant per
+    # channel -> output equals that constant (the weights sum to one)
+    rng = np.random.default_rng(8)
+    p = _problem(rng, [1, 3], [70, 45], 8, 2, 128, 16)
+    p["kc"][:] = p["kc"][0, 0, 0][None, None, None, :]
+    p["ks"][:] = p["ks"][0, 0, 0][None, None, None, :]
+    p["vc"][:] = 7
+    p["vs"][:] = _f16_bits_numpy(np.full(p["vs"].shape, 0.5))
+    out, lse = _run(p, 0.1)
+    qf = torch.from_numpy(p["q"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    k0 = _dequant(p["kc"][0, 0, 0], p["ks"][0, 0, 0])
+    np.testing.assert_allclose(out, 3.5, rtol=0, atol=1e-12)
+    counts = [70, 43, 44, 45]
+    for t in range(4):
+        for h in range(8):
+            s0 = float(np.float32(0.1)) * float(np.dot(qf[t, h], k0))
+            assert abs(lse[t * 8 + h] - (s0 + math.log(counts[t]))) < 1e-11
+
+
+def test_gqa_head_h_reads_kv_head_h_over_qpk():
+    rng = np.random.default_rng(6)
+    hq, hk = 12, 3
+    p = _problem(rng, [1], [40], hq, hk, 64, 16)
+    for kv in range(hk):
+        p["vc"][:, kv] = 10 * (kv + 1)
+    p["vs"][:] = _f16_bits_numpy(np.full(p["vs"].shape, 1.0))
+    out, _ = _run(p, 0.125)
+    for h in range(hq):
+        np.testing.assert_allclose(out[h], 10.0 * (h // (hq // hk) + 1), rtol=0, atol=1e-12)
+
+
+def test_causal_limit_is_bottom_right_aligned():
+    # value channel 0 of key j = j (code j, scale 1); q = 0 gives the mean of
+    # the visible positions: query i of a chunk with context c sees 0..c+i
+    rng = np.random.default_rng(7)
+    L, ql = 100, 6
+    p = _problem(rng, [ql], [L], 2, 1, 32, 16, q_scale=0.0)
+    s = 0
+    j = np.arange(L)
+    blk = p["bt"][s, j // 16]
+    p["vc"][blk, 0, j % 16, 0] = j.astype(np.int8)
+    p["vs"][:] = _f16_bits_numpy(np.full(p["vs"].shape, 1.0))
+    out, _ = _run(p, 1.0)
+    out = out.reshape(ql, 2, 32)
+    for i in range(ql):
+        c = L - ql
+        assert abs(out[i, 0, 0] - (c + i) / 2.0) < 1e-12
+
+
+def test_paged_equals_contiguous():
+    # the same logical cache laid out contiguously (identity block table) and
+    # scattered (permuted table) gives the same result bit for bit
+    rng = np.random.default_rng(10)
+    p = _problem(rng, [3, 1], [45, 64], 4, 2, 64, 16, spare=0)
+    out1, lse1 = _run(p, 0.125)
+    # build the contiguous copy: sequence s page k -> physical block offset_s + k
+    bt = p["bt"]
+    pages = [(L + 15) // 16 for L in p["sl"]]
+    ident = np.full_like(bt, -1)
+    order = []
+    pos = 0
+    for s, n in enumerate(pages):
+        ident[s, :n] = np.arange(pos, pos + n)
+        order.extend(bt[s, :n].tolist())
+        pos += n
+    q = dict(p)
+    for key in ("kc", "ks", "vc", "vs"):
+        q[key] = np.ascontiguousarray(p[key][order])
+    q["bt"] = ident
+    out2, lse2 = _run(q, 0.125)
+    np.testing.assert_array_equal(out1, out2)
+    np.testing.assert_array_equal(lse1, lse2)
+
+
+def test_split_segments_merged_by_lse_equal_one_joint_pass():
+    rng = np.random.default_rng(12)
+    p = _problem(rng, [1, 4], [300, 90], 4, 2, 64, 16)
+    scale = 0.125
+    full_out, full_lse = _run(p, scale)
+    args = (p["q"], p["kc"], p["ks"], p["vc"], p["vs"], p["cu"], p["sl"], p["bt"], scale)
+    for token, hi in ((0, 300), (3, 90)):
+        for bounds in ([0, 150, 300], [0, 64, 128, 192, 256, 300], [0, 1, 300], [0, 300, 320]):
+            parts = [oracle.attention_partial(*args, token=token, head=3, lo=a, hi=b)
+                     for a, b in zip(bounds[:-1], bounds[1:])]
+            m = [x[0] for x in parts]
+            l = [x[1] for x in parts]
+            acc = np.stack([x[2] for x in parts])
+            out, lse = oracle.merge_partials(m, l, acc)
+            r = token * 4 + 3
+            np.testing.assert_allclose(out, full_out[r], rtol=0, atol=1e-12)
+            assert abs(lse - full_lse[r]) < 1e-12
+
+
+def test_oracle_reports_bad_block_table():
+    rng = np.random.default_rng(13)
+    p = _problem(rng, [1], [40], 2, 1, 32, 16)
+    p["bt"][0, 1] = p["kc"].shape[0] + 5
+    with pytest.raises(RuntimeError):
+        _run(p, 0.1)
