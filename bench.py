@@ -1,0 +1,485 @@
+"""Benchmark of the paged q8-KV attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch: kv_store of the
+batch's new K/V rows (q8 quantize + scatter by slot) followed by
+paged_attention over the cache (unified causal prefill/decode, split-KV
+segments merged by LSE where the call splits).  The cache prefix is populated
+before timing; inputs live in HBM when the timed region starts.
+
+Default workload: the decode batch (64 sequences, one query token each, KV
+lengths uniform in [512, 8192], 32 q / 8 kv heads, D = 128, block size 16).
+Its KV cache (~0.6 GB) is larger than L2, so no flush is needed between steps.
+Metric: algorithmic HBM bytes of a step / step time (GB/s); prefill-only
+workloads report attention TFLOP/s instead.
+
+Under torchrun (N > 1) every rank runs an independent replica (seed offset by
+rank): the path has no exchange step, so there is no collective on the data
+path; the ranks meet only at the timing barriers and the max-over-ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_attention_int8_gb300 import _lib, build as pkg_build, inputs  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def step_work(w: inputs.Workload) -> dict:
+    """Algorithmic bytes and FLOPs of one step (see the design notes).
+
+    attention: every visible (row, key) pair's K and V codes + fp16 scales
+    once per kv head (sum_s L_s * Hk * 2 * (D + 2 * D/32)), plus q read, out and
+    lse written, the block-table entries used and the metadata;
+    kv_store: N * Hk * (4D read + 2(D + D/16) written) + 8N slot bytes."""
+    s = w.spec
+    G = s.d // 32
+    L = w.seq_lens.to(torch.int64)
+    T, S = w.num_tokens, w.num_seqs
+    kv = int(L.sum()) * s.hk * 2 * (s.d + 2 * G)
+    q_out = T * s.hq * s.d * 2 * 2 + T * s.hq * 4
+    pages = int(((L + s.bs - 1) // s.bs).sum()) * 4
+    meta = (2 * S + 1) * 4
+    attn_bytes = kv + q_out + pages + meta
+    n_new = int(w.new_slots.shape[0])
+    store_bytes = n_new * s.hk * (4 * s.d + 2 * (s.d + 2 * G)) + 8 * n_new
+    # visible (row, key) pairs: token i of sequence s sees ctx + i + 1 keys
+    ql = w.q_lens.to(torch.int64)
+    ctx = L - ql
+    pairs = int((ql * ctx + ql * (ql + 1) // 2).sum()) * s.hq
+    flops = 4 * s.d * pairs
+    return dict(attn_bytes=attn_bytes, store_bytes=store_bytes, step_bytes=attn_bytes + store_bytes,
+                kv_bytes=kv, flops=flops, pairs=pairs)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, if that summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"attention_{workload}.md")
+    src = os.path.join(ROOT, "paged_attention_int8_gb300", "csrc", "attention.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    rec_sha, traffic = None, None
+    for line in text.splitlines():
+        if line.startswith("source_sha256:"):
+            rec_sha = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if rec_sha == sha else None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l.split(", ") for (ts, l) in self.lines if t0 - 0.05 <= ts <= t1 + 0.05]
+        if not rows:
+            rows = [l.split(", ") for (_, l) in self.lines[-3:]]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                mx.append(float(r[3]))
+                for n, v in zip(names, r[6:10]):
+                    if v.strip() == "Active":
+                        reasons.add(n)
+            except (IndexError, ValueError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Runner:
+    def __init__(self, w: inputs.Workload, device, num_splits=None):
+        s = w.spec
+        self.w, self.device = w, device
+        self.kc, self.ks, self.vc, self.vs = inputs.empty_cache(w.num_blocks, s.hk, s.bs, s.d,
+                                                                device=device, canary=False)
+        self.status = torch.zeros(4, dtype=torch.int32, device=device)
+        # populate the cached prefix (untimed)
+        if w.prefix_key.shape[0]:
+            chunk = 1 << 18
+            for a in range(0, w.prefix_key.shape[0], chunk):
+                _lib.kv_store(w.prefix_key[a:a + chunk].to(device),
+                              w.prefix_value[a:a + chunk].to(device),
+                              w.prefix_slots[a:a + chunk].to(device),
+                              self.kc, self.ks, self.vc, self.vs, status=self.status)
+        self.new_k = w.new_key.to(device)
+        self.new_v = w.new_value.to(device)
+        self.slots = w.new_slots.to(device)
+        self.q = w.q.to(device)
+        self.cu = w.cu_seqlens_q.to(device)
+        self.seq_lens = w.seq_lens.to(device)
+        self.bt = w.block_table.to(device)
+        self.ns = s.num_splits if num_splits is None else num_splits
+        self.ns_eff = self.ns or _lib.auto_num_splits(w.num_seqs, s.hk, w.max_query_len,
+                                                      w.max_seq_len)
+        self.ws = torch.zeros(_lib.workspace_size(w.num_seqs, s.hq, s.d, self.ns_eff),
+                              dtype=torch.uint8, device=device)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((w.num_tokens, s.hq), dtype=torch.float32, device=device)
+        self.launches_per_step = 2 + (1 if self.ns_eff > 1 else 0)
+
+    def step(self, ev=None):
+        w = self.w
+        _lib.kv_store(self.new_k, self.new_v, self.slots, self.kc, self.ks, self.vc, self.vs,
+                      status=self.status)
+        if ev is not None:
+            ev[0].record()
+        _lib.paged_attention(self.q, self.kc, self.ks, self.vc, self.vs, self.cu, self.seq_lens,
+                             self.bt, w.max_query_len, w.max_seq_len, w.softmax_scale,
+                             num_splits=self.ns_eff, out=self.out, lse=self.lse,
+                             workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def check(self):
+        torch.cuda.synchronize()
+        assert _lib.check_status(self.status) == 0
+        assert _lib.check_status(self.ws) == 0
+
+
+def e2e_measure(r: Runner, steps: int, warmup: int):
+    """Same step through the public API with the step's inputs copied from
+    pinned host memory and the outputs read back, all inside the timed region."""
+    w = r.w
+    host_in = [t.pin_memory() for t in (w.q, w.new_key, w.new_value, w.new_slots,
+                                        w.cu_seqlens_q, w.seq_lens, w.block_table)]
+    dev_in = [r.q, r.new_k, r.new_v, r.slots, r.cu, r.seq_lens, r.bt]
+    host_out = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
+    host_lse = torch.empty(r.lse.shape, dtype=r.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * 2 + host_lse.numel() * 4
+
+    def one():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        r.step()
+        host_out.copy_(r.out, non_blocking=True)
+        host_lse.copy_(r.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_state(w: inputs.Workload):
+    import oracle
+    s = w.spec
+    kc, ks, vc, vs = [t.numpy() for t in inputs.empty_cache(w.num_blocks, s.hk, s.bs, s.d,
+                                                            canary=False)]
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    if w.prefix_key.shape[0]:
+        oracle.kv_store(inputs.bf16_bits(w.prefix_key), inputs.bf16_bits(w.prefix_value),
+                        w.prefix_slots.numpy(), kc, ks, vc, vs)
+    return kc, ks, vc, vs
+
+
+def oracle_sample_step(w, caches, rows, threads):
+    """The oracle's pass over one sample: kv_store of the new rows, then
+    attention for the sampled (token, head) rows."""
+    import oracle
+    kc, ks, vc, vs = caches
+    oracle.kv_store(inputs.bf16_bits(w.new_key), inputs.bf16_bits(w.new_value),
+                    w.new_slots.numpy(), kc, ks, vc, vs, n_threads=threads)
+    oracle.paged_attention(inputs.bf16_bits(w.q), kc, ks, vc, vs, w.cu_seqlens_q.numpy(),
+                           w.seq_lens.numpy(), w.block_table.numpy(), w.softmax_scale,
+                           rows=rows, n_threads=threads)
+
+
+def sample_bytes(w, rows) -> float:
+    """Algorithmic bytes of the sampled rows: their KV bytes (per q head,
+    i.e. a share 1/qpk of the kv head's stream) plus q/out/lse."""
+    s = w.spec
+    G = s.d // 32
+    cu = w.cu_seqlens_q.numpy()
+    L = w.seq_lens.numpy()
+    ql = w.q_lens.numpy()
+    tok = rows // s.hq
+    seq = np.searchsorted(cu, tok, side="right") - 1
+    keys = (L[seq] - ql[seq]) + (tok - cu[seq]) + 1
+    qpk = s.hq // s.hk
+    kv = float(np.sum(L[seq] / ql[seq].clip(min=1))) * 2 * (s.d + 2 * G) / qpk
+    return kv + rows.shape[0] * (s.d * 4 + 4), float(np.sum(keys)) * 4 * s.d
+
+
+def cpu_baseline(w, budget_s: float = 20.0):
+    threads = os.cpu_count() or 1
+    caches = oracle_state(w)
+    rows_all = np.arange(w.num_tokens * w.spec.hq, dtype=np.int64)
+    rng = np.random.default_rng(0)
+    # calibrate on a small sample, then size the sample to the budget
+    probe = np.sort(rng.choice(rows_all, size=min(rows_all.size, 4 * threads), replace=False))
+    t0 = time.perf_counter()
+    oracle_sample_step(w, caches, probe, threads)
+    per_row = (time.perf_counter() - t0) / probe.size
+    n = int(min(rows_all.size, max(probe.size, budget_s / max(per_row, 1e-9))))
+    rows = np.sort(rng.choice(rows_all, size=n, replace=False))
+    t0 = time.perf_counter()
+    oracle_sample_step(w, caches, rows, threads)
+    dt = time.perf_counter() - t0
+    b, f = sample_bytes(w, rows)
+    store = step_work(w)["store_bytes"]
+    return {"bytes": b + store, "flops": f, "seconds": dt, "rows": int(n),
+            "rows_total": int(rows_all.size), "cores": threads}
+
+
+# ----------------------------------------------------------------------------- main
+
+METRIC = "paged q8-KV attention: decode HBM GB/s (% of peak), prefill TFLOP/s"
+
+
+def metric_for(spec: inputs.Spec):
+    """Prefill-only workloads are tensor-bound (TFLOP/s); the rest HBM-bound (GB/s)."""
+    if spec.n_prefill and not spec.n_decode and not spec.fixed_decode_lens:
+        return METRIC, "TFLOP/s", "tensor"
+    return METRIC, "GB/s", "hbm"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="decode_batch", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--num-splits", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = inputs.WORKLOADS[args.workload]
+    metric, unit, bound = metric_for(spec)
+
+    if args.impl == "reference":
+        run_reference(args, spec, metric, unit, world, rank)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        pkg_build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    w = inputs.make_workload(spec.replace(seed=spec.seed + 1000 * rank) if rank else spec)
+    work = step_work(w)
+    r = Runner(w, device, args.num_splits)
+    for _ in range(args.warmup):
+        r.step()
+    r.check()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record()
+    for i in range(args.steps):
+        r.step(ev[i])
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = clocks.stop(t_wall0, t_wall1)
+    r.check()
+    ms_total = e0.elapsed_time(e1)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    units_per_step = (work["flops"] if unit == "TFLOP/s" else work["step_bytes"]) * world
+    scale = 1e-12 if unit == "TFLOP/s" else 1e-9
+    value = units_per_step / (ms_step * 1e-3) * scale
+
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e_ms, h2d, d2h = e2e_measure(r, max(10, args.steps // 10), 5)
+        e2e = {"value": (units_per_step / world) / (e2e_ms * 1e-3) * scale, "unit": unit,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    if bound == "hbm":
+        achieved = work["attn_bytes"] / (attn_ms * 1e-3) * 1e-9
+        peak, runit = hbm_peak, "GB/s"
+    else:
+        achieved = work["flops"] / (attn_ms * 1e-3) * 1e-12
+        peak, runit = tc_peak, "TFLOP/s"
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
+                "kernel": "paged_attention call (attention_kernel + reduce_kernel)",
+                "launch_ms": round(attn_ms, 5), "peak_source": peak_src,
+                "algorithmic_per_launch": work["attn_bytes"] if bound == "hbm" else work["flops"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w)
+        cv = (cb["flops"] * 1e-12 if unit == "TFLOP/s" else cb["bytes"] * 1e-9) / cb["seconds"]
+        cpu = {"value": round(cv, 4), "unit": unit, "cores": cb["cores"], "kind": "oracle",
+               "sample": f"kv_store of the step's {int(w.new_slots.shape[0])} new rows + "
+                         f"fp64 attention of {cb['rows']} of {cb['rows_total']} (token, q head) "
+                         f"rows, {cb['seconds']:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 cache, fp16 mma, fp32 softmax", "data": "synthetic",
+            "config": {"workload": args.workload, "num_seqs": w.num_seqs,
+                       "num_tokens": w.num_tokens, "q_heads": spec.hq, "kv_heads": spec.hk,
+                       "head_dim": spec.d, "block_size": spec.bs, "max_seq_len": w.max_seq_len,
+                       "sum_kv_len": int(w.seq_lens.sum()), "num_splits": r.ns_eff,
+                       "l2": "inputs larger than L2 (no flush)"
+                       if work["kv_bytes"] > 2 * 129e6 else "L2 not flushed",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": r.launches_per_step * args.steps, "clocks": clk,
+            "step_bytes": work["step_bytes"], "step_flops": work["flops"],
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, spec, metric, unit, world, rank):
+    """The oracle as the reference arm: each step one bounded sample of the
+    workload on the host cores, sized so that warmup + steps fit ~2 minutes."""
+    if rank != 0:
+        return
+    w = inputs.make_workload(spec)
+    threads = os.cpu_count() or 1
+    caches = oracle_state(w)
+    rows_all = np.arange(w.num_tokens * spec.hq, dtype=np.int64)
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(rows_all, size=min(rows_all.size, 2 * threads), replace=False))
+    t0 = time.perf_counter()
+    oracle_sample_step(w, caches, probe, threads)
+    per_row = (time.perf_counter() - t0) / probe.size
+    budget = 120.0 / (args.steps + args.warmup)
+    n = int(min(rows_all.size, max(1, budget / max(per_row, 1e-9))))
+    rows = np.sort(rng.choice(rows_all, size=n, replace=False))
+    for _ in range(args.warmup):
+        oracle_sample_step(w, caches, rows, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(w, caches, rows, threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    b, f = sample_bytes(w, rows)
+    b += step_work(w)["store_bytes"]
+    value = (f * 1e-12 if unit == "TFLOP/s" else b * 1e-9) / dt
+    line = {"impl": "reference", "metric": metric, "value": round(value, 5), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": round(value, 5), "unit": unit, "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"{n} of {rows_all.size} (token, q head) rows per step"},
+            "e2e": {"value": round(value, 5), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

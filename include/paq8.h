@@ -1,0 +1,171 @@
+/*
+ * paq8 -- paged attention over a q8 KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  All tensors are caller-owned device buffers passed as plain
+ * pointers; the library never allocates or frees device memory, never
+ * synchronizes a stream (except pa_check_status), and launches every kernel
+ * on the stream given.  `stream` is a cudaStream_t (NULL = the legacy default
+ * stream).  bf16 and fp16 buffers are passed as raw 16-bit words.
+ *
+ * The q8 format (page "shared/attention_kit.py", `quantize_q8` and the
+ * `KVPrefix` docstring): int8 codes, one fp16 scale per (token, kv head,
+ * group of 32 consecutive channels):
+ *     s     = max(max|x| / 127, 1e-8)                 (fp32)
+ *     code  = clamp(round_half_away(x / s), -127, 127) (fp32 divide)
+ *     scale = fp16(s), round to nearest even
+ * Rounding half away from zero follows "shared/kernels/qk_quant_triton.py"
+ * (`_norm_rope_quant`).  -128 is never produced.
+ *
+ * Cache layout ("HND"; the page "attention_impl.py" allows NHD or HND per
+ * layer, this library uses HND so that one (block, kv head) page of codes and
+ * of scales is contiguous):
+ *     k_cache, v_cache : int8 [num_blocks][num_kv_heads][block_size][head_dim]
+ *     k_scale, v_scale : fp16 [num_blocks][num_kv_heads][block_size][head_dim/32]
+ * Every base pointer must be 16-byte aligned.
+ *
+ * Supported shapes: head_dim in {64, 128, 256}; block_size in {16, 32};
+ * num_q_heads % num_kv_heads == 0 with num_q_heads / num_kv_heads <= 16.
+ *
+ * Device-side checks: bad metadata found by a kernel (a slot beyond the cache,
+ * a block-table entry outside [0, num_blocks), seq_len < q_len, a
+ * cu_seqlens_q entry beyond num_tokens) never faults; the kernel skips the
+ * access and ORs a bit into a 32-bit status word in device memory, which
+ * pa_check_status reads.  The status word must start zeroed.
+ */
+#ifndef PAQ8_H
+#define PAQ8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or workspace */
+    PA_ERR_UNSUPPORTED = 2,   /* shape outside the supported list */
+    PA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    PA_ERR_DEVICE_CHECK = 4,  /* a kernel found bad metadata (status bits 0x1-0x4) */
+    PA_ERR_TIMEOUT = 5        /* a bounded device-side wait expired (status bit 0x8) */
+} pa_status;
+
+/* Bits of the device status word. */
+#define PA_DEV_BAD_SLOT  0x1u  /* kv_store: slot >= num_blocks * block_size */
+#define PA_DEV_BAD_BLOCK 0x2u  /* block_table entry outside [0, num_blocks) or past its row */
+#define PA_DEV_BAD_SEQ   0x4u  /* seq_len < q_len, or cu_seqlens_q inconsistent */
+#define PA_DEV_TIMEOUT   0x8u  /* a pipeline wait gave up after its time limit */
+
+/*
+ * kv_store -- quantize new K/V rows to q8 and scatter them into the paged
+ * cache by slot.
+ * Passage: "attention_impl.py" (fastkernels-b200), `_store_kvcache_nhd` /
+ * `StoreKVCache.forward(key, value, k_cache, v_cache, slot_mapping)`: token n
+ * goes to block slot / block_size, offset slot % block_size; slot < 0 (a
+ * padding row) is skipped.  Quantization as in the format note above.
+ *
+ *   key, value        bf16 [num_tokens][num_kv_heads][head_dim]; the head and
+ *                     channel dims contiguous, token stride given in elements
+ *                     (a multiple of 8, so each row is 16-byte aligned).
+ *   slot_mapping      int64 [num_tokens].
+ *   k_cache .. v_scale the HND caches (written).
+ *   status            device uint32 status word (may be NULL: no reporting).
+ * Slots >= num_blocks * block_size are skipped and flagged PA_DEV_BAD_SLOT.
+ * Two tokens with the same non-negative slot in one call: undefined.
+ * num_tokens == 0 is a no-op.  Returns PA_OK or an error; asynchronous.
+ */
+pa_status pa_kv_store(const void *key, int64_t key_token_stride,
+                      const void *value, int64_t value_token_stride,
+                      const int64_t *slot_mapping, int32_t num_tokens,
+                      int32_t num_kv_heads, int32_t head_dim,
+                      void *k_cache, void *k_scale, void *v_cache, void *v_scale,
+                      int32_t num_blocks, int32_t block_size,
+                      uint32_t *status, void *stream);
+
+/*
+ * Split-KV segments chosen when pa_paged_attention gets num_splits == 0, for
+ * these host-side hints (no device access).  Result in [1, 16].
+ * Passage: "triton_turboquant_unified_attention.py" launcher (16 segments by
+ * default, capped by the KV length); this library targets ~512 keys per
+ * segment.
+ */
+int32_t pa_auto_num_splits(int32_t num_seqs, int32_t num_kv_heads,
+                           int32_t max_query_len, int32_t max_seq_len);
+
+/*
+ * Bytes of workspace pa_paged_attention needs: 256 bytes of header (the
+ * status word at offset 0) plus, when num_splits > 1, fp32 partial triples
+ * [num_seqs][num_q_heads][num_splits][head_dim + 2].
+ * num_splits == 0 sizes for the largest automatic choice (16).
+ */
+size_t pa_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                         int32_t num_splits);
+
+/*
+ * paged_attention -- unified causal prefill + decode over the q8 cache.
+ * Passages: "triton_turboquant_unified_attention.py" (vLLM unified kernel
+ * and launcher: query_start_loc / seq_lens / block_table, GQA heads stacked
+ * into the row tile, in-tile dequantization, online softmax, 3D split-KV
+ * segments merged by `reduce_segments`); "attention_impl.py" torch reference
+ * paths for the causal alignment (key_offset = k_len - q_len).
+ *
+ *   q             bf16 [num_tokens][num_q_heads][head_dim], contiguous.
+ *   k_cache..     HND caches (read only).
+ *   cu_seqlens_q  int32 [num_seqs + 1]; sequence s owns query tokens
+ *                 [cu[s], cu[s+1]); cu[0] = 0, non-decreasing, cu[S] <= num_tokens.
+ *   seq_lens      int32 [num_seqs]; the KV length of sequence s INCLUDING its
+ *                 new tokens (they must already be stored).  Query i of s sees
+ *                 keys 0 .. seq_len - q_len + i (bottom-right causal).
+ *   block_table   int32 [num_seqs][block_table_stride]; logical page p of s
+ *                 lives in physical block block_table[s][p].
+ *   max_query_len, max_seq_len   host upper bounds (never synced); they steer
+ *                 the tiling and the segment length only: results are correct
+ *                 for any positive values.
+ *   softmax_scale applied to q.k before the softmax (1/sqrt(D) typically).
+ *   num_splits    0 = automatic, 1 = none, k in [2, 16] = k segments.
+ *                 Segments apply to sequences with exactly one query token
+ *                 (decode rows); longer query chunks are never split.
+ *   out           bf16 [num_tokens][num_q_heads][head_dim] (written).
+ *   lse           fp32 [num_tokens][num_q_heads] natural-log LSE of
+ *                 softmax_scale * q.k over the visible keys, or NULL.
+ *   workspace     device buffer of workspace_bytes >= pa_workspace_size(...);
+ *                 its first 4 bytes are the status word (zero it once).
+ *   flags         must be 0.
+ * Rows of tokens no sequence owns are not written.  Asynchronous.
+ * Numerics: K codes enter the QK^T product exactly (fp16 integers), each
+ * 32-channel group accumulated in fp32 and then scaled; q is rounded to fp16
+ * (exact for |q| in [2^-14, 65504]); V is dequantized to fp16 (code * scale);
+ * softmax and accumulation in fp32; the output rounded to bf16.
+ */
+pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_scale,
+                             const void *v_cache, const void *v_scale,
+                             const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                             const int32_t *block_table, int32_t block_table_stride,
+                             int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                             int32_t block_size, int32_t max_query_len, int32_t max_seq_len,
+                             float softmax_scale, int32_t num_splits,
+                             void *out, float *lse, void *workspace, size_t workspace_bytes,
+                             uint32_t flags, void *stream);
+
+/*
+ * Synchronizes `stream`, reads the device status word at `status` (a kv_store
+ * status word, or the start of an attention workspace), clears it, and maps
+ * it to PA_OK / PA_ERR_TIMEOUT (bit 0x8 set) / PA_ERR_DEVICE_CHECK (other
+ * bits).  The raw bits go to *bits_out when it is not NULL.  The only call of
+ * this library that blocks the host.
+ */
+pa_status pa_check_status(uint32_t *status, uint32_t *bits_out, void *stream);
+
+/* Static description of a status code. */
+const char *pa_status_string(pa_status s);
+
+/* Description of the last argument error on the calling thread ("" if none). */
+const char *pa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAQ8_H */

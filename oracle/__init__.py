@@ -70,7 +70,7 @@ def _load():
         lib.or_q8_quantize_group.restype = None
         lib.or_q8_quantize_rows.argtypes = [P, i64, i32, P, P]
         lib.or_q8_quantize_rows.restype = None
-        lib.or_kv_store.argtypes = [P, P, P, i64, i32, i32, P, P, P, P, i64, i32]
+        lib.or_kv_store.argtypes = [P, P, P, i64, i32, i32, P, P, P, P, i64, i32, i32]
         lib.or_kv_store.restype = i64
         lib.or_paged_attention.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
                                            P, P, i32, P, i32, f32, P, i64, P, P, i32]
@@ -134,7 +134,8 @@ def q8_quantize_rows(x_bf16_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
-def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_scale) -> int:
+def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_scale,
+             n_threads: int = 0) -> int:
     """Quantize and scatter [N, Hk, D] bf16 rows into HND caches, in place.
 
     Caches: codes [num_blocks, Hk, bs, D] int8, scales [num_blocks, Hk, bs, D/32]
@@ -154,7 +155,7 @@ def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_sc
         raise ValueError("shape mismatch")
     return int(_load().or_kv_store(_ptr(key), _ptr(value), _ptr(slots), n, hk, d,
                                    _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
-                                   _ptr(v_scale), num_blocks, bs))
+                                   _ptr(v_scale), num_blocks, bs, n_threads))
 
 
 # --------------------------------------------------------------------------- attention

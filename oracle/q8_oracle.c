@@ -183,28 +183,65 @@ void or_q8_quantize_rows(const uint16_t *x_bf16, int64_t n_rows, int32_t d,
  * Scatter ("attention_impl.py", `_store_kvcache_nhd`): slot < 0 is skipped;
  * block = slot / bs, offset = slot % bs.  A slot at or beyond
  * num_blocks * bs is skipped and counted in the return value.
+ * Tokens are independent (two tokens with one slot are undefined), so the
+ * token range is shared out over n_threads threads (<= 0: every core).
  */
+typedef struct {
+    const uint16_t *key, *value;
+    const int64_t *slot_mapping;
+    int64_t n0, n1;
+    int32_t hk, d;
+    int8_t *k_cache, *v_cache;
+    uint16_t *k_scale, *v_scale;
+    int64_t num_blocks;
+    int32_t bs;
+    int64_t bad;
+} or_store_job;
+
+static void *or_store_worker(void *arg)
+{
+    or_store_job *j = (or_store_job *)arg;
+    int32_t groups = j->d / OR_GROUP;
+    for (int64_t n = j->n0; n < j->n1; ++n) {
+        int64_t slot = j->slot_mapping[n];
+        if (slot < 0) continue;
+        if (slot >= j->num_blocks * j->bs) { ++j->bad; continue; }
+        int64_t block = slot / j->bs;
+        int64_t offset = slot % j->bs;
+        for (int32_t h = 0; h < j->hk; ++h) {
+            int64_t row = (block * j->hk + h) * j->bs + offset;     /* HND row */
+            const uint16_t *ks = j->key + (n * j->hk + h) * (int64_t)j->d;
+            const uint16_t *vs = j->value + (n * j->hk + h) * (int64_t)j->d;
+            or_q8_quantize_rows(ks, 1, j->d, j->k_cache + row * j->d, j->k_scale + row * groups);
+            or_q8_quantize_rows(vs, 1, j->d, j->v_cache + row * j->d, j->v_scale + row * groups);
+        }
+    }
+    return NULL;
+}
+
 int64_t or_kv_store(const uint16_t *key, const uint16_t *value,
                     const int64_t *slot_mapping, int64_t n_tokens, int32_t hk,
                     int32_t d, int8_t *k_cache, uint16_t *k_scale,
                     int8_t *v_cache, uint16_t *v_scale, int64_t num_blocks,
-                    int32_t bs)
+                    int32_t bs, int32_t n_threads)
 {
+    if (n_threads <= 0) n_threads = (int32_t)sysconf(_SC_NPROCESSORS_ONLN);
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 512) n_threads = 512;
+    if (n_tokens < (int64_t)n_threads * 64) n_threads = 1;
+    or_store_job jobs[512];
+    pthread_t tids[512];
+    for (int32_t i = 0; i < n_threads; ++i) {
+        or_store_job j = {key, value, slot_mapping, n_tokens * i / n_threads,
+                          n_tokens * (i + 1) / n_threads, hk, d, k_cache, v_cache,
+                          k_scale, v_scale, num_blocks, bs, 0};
+        jobs[i] = j;
+    }
+    for (int32_t i = 0; i < n_threads; ++i) pthread_create(&tids[i], NULL, or_store_worker, &jobs[i]);
     int64_t bad = 0;
-    int32_t groups = d / OR_GROUP;
-    for (int64_t n = 0; n < n_tokens; ++n) {
-        int64_t slot = slot_mapping[n];
-        if (slot < 0) continue;
-        if (slot >= num_blocks * bs) { ++bad; continue; }
-        int64_t block = slot / bs;
-        int64_t offset = slot % bs;
-        for (int32_t h = 0; h < hk; ++h) {
-            int64_t row = (block * hk + h) * bs + offset;     /* HND row */
-            const uint16_t *ks = key + (n * hk + h) * (int64_t)d;
-            const uint16_t *vs = value + (n * hk + h) * (int64_t)d;
-            or_q8_quantize_rows(ks, 1, d, k_cache + row * d, k_scale + row * groups);
-            or_q8_quantize_rows(vs, 1, d, v_cache + row * d, v_scale + row * groups);
-        }
+    for (int32_t i = 0; i < n_threads; ++i) {
+        pthread_join(tids[i], NULL);
+        bad += jobs[i].bad;
     }
     return bad;
 }

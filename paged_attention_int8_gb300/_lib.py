@@ -1,0 +1,224 @@
+"""ctypes binding of libpaq8.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+turns torch tensors into pointers, sizes and the current CUDA stream, calls
+the C ABI declared in include/paq8.h, and raises on an error status.  There
+is no fallback: if the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libpaq8.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED = 2
+    CUDA = 3
+    DEVICE_CHECK = 4
+    TIMEOUT = 5
+
+
+DEV_BAD_SLOT = 0x1
+DEV_BAD_BLOCK = 0x2
+DEV_BAD_SEQ = 0x4
+DEV_TIMEOUT = 0x8
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, message: str, bits: int = 0):
+        super().__init__(f"{Status(status).name}: {message}")
+        self.status = Status(status)
+        self.bits = bits
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libpaq8.so (built by paged_attention_int8_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libpaq8.so not built ({_LIB_PATH}); run "
+                "`python -m paged_attention_int8_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.pa_kv_store.argtypes = [P, i64, P, i64, P, i32, i32, i32, P, P, P, P, i32, i32, P, P]
+        lib.pa_kv_store.restype = ctypes.c_int
+        lib.pa_auto_num_splits.argtypes = [i32, i32, i32, i32]
+        lib.pa_auto_num_splits.restype = i32
+        lib.pa_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.pa_workspace_size.restype = ctypes.c_size_t
+        lib.pa_paged_attention.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                           i32, i32, i32, i32, ctypes.c_float, i32, P, P, P,
+                                           ctypes.c_size_t, ctypes.c_uint32, P]
+        lib.pa_paged_attention.restype = ctypes.c_int
+        lib.pa_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+        lib.pa_check_status.restype = ctypes.c_int
+        lib.pa_status_string.argtypes = [ctypes.c_int]
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_last_error.argtypes = []
+        lib.pa_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _raise_if(status: int):
+    if status != Status.OK:
+        lib = load()
+        msg = lib.pa_last_error().decode() or lib.pa_status_string(status).decode()
+        raise PagedAttentionError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(*tensors):
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+
+
+def _check16(name, t):
+    if t.element_size() != 2:
+        raise TypeError(f"{name} must hold 16-bit elements (fp16 scales)")
+
+
+# ----------------------------------------------------------------------------- API
+
+def kv_store(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, status=None,
+             stream=None) -> None:
+    """Quantize key/value rows [N, Hk, D] (bf16) to q8 and scatter them by
+    ``slot_mapping`` (int64 [N]; slot < 0 skipped) into the HND caches
+    ``k_cache``/``v_cache`` (int8 [num_blocks, Hk, bs, D]) and
+    ``k_scale``/``v_scale`` ([num_blocks, Hk, bs, D/32], fp16 or int16 bits).
+    ``status``: optional int32 CUDA tensor (>= 1 element, zeroed) for device checks."""
+    _check_cuda(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, status)
+    if key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
+        raise TypeError("key and value must be bf16")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if k_cache.dtype != torch.int8 or v_cache.dtype != torch.int8:
+        raise TypeError("caches must be int8")
+    _check16("k_scale", k_scale)
+    _check16("v_scale", v_scale)
+    n, hk, d = key.shape
+    if value.shape != key.shape or slot_mapping.shape != (n,):
+        raise ValueError("key/value/slot_mapping shapes differ")
+    for t in (key, value):
+        if t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError("key/value head and channel dims must be contiguous")
+    num_blocks, hk2, bs, d2 = k_cache.shape
+    if (hk2, d2) != (hk, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if k_scale.shape != (num_blocks, hk, bs, d // 32) or v_scale.shape != k_scale.shape:
+        raise ValueError("scale shape mismatch")
+    for t in (k_cache, v_cache, k_scale, v_scale, slot_mapping):
+        if not t.is_contiguous():
+            raise ValueError("caches and slot_mapping must be contiguous")
+    lib = load()
+    st = lib.pa_kv_store(_ptr(key), key.stride(0), _ptr(value), value.stride(0),
+                         _ptr(slot_mapping), n, hk, d, _ptr(k_cache), _ptr(k_scale),
+                         _ptr(v_cache), _ptr(v_scale), num_blocks, bs, _ptr(status),
+                         _stream(stream))
+    _raise_if(st)
+
+
+def auto_num_splits(num_seqs: int, num_kv_heads: int, max_query_len: int,
+                    max_seq_len: int) -> int:
+    return int(load().pa_auto_num_splits(num_seqs, num_kv_heads, max_query_len, max_seq_len))
+
+
+def workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, num_splits: int = 0) -> int:
+    return int(load().pa_workspace_size(num_seqs, num_q_heads, head_dim, num_splits))
+
+
+def paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
+                    max_query_len: int, max_seq_len: int, softmax_scale: float | None = None,
+                    num_splits: int = 0, out=None, lse=None, workspace=None, stream=None,
+                    return_lse: bool = True):
+    """Unified causal paged attention over the q8 cache.
+
+    q [T, Hq, D] bf16; cu_seqlens_q int32 [S+1]; seq_lens int32 [S] (KV length
+    including the new tokens); block_table int32 [S, max_blocks].
+    ``max_query_len`` / ``max_seq_len`` are host-side upper bounds (no sync).
+    Returns (out bf16 [T, Hq, D], lse fp32 [T, Hq]) or out alone when
+    ``return_lse`` is False.  ``workspace``: optional uint8 CUDA tensor of at
+    least ``workspace_size(S, Hq, D, num_splits)`` bytes whose first 4 bytes
+    are zero (the device status word); allocated zeroed when omitted."""
+    _check_cuda(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
+                out, lse, workspace)
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise TypeError("q must be a contiguous bf16 tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens", seq_lens),
+                    ("block_table", block_table)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    if not (cu_seqlens_q.is_contiguous() and seq_lens.is_contiguous()):
+        raise ValueError("cu_seqlens_q and seq_lens must be contiguous")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [S, max_blocks] with unit column stride")
+    _check16("k_scale", k_scale)
+    _check16("v_scale", v_scale)
+    T, hq, d = q.shape
+    num_blocks, hk, bs, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape mismatch")
+    S = seq_lens.shape[0]
+    if cu_seqlens_q.shape != (S + 1,) or block_table.shape[0] != S:
+        raise ValueError("metadata shapes disagree with seq_lens")
+    if softmax_scale is None:
+        softmax_scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    lib = load()
+    need = int(lib.pa_workspace_size(S, hq, d, num_splits))
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    st = lib.pa_paged_attention(_ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
+                                _ptr(v_scale), _ptr(cu_seqlens_q), _ptr(seq_lens),
+                                _ptr(block_table), block_table.stride(0), S, T, hq, hk, d,
+                                num_blocks, bs, int(max_query_len), int(max_seq_len),
+                                float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                0, _stream(stream))
+    _raise_if(st)
+    return (out, lse) if return_lse else out
+
+
+def check_status(status_tensor, stream=None) -> int:
+    """Synchronize, read and clear a device status word (a kv_store status
+    tensor or an attention workspace).  Returns the raw bits; raises
+    PagedAttentionError when any bit is set."""
+    lib = load()
+    bits = ctypes.c_uint32(0)
+    st = lib.pa_check_status(_ptr(status_tensor), ctypes.byref(bits), _stream(stream))
+    if st == Status.CUDA:
+        _raise_if(st)
+    if st != Status.OK:
+        raise PagedAttentionError(st, lib.pa_status_string(st).decode(), bits.value)
+    return bits.value

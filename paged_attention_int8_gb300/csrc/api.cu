@@ -1,0 +1,183 @@
+// C ABI of libpaq8: argument validation and dispatch.  Every entry point is
+// declared, with its contract, in include/paq8.h.
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+pa_status fail(pa_status s, const char *msg) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+  return s;
+}
+
+pa_status cuda_fail(cudaError_t e) {
+  std::snprintf(g_last_error, sizeof g_last_error, "CUDA: %s", cudaGetErrorString(e));
+  return PA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dim(int32_t d) { return d == 64 || d == 128 || d == 256; }
+bool supported_bs(int32_t bs) { return bs == 16 || bs == 32; }
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_kv_store(const void *key, int64_t key_token_stride, const void *value,
+                      int64_t value_token_stride, const int64_t *slot_mapping,
+                      int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                      void *k_cache, void *k_scale, void *v_cache, void *v_scale,
+                      int32_t num_blocks, int32_t block_size, uint32_t *status, void *stream) {
+  g_last_error[0] = '\0';
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !slot_mapping || !k_cache || !k_scale || !v_cache || !v_scale)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be positive");
+  if (!supported_dim(head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (!supported_bs(block_size)) return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32");
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row)
+    return fail(PA_ERR_INVALID_ARG, "token stride smaller than num_kv_heads * head_dim");
+  if (key_token_stride % 8 || value_token_stride % 8 || !aligned16(key) || !aligned16(value))
+    return fail(PA_ERR_INVALID_ARG, "key/value rows must be 16-byte aligned");
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) || !aligned16(v_scale))
+    return fail(PA_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size >= (int64_t{1} << 31))
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * block_size must be < 2^31");
+  cudaError_t e = paq8::launch_kv_store(
+      static_cast<const uint16_t *>(key), key_token_stride, static_cast<const uint16_t *>(value),
+      value_token_stride, slot_mapping, num_tokens, num_kv_heads, head_dim,
+      static_cast<int8_t *>(k_cache), static_cast<uint16_t *>(k_scale),
+      static_cast<int8_t *>(v_cache), static_cast<uint16_t *>(v_scale), num_blocks, block_size,
+      status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int32_t pa_auto_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_query_len,
+                           int32_t max_seq_len) {
+  return paq8::auto_num_splits(num_seqs, num_kv_heads, max_query_len, max_seq_len);
+}
+
+size_t pa_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                         int32_t num_splits) {
+  if (num_seqs < 0 || num_q_heads < 0 || head_dim < 0 || num_splits < 0) return 0;
+  const int32_t ns = num_splits == 0 ? 16 : num_splits;
+  size_t bytes = 256;
+  if (ns > 1)
+    bytes += static_cast<size_t>(num_seqs) * num_q_heads * ns * (head_dim + 2) * sizeof(float);
+  return bytes;
+}
+
+pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_scale,
+                             const void *v_cache, const void *v_scale,
+                             const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                             const int32_t *block_table, int32_t block_table_stride,
+                             int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                             int32_t block_size, int32_t max_query_len, int32_t max_seq_len,
+                             float softmax_scale, int32_t num_splits, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, uint32_t flags,
+                             void *stream) {
+  g_last_error[0] = '\0';
+  if (flags != 0) return fail(PA_ERR_INVALID_ARG, "flags must be 0");
+  if (num_seqs < 0 || num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+  if (!workspace) return fail(PA_ERR_INVALID_ARG, "null workspace");
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (!q || !k_cache || !k_scale || !v_cache || !v_scale || !cu_seqlens_q || !seq_lens ||
+      !block_table || !out)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (num_q_heads / num_kv_heads > 16)
+    return fail(PA_ERR_UNSUPPORTED, "more than 16 q heads per kv head");
+  if (!supported_dim(head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (!supported_bs(block_size)) return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32");
+  if (num_blocks <= 0 || block_table_stride <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_blocks and block_table_stride must be positive");
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size >= (int64_t{1} << 31))
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * block_size must be < 2^31");
+  if (max_query_len <= 0 || max_seq_len <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_query_len and max_seq_len must be positive");
+  if (num_splits < 0 || num_splits > 16) return fail(PA_ERR_INVALID_ARG, "num_splits in [0, 16]");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_scale) || !aligned16(v_scale) || !aligned16(workspace))
+    return fail(PA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  int32_t ns = num_splits == 0
+                   ? paq8::auto_num_splits(num_seqs, num_kv_heads, max_query_len, max_seq_len)
+                   : num_splits;
+  if (workspace_bytes < pa_workspace_size(num_seqs, num_q_heads, head_dim, ns)) {
+    if (num_splits != 0) return fail(PA_ERR_INVALID_ARG, "workspace too small for num_splits");
+    while (ns > 1 && workspace_bytes < pa_workspace_size(num_seqs, num_q_heads, head_dim, ns))
+      --ns;
+    if (workspace_bytes < pa_workspace_size(num_seqs, num_q_heads, head_dim, ns))
+      return fail(PA_ERR_INVALID_ARG, "workspace smaller than 256 bytes");
+  }
+  paq8::AttnLaunch L;
+  L.q = q;
+  L.k_cache = k_cache;
+  L.k_scale = k_scale;
+  L.v_cache = v_cache;
+  L.v_scale = v_scale;
+  L.cu = cu_seqlens_q;
+  L.seq_lens = seq_lens;
+  L.block_table = block_table;
+  L.bt_stride = block_table_stride;
+  L.num_seqs = num_seqs;
+  L.num_tokens = num_tokens;
+  L.hq = num_q_heads;
+  L.hk = num_kv_heads;
+  L.d = head_dim;
+  L.num_blocks = num_blocks;
+  L.bs = block_size;
+  L.max_query_len = max_query_len;
+  L.max_seq_len = max_seq_len;
+  L.num_splits = ns;
+  L.softmax_scale = softmax_scale;
+  L.out = out;
+  L.lse = lse;
+  L.workspace = static_cast<uint8_t *>(workspace);
+  cudaError_t e = paq8::launch_paged_attention(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_check_status(uint32_t *status, uint32_t *bits_out, void *stream) {
+  if (!status) return fail(PA_ERR_INVALID_ARG, "null status pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  cudaError_t e = cudaMemcpyAsync(&bits, status, sizeof bits, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && bits) e = cudaMemsetAsync(status, 0, sizeof bits, s);
+  if (e == cudaSuccess && bits) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (bits_out) *bits_out = bits;
+  if (bits & PA_DEV_TIMEOUT) return PA_ERR_TIMEOUT;
+  if (bits) return PA_ERR_DEVICE_CHECK;
+  return PA_OK;
+}
+
+const char *pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_DEVICE_CHECK: return "device-side metadata check failed";
+    case PA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char *pa_last_error(void) { return g_last_error; }
+
+}  // extern "C"

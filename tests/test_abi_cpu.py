@@ -1,0 +1,133 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry
+point that include/paq8.h declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_attention_int8_gb300 import _lib, build as pkg_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "paq8.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg_build.build()
+    return _lib.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("pa_kv_store", "pa_paged_attention", "pa_workspace_size", "pa_check_status",
+              "pa_status_string", "pa_auto_num_splits", "pa_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (pa_\w+)", out))
+    for name in _declared():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for s in _lib.Status:
+        assert lib.pa_status_string(int(s)).decode()
+
+
+def test_workspace_size_formula(lib):
+    # 256-byte header, plus fp32 [S, Hq, NS, D + 2] partials when splitting
+    assert lib.pa_workspace_size(64, 32, 128, 1) == 256
+    assert lib.pa_workspace_size(64, 32, 128, 16) == 256 + 64 * 32 * 16 * 130 * 4
+    assert lib.pa_workspace_size(8, 32, 256, 0) == 256 + 8 * 32 * 16 * 258 * 4
+
+
+def test_auto_splits_range(lib):
+    for L in (1, 64, 511, 512, 513, 8192, 131072):
+        ns = lib.pa_auto_num_splits(64, 8, 1, L)
+        assert 1 <= ns <= 16
+    assert lib.pa_auto_num_splits(8, 8, 1, 131072) == 16
+    assert lib.pa_auto_num_splits(2, 2, 1, 100) == 1
+
+
+def _store_args(**kw):
+    a = dict(key=16, kstride=256, value=16, vstride=256, slots=16, n=4, hk=2, d=128,
+             kc=16, ks=16, vc=16, vs=16, nb=4, bs=16, status=None, stream=None)
+    a.update(kw)
+    v = lambda x: ctypes.c_void_p(x) if x is not None else None  # noqa: E731
+    return [v(a["key"]), a["kstride"], v(a["value"]), a["vstride"], v(a["slots"]), a["n"],
+            a["hk"], a["d"], v(a["kc"]), v(a["ks"]), v(a["vc"]), v(a["vs"]), a["nb"], a["bs"],
+            v(a["status"]), v(a["stream"])]
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(key=None), _lib.Status.INVALID_ARG),
+    (dict(n=-1), _lib.Status.INVALID_ARG),
+    (dict(d=96), _lib.Status.UNSUPPORTED),
+    (dict(bs=8), _lib.Status.UNSUPPORTED),
+    (dict(kstride=100), _lib.Status.INVALID_ARG),
+    (dict(key=24), _lib.Status.INVALID_ARG),
+    (dict(kc=8), _lib.Status.INVALID_ARG),
+    (dict(nb=0), _lib.Status.INVALID_ARG),
+])
+def test_kv_store_rejects_bad_arguments(lib, kw, expect):
+    assert lib.pa_kv_store(*_store_args(**kw)) == expect
+    assert lib.pa_last_error().decode()
+
+
+def test_kv_store_zero_tokens_is_a_no_op(lib):
+    assert lib.pa_kv_store(*_store_args(n=0, key=None)) == _lib.Status.OK
+
+
+def _attn_args(**kw):
+    a = dict(q=16, kc=16, ks=16, vc=16, vs=16, cu=16, sl=16, bt=16, bts=8, S=2, T=2, hq=8,
+             hk=2, d=128, nb=16, bs=16, mq=1, ms=100, scale=0.1, ns=1, out=16, lse=16, ws=16,
+             wsb=256, flags=0, stream=None)
+    a.update(kw)
+    v = lambda x: ctypes.c_void_p(x) if x is not None else None  # noqa: E731
+    return [v(a["q"]), v(a["kc"]), v(a["ks"]), v(a["vc"]), v(a["vs"]), v(a["cu"]), v(a["sl"]),
+            v(a["bt"]), a["bts"], a["S"], a["T"], a["hq"], a["hk"], a["d"], a["nb"], a["bs"],
+            a["mq"], a["ms"], ctypes.c_float(a["scale"]), a["ns"], v(a["out"]), v(a["lse"]),
+            v(a["ws"]), a["wsb"], a["flags"], v(a["stream"])]
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(flags=1), _lib.Status.INVALID_ARG),
+    (dict(ws=None), _lib.Status.INVALID_ARG),
+    (dict(q=None), _lib.Status.INVALID_ARG),
+    (dict(hq=7), _lib.Status.INVALID_ARG),
+    (dict(hq=34, hk=2), _lib.Status.UNSUPPORTED),
+    (dict(d=80), _lib.Status.UNSUPPORTED),
+    (dict(bs=64), _lib.Status.UNSUPPORTED),
+    (dict(mq=0), _lib.Status.INVALID_ARG),
+    (dict(ns=17), _lib.Status.INVALID_ARG),
+    (dict(ns=4, wsb=256), _lib.Status.INVALID_ARG),
+    (dict(out=8), _lib.Status.INVALID_ARG),
+    (dict(bts=0), _lib.Status.INVALID_ARG),
+    (dict(nb=1 << 30), _lib.Status.UNSUPPORTED),
+])
+def test_paged_attention_rejects_bad_arguments(lib, kw, expect):
+    assert lib.pa_paged_attention(*_attn_args(**kw)) == expect
+
+
+def test_paged_attention_empty_batch_is_a_no_op(lib):
+    assert lib.pa_paged_attention(*_attn_args(S=0, T=0, q=None)) == _lib.Status.OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.load()
