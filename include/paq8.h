@@ -158,6 +158,36 @@ pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_s
  */
 pa_status pa_check_status(uint32_t *status, uint32_t *bits_out, void *stream);
 
+/*
+ * Allocation-free variant of pa_paged_attention.  The paper has no
+ * counterpart to this call; it is an integration convenience.  For callers
+ * that cannot call cudaMalloc: plugins run inside another framework's executor where
+ * allocation is forbidden, serving loops that must never wait on the
+ * allocator, fixed-budget embeddings.  Arguments as pa_paged_attention,
+ * except that there is no workspace: the split-KV partials live in a
+ * file-scope device array of 8 MiB that every GPU loading the library holds
+ * until exit.  The caller still passes inputs and outputs.
+ *   status  optional device uint32: receives this call's status bits
+ *           (overwritten, not OR-ed); NULL = no reporting.
+ * A num_splits > 1 whose partials exceed 8 MiB is rejected
+ * (PA_ERR_INVALID_ARG); num_splits == 0 picks the largest automatic count that
+ * fits.  The first call on a device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the one array: calls that overlap on the GPU (other
+ * streams, other threads) race and give wrong results; serialize them.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ */
+pa_status pa_paged_attention_noalloc(const void *q, const void *k_cache, const void *k_scale,
+                                     const void *v_cache, const void *v_scale,
+                                     const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                     const int32_t *block_table, int32_t block_table_stride,
+                                     int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                     int32_t block_size, int32_t max_query_len,
+                                     int32_t max_seq_len, float softmax_scale,
+                                     int32_t num_splits, void *out, float *lse,
+                                     uint32_t *status, void *stream);
+
 /* Static description of a status code. */
 const char *pa_status_string(pa_status s);
 

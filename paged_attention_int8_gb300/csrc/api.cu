@@ -2,6 +2,7 @@
 // declared, with its contract, in include/paq8.h.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -181,3 +182,82 @@ const char *pa_status_string(pa_status s) {
 const char *pa_last_error(void) { return g_last_error; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free paged attention.
+//
+// Some callers cannot call cudaMalloc: a plugin run inside another
+// framework's executor that forbids allocation on its hot path, a serving
+// loop that must never wait on the allocator (cudaMalloc can synchronize the
+// device), or an embedding with a fixed memory budget.  For them the split-KV
+// scratch comes from this file-scope device array instead of a caller
+// workspace.  Every GPU that loads the library holds it until the process
+// exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t{8} << 20;  // 8 MiB per device
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's
+// name is only a host-side stand-in in host code, so the address is looked up
+// once per device, with that device current.
+pa_status noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device index >= 64");
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_paged_attention_noalloc(
+    const void *q, const void *k_cache, const void *k_scale, const void *v_cache,
+    const void *v_scale, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+    const int32_t *block_table, int32_t block_table_stride, int32_t num_seqs,
+    int32_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t num_blocks, int32_t block_size, int32_t max_query_len, int32_t max_seq_len,
+    float softmax_scale, int32_t num_splits, void *out, float *lse, uint32_t *status,
+    void *stream) {
+  g_last_error[0] = '\0';
+  if (num_splits > 1 &&
+      pa_workspace_size(num_seqs, num_q_heads, head_dim, num_splits) > kNoAllocScratchBytes) {
+    char msg[160];
+    std::snprintf(msg, sizeof msg,
+                  "num_splits=%d needs %zu bytes of split scratch; the static scratch holds %zu",
+                  num_splits, pa_workspace_size(num_seqs, num_q_heads, head_dim, num_splits),
+                  kNoAllocScratchBytes);
+    return fail(PA_ERR_INVALID_ARG, msg);
+  }
+  void *scratch = nullptr;
+  pa_status st = noalloc_scratch(&scratch);
+  if (st != PA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The scratch keeps the previous call's contents: its status word must
+  // start at zero; the split partials are always written before they are read.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  st = pa_paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
+                          block_table, block_table_stride, num_seqs, num_tokens, num_q_heads,
+                          num_kv_heads, head_dim, num_blocks, block_size, max_query_len,
+                          max_seq_len, softmax_scale, num_splits, out, lse, scratch,
+                          kNoAllocScratchBytes, 0, stream);
+  if (st != PA_OK) return st;
+  if (status) {
+    e = cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return PA_OK;
+}
