@@ -16,12 +16,17 @@
  * Rounding half away from zero follows "shared/kernels/qk_quant_triton.py"
  * (`_norm_rope_quant`).  -128 is never produced.
  *
- * Cache layout ("HND"; the page "attention_impl.py" allows NHD or HND per
- * layer, this library uses HND so that one (block, kv head) page of codes and
- * of scales is contiguous):
- *     k_cache, v_cache : int8 [num_blocks][num_kv_heads][block_size][head_dim]
- *     k_scale, v_scale : fp16 [num_blocks][num_kv_heads][block_size][head_dim/32]
- * Every base pointer must be 16-byte aligned.
+ * Cache layout (head-major pages, "HND"; the page "attention_impl.py" allows
+ * NHD or HND per layer).  One (block, kv head) page of codes and of scales is
+ * contiguous; K pages are token-major, V pages channel-major (a V page is the
+ * transpose of its token rows, so that 4 consecutive keys of one channel are
+ * one 32-bit word for the PV product):
+ *     k_cache : int8 [num_blocks][num_kv_heads][block_size][head_dim]
+ *     k_scale : fp16 [num_blocks][num_kv_heads][block_size][head_dim/32]
+ *     v_cache : int8 [num_blocks][num_kv_heads][head_dim][block_size]
+ *     v_scale : fp16 [num_blocks][num_kv_heads][head_dim/32][block_size]
+ * Every base pointer must be 16-byte aligned;
+ * num_blocks * num_kv_heads * head_dim must be below 2^31.
  *
  * Supported shapes: head_dim in {64, 128, 256}; block_size in {16, 32};
  * num_q_heads % num_kv_heads == 0 with num_q_heads / num_kv_heads <= 16.
@@ -87,7 +92,7 @@ pa_status pa_kv_store(const void *key, int64_t key_token_stride,
  * Split-KV segments chosen when pa_paged_attention gets num_splits == 0, for
  * these host-side hints (no device access).  Result in [1, 16].
  * Passage: "triton_turboquant_unified_attention.py" launcher (16 segments by
- * default, capped by the KV length); this library targets ~512 keys per
+ * default, capped by the KV length); this library targets ~2048 keys per
  * segment.
  */
 int32_t pa_auto_num_splits(int32_t num_seqs, int32_t num_kv_heads,
@@ -119,9 +124,12 @@ size_t pa_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim
  *                 keys 0 .. seq_len - q_len + i (bottom-right causal).
  *   block_table   int32 [num_seqs][block_table_stride]; logical page p of s
  *                 lives in physical block block_table[s][p].
- *   max_query_len, max_seq_len   host upper bounds (never synced); they steer
- *                 the tiling and the segment length only: results are correct
- *                 for any positive values.
+ *   max_query_len host upper bound on every q_len (never synced).  With 1 the
+ *                 call takes the decode-only path; a sequence with more query
+ *                 tokens is then left unprocessed and flagged PA_DEV_BAD_SEQ.
+ *   max_seq_len   host hint for the segment length only; any positive value
+ *                 gives correct results (a sequence longer than the hint just
+ *                 gets a longer last segment).
  *   softmax_scale applied to q.k before the softmax (1/sqrt(D) typically).
  *   num_splits    0 = automatic, 1 = none, k in [2, 16] = k segments.
  *                 Segments apply to sequences with exactly one query token

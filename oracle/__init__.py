@@ -85,6 +85,15 @@ def _load():
         return lib
 
 
+def _check_cache(kc, ks, vc, vs):
+    nb, hk, bs, d = kc.shape
+    if d > 1024 or d % 32:
+        raise ValueError("head_dim must be a multiple of 32, at most 1024")
+    want = ((nb, hk, bs, d // 32), (nb, hk, d, bs), (nb, hk, d // 32, bs))
+    if (ks.shape, vc.shape, vs.shape) != want:
+        raise ValueError(f"cache shapes {ks.shape, vc.shape, vs.shape} != {want}")
+
+
 def _ptr(a: np.ndarray):
     return ctypes.c_void_p(a.ctypes.data)
 
@@ -136,10 +145,12 @@ def q8_quantize_rows(x_bf16_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
 
 def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_scale,
              n_threads: int = 0) -> int:
-    """Quantize and scatter [N, Hk, D] bf16 rows into HND caches, in place.
+    """Quantize and scatter [N, Hk, D] bf16 rows into the caches, in place.
 
-    Caches: codes [num_blocks, Hk, bs, D] int8, scales [num_blocks, Hk, bs, D/32]
-    uint16 (fp16 bits).  Returns the number of skipped out-of-range slots."""
+    K: codes [num_blocks, Hk, bs, D] int8, scales [num_blocks, Hk, bs, D/32]
+    uint16 (fp16 bits).  V pages channel-major: codes [num_blocks, Hk, D, bs],
+    scales [num_blocks, Hk, D/32, bs].  Returns the number of skipped
+    out-of-range slots."""
     key = _c(key_bits, np.uint16)
     value = _c(value_bits, np.uint16)
     slots = _c(slot_mapping, np.int64)
@@ -153,6 +164,7 @@ def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_sc
     num_blocks, hk2, bs, d2 = k_cache.shape
     if (hk2, d2) != (hk, d) or value.shape != key.shape or slots.shape != (n,):
         raise ValueError("shape mismatch")
+    _check_cache(k_cache, k_scale, v_cache, v_scale)
     return int(_load().or_kv_store(_ptr(key), _ptr(value), _ptr(slots), n, hk, d,
                                    _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
                                    _ptr(v_scale), num_blocks, bs, n_threads))
@@ -170,8 +182,9 @@ def _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
     bt = _c(block_table, np.int32)
     T, hq, d = q.shape
     num_blocks, hk, bs, d2 = kc.shape
-    if d2 != d or vc.shape != kc.shape or hq % hk:
+    if d2 != d or hq % hk:
         raise ValueError("shape mismatch")
+    _check_cache(kc, ks, vc, vs)
     S = sl.shape[0]
     if cu.shape != (S + 1,) or bt.ndim != 2 or bt.shape[0] != S:
         raise ValueError("metadata shape mismatch")

@@ -35,8 +35,9 @@
  *  - the scale floor is 1e-8 (fp32), and FP16 conversion is round to nearest
  *    even;
  *  - the LSE is the natural log of sum_j exp(scale * q.k_j);
- *  - caches are HND: codes [num_blocks, Hk, block_size, D] int8, scales
- *    [num_blocks, Hk, block_size, D/32] fp16.
+ *  - caches are HND: K codes [num_blocks, Hk, block_size, D] int8, K scales
+ *    [num_blocks, Hk, block_size, D/32] fp16; V pages channel-major, codes
+ *    [num_blocks, Hk, D, block_size], scales [num_blocks, Hk, D/32, block_size].
  */
 #include <math.h>
 #include <pthread.h>
@@ -178,8 +179,10 @@ void or_q8_quantize_rows(const uint16_t *x_bf16, int64_t n_rows, int32_t d,
 
 /*
  * key, value: [n_tokens, hk, d] bf16 bits, contiguous.
- * Caches (HND): codes [num_blocks, hk, bs, d] int8; scales
- * [num_blocks, hk, bs, d/32] fp16 bits.
+ * K cache (HND): codes [num_blocks, hk, bs, d] int8, scales
+ * [num_blocks, hk, bs, d/32] fp16 bits.  V cache: the same pages stored
+ * channel-major, codes [num_blocks, hk, d, bs], scales
+ * [num_blocks, hk, d/32, bs] (a layout reading; the values are the same).
  * Scatter ("attention_impl.py", `_store_kvcache_nhd`): slot < 0 is skipped;
  * block = slot / bs, offset = slot % bs.  A slot at or beyond
  * num_blocks * bs is skipped and counted in the return value.
@@ -213,7 +216,15 @@ static void *or_store_worker(void *arg)
             const uint16_t *ks = j->key + (n * j->hk + h) * (int64_t)j->d;
             const uint16_t *vs = j->value + (n * j->hk + h) * (int64_t)j->d;
             or_q8_quantize_rows(ks, 1, j->d, j->k_cache + row * j->d, j->k_scale + row * groups);
-            or_q8_quantize_rows(vs, 1, j->d, j->v_cache + row * j->d, j->v_scale + row * groups);
+            /* V: quantize the row, then place channel c at page row c */
+            int8_t vcodes[1024];
+            uint16_t vscales[32];
+            or_q8_quantize_rows(vs, 1, j->d, vcodes, vscales);
+            int64_t page = block * j->hk + h;
+            for (int32_t c = 0; c < j->d; ++c)
+                j->v_cache[(page * j->d + c) * j->bs + offset] = vcodes[c];
+            for (int32_t g = 0; g < groups; ++g)
+                j->v_scale[(page * groups + g) * j->bs + offset] = vscales[g];
         }
     }
     return NULL;
@@ -280,14 +291,24 @@ static int64_t or_kv_row(const or_problem *p, int32_t s, int32_t h, int64_t j)
     return (blk * p->hk + h) * p->bs + off;
 }
 
-/* Dequantized channel c of an HND row: code * scale, exact in fp64
+/* Dequantized channel c of the K row `row`: code * scale, exact in fp64
  * ("shared/attention_kit.py", `dequantize_q8_into`). */
-static double or_dequant(const or_problem *p, const int8_t *cache,
-                         const uint16_t *scale, int64_t row, int32_t c)
+static double or_dequant_k(const or_problem *p, int64_t row, int32_t c)
 {
     int32_t groups = p->d / OR_GROUP;
-    double code = (double)cache[row * p->d + c];
-    double sc = (double)or_f16_to_f32(scale[row * groups + c / OR_GROUP]);
+    double code = (double)p->k_cache[row * p->d + c];
+    double sc = (double)or_f16_to_f32(p->k_scale[row * groups + c / OR_GROUP]);
+    return code * sc;
+}
+
+/* The same for V, whose pages are channel-major: page = row / bs, offset =
+ * row % bs. */
+static double or_dequant_v(const or_problem *p, int64_t row, int32_t c)
+{
+    int32_t groups = p->d / OR_GROUP;
+    int64_t page = row / p->bs, off = row % p->bs;
+    double code = (double)p->v_cache[(page * p->d + c) * p->bs + off];
+    double sc = (double)or_f16_to_f32(p->v_scale[(page * groups + c / OR_GROUP) * p->bs + off]);
     return code * sc;
 }
 
@@ -334,7 +355,7 @@ static int or_partial(const or_problem *p, int32_t t, int32_t h, int64_t lo,
         else
             for (int32_t c = 0; c < p->d; ++c)
                 dot += (double)or_bf16_to_f32(qrow[c]) *
-                       or_dequant(p, p->k_cache, p->k_scale, row, c);
+                       or_dequant_k(p, row, c);
         scores[j - lo] = p->softmax_scale * dot;
         if (scores[j - lo] > m) m = scores[j - lo];
     }
@@ -345,7 +366,7 @@ static int or_partial(const or_problem *p, int32_t t, int32_t h, int64_t lo,
         l += w;
         if (row >= 0)
             for (int32_t c = 0; c < p->d; ++c)
-                acc[c] += w * or_dequant(p, p->v_cache, p->v_scale, row, c);
+                acc[c] += w * or_dequant_v(p, row, c);
     }
     *m_out = m;
     *l_out = l;

@@ -106,14 +106,24 @@ def _check16(name, t):
         raise TypeError(f"{name} must hold 16-bit elements (fp16 scales)")
 
 
+def _check_cache_shapes(k_cache, k_scale, v_cache, v_scale):
+    """K pages token-major, V pages channel-major (see include/paq8.h)."""
+    nb, hk, bs, d = k_cache.shape
+    want = ((nb, hk, bs, d // 32), (nb, hk, d, bs), (nb, hk, d // 32, bs))
+    got = (tuple(k_scale.shape), tuple(v_cache.shape), tuple(v_scale.shape))
+    if got != want:
+        raise ValueError(f"cache shapes {got} != {want} (k_scale, v_cache, v_scale)")
+
+
 # ----------------------------------------------------------------------------- API
 
 def kv_store(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, status=None,
              stream=None) -> None:
     """Quantize key/value rows [N, Hk, D] (bf16) to q8 and scatter them by
-    ``slot_mapping`` (int64 [N]; slot < 0 skipped) into the HND caches
-    ``k_cache``/``v_cache`` (int8 [num_blocks, Hk, bs, D]) and
-    ``k_scale``/``v_scale`` ([num_blocks, Hk, bs, D/32], fp16 or int16 bits).
+    ``slot_mapping`` (int64 [N]; slot < 0 skipped) into the paged caches:
+    ``k_cache`` int8 [num_blocks, Hk, bs, D], ``k_scale`` [num_blocks, Hk, bs, D/32],
+    ``v_cache`` int8 [num_blocks, Hk, D, bs], ``v_scale`` [num_blocks, Hk, D/32, bs]
+    (scales fp16 or their int16 bits).
     ``status``: optional int32 CUDA tensor (>= 1 element, zeroed) for device checks."""
     _check_cuda(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, status)
     if key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
@@ -131,10 +141,9 @@ def kv_store(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, statu
         if t.stride(2) != 1 or t.stride(1) != d:
             raise ValueError("key/value head and channel dims must be contiguous")
     num_blocks, hk2, bs, d2 = k_cache.shape
-    if (hk2, d2) != (hk, d) or v_cache.shape != k_cache.shape:
+    if (hk2, d2) != (hk, d):
         raise ValueError("cache shape mismatch")
-    if k_scale.shape != (num_blocks, hk, bs, d // 32) or v_scale.shape != k_scale.shape:
-        raise ValueError("scale shape mismatch")
+    _check_cache_shapes(k_cache, k_scale, v_cache, v_scale)
     for t in (k_cache, v_cache, k_scale, v_scale, slot_mapping):
         if not t.is_contiguous():
             raise ValueError("caches and slot_mapping must be contiguous")
@@ -184,8 +193,9 @@ def paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
     _check16("v_scale", v_scale)
     T, hq, d = q.shape
     num_blocks, hk, bs, d2 = k_cache.shape
-    if d2 != d or v_cache.shape != k_cache.shape:
+    if d2 != d:
         raise ValueError("cache shape mismatch")
+    _check_cache_shapes(k_cache, k_scale, v_cache, v_scale)
     S = seq_lens.shape[0]
     if cu_seqlens_q.shape != (S + 1,) or block_table.shape[0] != S:
         raise ValueError("metadata shapes disagree with seq_lens")

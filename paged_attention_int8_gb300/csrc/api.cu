@@ -104,8 +104,8 @@ pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_s
   if (!supported_bs(block_size)) return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32");
   if (num_blocks <= 0 || block_table_stride <= 0)
     return fail(PA_ERR_INVALID_ARG, "num_blocks and block_table_stride must be positive");
-  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size >= (int64_t{1} << 31))
-    return fail(PA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * block_size must be < 2^31");
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * head_dim >= (int64_t{1} << 31))
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * head_dim must be < 2^31");
   if (max_query_len <= 0 || max_seq_len <= 0)
     return fail(PA_ERR_INVALID_ARG, "max_query_len and max_seq_len must be positive");
   if (num_splits < 0 || num_splits > 16) return fail(PA_ERR_INVALID_ARG, "num_splits in [0, 16]");

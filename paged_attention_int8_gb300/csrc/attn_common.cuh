@@ -1,0 +1,182 @@
+// Pieces shared by the paged-attention kernels: arguments, the staged page
+// layouts in shared memory, the TMA producer loop and the key permutation
+// that lets a lane read its MMA fragments with plain vector loads.
+#pragma once
+
+#include "common.cuh"
+
+namespace paq8 {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 4;  // pipeline depth; a multiple of the kv groups (1, 2, 4)
+constexpr int kMaxSplits = 16;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct AttnArgs {
+  const uint16_t *q;            // [T, Hq, D] bf16
+  const int32_t *cu_seqlens_q;  // [S+1]
+  const int32_t *seq_lens;      // [S]
+  const int32_t *block_table;   // [S, bt_stride]
+  const uint16_t *k_scale;      // [nb, Hk, bs, G] fp16
+  const uint16_t *v_scale;      // [nb, Hk, G, bs] fp16
+  uint16_t *out;                // [T, Hq, D] bf16
+  float *lse;                   // [T, Hq] or null
+  float *part_acc;              // [S, Hq, NS, D]
+  float *part_ml;               // [S, Hq, NS, 2]  (max in log2 units, expsum)
+  uint32_t *status;
+  int32_t num_seqs, num_tokens, hq, hk, qpk, num_blocks, bt_stride;
+  int32_t block_q;              // tokens per q-block (prefill kernel)
+  int32_t n_qblocks;            // grid.x entries that are q-blocks (prefill kernel)
+  int32_t num_splits;           // segments of single-token sequences
+  int32_t seg_tiles;            // tiles per segment
+  int32_t skip_single;          // prefill kernel: leave single-token sequences alone
+  int32_t multi_token_ok;       // decode kernel: a prefill kernel runs for q_len > 1
+  float scale_log2;             // softmax_scale * log2(e)
+};
+
+// Layout of one pipeline stage of TILE keys (a whole number of pages):
+//   K codes  [TILE][D]    token-major pages, 2-D TMA with 128-byte swizzle
+//                         (64-byte for D = 64); D = 256 rows are two boxes
+//   V codes  [pages][D][BS] channel-major pages, one TMA box per page
+//                         (32-byte swizzle for BS = 32)
+//   K scales [TILE][G]    fp16, one bulk copy per page
+//   V scales [pages][G][BS] fp16, one bulk copy per page
+template <int D, int BS, int TILE>
+struct StageLayout {
+  static constexpr int kD = D;
+  static constexpr int G = D / 32;
+  static constexpr int kPages = TILE / BS;
+  static constexpr int kRowBytes = D >= 128 ? 128 : D;  // K box row bytes
+  static constexpr int kSub = D / kRowBytes;             // K boxes per row
+  static constexpr int kCodeBytes = TILE * D;
+  static constexpr int kScaleBytes = TILE * G * 2;
+  static constexpr int kVOff = kCodeBytes;
+  static constexpr int kKsOff = 2 * kCodeBytes;
+  static constexpr int kVsOff = 2 * kCodeBytes + kScaleBytes;
+  static constexpr int kBytes = 2 * kCodeBytes + 2 * kScaleBytes;
+  static constexpr uint32_t kPageTx = 2u * BS * D + 2u * BS * G * 2;
+  static_assert(TILE % BS == 0 && TILE % 16 == 0, "tile");
+  static_assert(kBytes % 512 == 0, "stage alignment for the swizzled boxes");
+
+  // K: byte b of key row r (swizzle as laid out by the TMA unit)
+  __device__ static __forceinline__ uint32_t k_off(int r, int b) {
+    if constexpr (D >= 128) {
+      const int off = r * 128 + (b & 127);
+      return (b >> 7) * (TILE * 128) + (off ^ (((off >> 7) & 7) << 4));
+    } else {
+      const int off = r * 64 + b;
+      return off ^ (((off >> 7) & 3) << 4);
+    }
+  }
+  // V: byte of key `key` (0..TILE-1) of channel c
+  __device__ static __forceinline__ uint32_t v_off(int c, int key) {
+    const int page = key / BS;
+    const int off = c * BS + (key % BS);
+    if constexpr (BS == 32) {
+      return kVOff + page * (D * BS) + (off ^ (((off >> 7) & 1) << 4));
+    } else {
+      return kVOff + page * (D * BS) + off;
+    }
+  }
+  // K scales: group g of key `key`
+  __device__ static __forceinline__ uint32_t ks_off(int key, int g) {
+    return kKsOff + (key * G + g) * 2;
+  }
+  // V scales: group g of key `key`
+  __device__ static __forceinline__ uint32_t vs_off(int key, int g) {
+    return kVsOff + ((key / BS) * (G * BS) + g * BS + key % BS) * 2;
+  }
+};
+
+// MMA k index -> key within a 16-key block.  A lane reads 4 consecutive keys
+// of one V channel (a 32-bit word): keys 4t..4t+1 serve k = 2t, 2t+1 and keys
+// 4t+2..4t+3 serve k = 2t+8, 2t+9.  K rows and scores follow the same order.
+__device__ __forceinline__ int perm16(int k) {
+  return ((k & 7) >> 1) * 4 + (k >> 3) * 2 + (k & 1);
+}
+
+// The producer warp: walks tiles [tile_lo, tile_lo + n_iter) of sequence
+// `seq`, kv head h, staging each tile's pages through the mbarrier ring.
+// Block-table entries are read 32 pages at a time, one per lane.
+template <class L, int BS>
+__device__ __forceinline__ void produce_tiles(const AttnArgs &a, const CUtensorMap *tmap_k,
+                                              const CUtensorMap *tmap_v, uint32_t smem_base,
+                                              uint32_t bar_full, uint32_t bar_empty, int seq,
+                                              int h, int tile_lo, int n_iter, int kv_end,
+                                              int lane) {
+  const int n_pages = (kv_end + BS - 1) / BS;
+  const int32_t *bt_row = a.block_table + static_cast<int64_t>(seq) * a.bt_stride;
+  int page_base = -(1 << 30);
+  int my_blk = -1;
+  for (int it = 0; it < n_iter; ++it) {
+    const int stage = it % kStages;
+    if (it >= kStages) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / kStages) - 1) & 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
+        return;
+      }
+    }
+    const int lp0 = (tile_lo + it) * L::kPages;
+    if (lp0 - page_base >= 32) {
+      page_base = lp0;
+      const int lp = page_base + lane;
+      my_blk = -1;
+      if (lp < n_pages) {
+        const int b = lp < a.bt_stride ? bt_row[lp] : -1;
+        if (b >= 0 && b < a.num_blocks) my_blk = b;
+        else flag_status(a.status, PA_DEV_BAD_BLOCK);
+      }
+    }
+    int blk[L::kPages];
+    int nvalid = 0;
+#pragma unroll
+    for (int p = 0; p < L::kPages; ++p) {
+      blk[p] = __shfl_sync(0xffffffffu, my_blk, lp0 + p - page_base);
+      nvalid += blk[p] >= 0;
+    }
+    if (lane == 0) {
+      const uint32_t full = bar_full + 8 * stage;
+      const uint32_t st = smem_base + stage * L::kBytes;
+      mbar_arrive_expect_tx(full, nvalid * L::kPageTx);
+#pragma unroll
+      for (int p = 0; p < L::kPages; ++p) {
+        if (blk[p] < 0) continue;
+        const int64_t page = static_cast<int64_t>(blk[p]) * a.hk + h;
+#pragma unroll
+        for (int sub = 0; sub < L::kSub; ++sub)
+          tma_load_2d(st + sub * (L::kCodeBytes / L::kSub) + p * (BS * L::kRowBytes), tmap_k,
+                      sub * L::kRowBytes, static_cast<int32_t>(page * BS), full);
+        // V page: D channel rows of BS key bytes; row index page * D in the map
+        tma_load_2d(st + L::kVOff + p * (L::kD * BS), tmap_v, 0,
+                    static_cast<int32_t>(page * L::kD), full);
+        bulk_load(st + L::kKsOff + p * (BS * L::G * 2), a.k_scale + page * BS * L::G,
+                  BS * L::G * 2, full);
+        bulk_load(st + L::kVsOff + p * (BS * L::G * 2), a.v_scale + page * BS * L::G,
+                  BS * L::G * 2, full);
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// Load 4 consecutive fp16 V scales (keys 4t..4t+3 of group g) as two half2
+// words, zeroing keys at or beyond kv_end (stale bytes may sit there).
+template <class L>
+__device__ __forceinline__ uint2 v_scales4(uint32_t st, int key, int g, bool tail, int key0,
+                                           int kv_end) {
+  uint2 s = lds64(st + L::vs_off(key, g));
+  if (tail) {
+    const int k = key0 + key;
+    if (k + 0 >= kv_end) s.x &= 0xffff0000u;
+    if (k + 1 >= kv_end) s.x &= 0x0000ffffu;
+    if (k + 2 >= kv_end) s.y &= 0xffff0000u;
+    if (k + 3 >= kv_end) s.y &= 0x0000ffffu;
+  }
+  return s;
+}
+
+}  // namespace paq8

@@ -1,0 +1,385 @@
+// Decode kernel: sequences with a single query token, their q heads (up to
+// 8 per kv head) attending one KV segment each.
+//
+// Computes, for the token's q heads h of kv head hk (GQA: h / qpk == hk),
+// the online-softmax triple of "triton_turboquant_unified_attention.py"
+// (3D split-KV kernel): m = max_j s_j, l = sum_j exp(s_j - m),
+// acc = sum_j exp(s_j - m) v_j over the segment's keys, s_j = scale * q.k_j.
+// Unsplit, it writes out = acc / l and lse = m + ln l directly.
+//
+// Swap-AB form: with one token the GQA group has only qpk <= 8 rows, so the
+// keys take the MMA's M dimension and the heads its N dimension:
+//   S^T[16 keys x 8 heads]  = K[16 keys x 16 ch] . Q^T[16 ch x 8 heads]
+//   O^T[16 ch x 8 heads]   += V^T[16 ch x 16 keys] . P^T[16 keys x 8 heads]
+// K codes are exact fp16 integers; each 32-channel group's partial scores are
+// scaled by the group's fp16 K scale in fp32.  V^T comes straight from the
+// channel-major V pages (4 consecutive keys per 32-bit load) and is scaled to
+// fp16.  P^T reaches the B-operand layout with one movmatrix per 8x8 block.
+//
+// CTA = 4 consumer warps taking alternate 64-key tiles (32 for D = 256) with
+// private softmax states, merged at the end, plus one TMA producer warp.
+// Grid: (num_seqs * num_splits, num_kv_heads); sequence and segment come
+// straight from blockIdx.x.
+#include "attn_common.cuh"
+
+namespace paq8 {
+
+// The G fp16 K scales of one key row (contiguous) as floats.
+template <int G>
+__device__ __forceinline__ void load_scales_row(uint32_t addr, float (&f)[G]) {
+  uint32_t w[G / 2];
+  if constexpr (G == 2) {
+    w[0] = lds32(addr);
+  } else if constexpr (G == 4) {
+    const uint2 v = lds64(addr);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < G / 8; ++i) {
+      const uint4 v = lds128(addr + 16 * i);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < G / 2; ++i) {
+    const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+
+template <int D>
+struct DecodeCfg {
+  static constexpr int kTile = D == 256 ? 32 : 64;
+  static constexpr int kMt = kTile / 16;   // 16-key blocks per tile
+  static constexpr int kCm = D / 16;       // 16-channel blocks of the output
+  static constexpr int G = D / 32;
+};
+
+template <int D, int BS>
+__global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
+    decode_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v) {
+  using Cfg = DecodeCfg<D>;
+  using L = StageLayout<D, BS, Cfg::kTile>;
+  constexpr int G = Cfg::G;
+  constexpr int kTile = Cfg::kTile;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  float *smem_f = reinterpret_cast<float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int seq = blockIdx.x / a.num_splits;
+  const int sigma = blockIdx.x % a.num_splits;
+
+  const int q_start = a.cu_seqlens_q[seq];
+  const int q_len = a.cu_seqlens_q[seq + 1] - q_start;
+  if (q_len != 1) {  // not a single-token sequence: the prefill kernel's, if it runs
+    if (q_len > 1 && !a.multi_token_ok && sigma == 0 && h == 0 && threadIdx.x == 0)
+      flag_status(a.status, PA_DEV_BAD_SEQ);  // max_query_len hint was below a q_len
+    return;
+  }
+  if (q_start < 0 || q_start >= a.num_tokens) {
+    if (threadIdx.x == 0 && sigma == 0) flag_status(a.status, PA_DEV_BAD_SEQ);
+    return;
+  }
+  const int seq_len = a.seq_lens[seq];
+  if (seq_len < 1) {
+    if (threadIdx.x == 0 && sigma == 0) flag_status(a.status, PA_DEV_BAD_SEQ);
+    return;
+  }
+  const bool split = a.num_splits > 1;
+  const int kv_end = seq_len;
+  const int num_tiles = (kv_end + kTile - 1) / kTile;
+  int tile_lo = 0, tile_hi = num_tiles;
+  if (split) {
+    if (static_cast<int64_t>(sigma) * a.seg_tiles * kTile >= seq_len) return;
+    tile_lo = sigma * a.seg_tiles;
+    tile_hi = sigma == a.num_splits - 1 ? num_tiles : min(num_tiles, tile_lo + a.seg_tiles);
+  }
+  const int n_iter = tile_hi - tile_lo;
+  if (n_iter <= 0) return;
+
+  constexpr int kMergeBytes = 3 * 32 * (4 + 4 * Cfg::kCm) * 4;
+  constexpr int kRingBytes = kStages * L::kBytes;
+  static_assert(kMergeBytes <= kRingBytes, "merge area fits in the ring");
+  const uint32_t bar_full = smem_base + kRingBytes;
+  const uint32_t bar_empty = bar_full + kStages * 8;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);  // each stage is consumed by one warp
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
+    produce_tiles<L, BS>(a, &tmap_k, &tmap_v, smem_base, bar_full, bar_empty, seq, h, tile_lo,
+                         n_iter, kv_end, lane);
+    return;
+  }
+
+  const int g = lane >> 2;
+  const int t = lane & 3;
+
+  // Q^T as the B operand: lane (g, t) holds head g, channels 32gq + 8t + 4s +
+  // {0,1} (k = 2t, 2t+1) and + {2,3} (k = 2t+8, 2t+9) for k-step s.
+  uint32_t qb[G][2][2];
+  {
+    const bool hv = g < a.qpk;
+    const uint16_t *src =
+        a.q + (static_cast<int64_t>(q_start) * a.hq + h * a.qpk + (hv ? g : 0)) * D + t * 8;
+#pragma unroll
+    for (int gq = 0; gq < G; ++gq) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (hv) v = *reinterpret_cast<const uint4 *>(src + gq * 32);
+      qb[gq][0][0] = pack_half2(bf16_lo(v.x), bf16_hi(v.x));
+      qb[gq][0][1] = pack_half2(bf16_lo(v.y), bf16_hi(v.y));
+      qb[gq][1][0] = pack_half2(bf16_lo(v.z), bf16_hi(v.z));
+      qb[gq][1][1] = pack_half2(bf16_lo(v.w), bf16_hi(v.w));
+    }
+  }
+  const int r0 = perm16(g);      // key (within a 16-key block) of score row g
+  const int r1 = perm16(g + 8);  // ... of score row g + 8
+
+  float m_run[2] = {-INFINITY, -INFINITY};  // heads 2t, 2t+1 (log2 units)
+  float l_run[2] = {0.0f, 0.0f};            // this lane's share of the expsum
+  float o[Cfg::kCm][4];                     // O^T: channels (g, g+8) x heads (2t, 2t+1)
+#pragma unroll
+  for (int i = 0; i < Cfg::kCm; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[i][e] = 0.0f;
+
+  bool timed_out = false;
+  for (int it = warp; it < n_iter; it += kConsumerWarps) {
+    const int stage = it % kStages;
+    if (!mbar_wait(bar_full + 8 * stage, (it / kStages) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const uint32_t st = smem_base + stage * L::kBytes;
+    const int key0 = (tile_lo + it) * kTile;
+    const bool tail = key0 + kTile > kv_end;
+
+    // ---------------- S^T = K Q^T with exact codes, scaled per group
+    float s[Cfg::kMt][4];
+#pragma unroll
+    for (int mt = 0; mt < Cfg::kMt; ++mt) {
+      const int k0 = mt * 16 + r0, k1 = mt * 16 + r1;
+      float ks0[G], ks1[G];
+      load_scales_row<G>(st + L::ks_off(k0, 0), ks0);
+      load_scales_row<G>(st + L::ks_off(k1, 0), ks1);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[mt][e] = 0.0f;
+#pragma unroll
+      for (int gq = 0; gq < G; ++gq) {
+        const uint2 c0 = lds64(st + L::k_off(k0, gq * 32 + t * 8));
+        const uint2 c1 = lds64(st + L::k_off(k1, gq * 32 + t * 8));
+        uint32_t a00, a02, a01, a03, a10, a12, a11, a13;
+        codes4_to_half2(c0.x, a00, a02);  // row g, k-step 0: (k 2t,2t+1), (k 2t+8,2t+9)
+        codes4_to_half2(c1.x, a01, a03);  // row g+8
+        codes4_to_half2(c0.y, a10, a12);  // k-step 1
+        codes4_to_half2(c1.y, a11, a13);
+        float sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_f16_16816(sg, a00, a01, a02, a03, qb[gq][0][0], qb[gq][0][1]);
+        mma_f16_16816(sg, a10, a11, a12, a13, qb[gq][1][0], qb[gq][1][1]);
+        s[mt][0] = fmaf(sg[0], ks0[gq], s[mt][0]);
+        s[mt][1] = fmaf(sg[1], ks0[gq], s[mt][1]);
+        s[mt][2] = fmaf(sg[2], ks1[gq], s[mt][2]);
+        s[mt][3] = fmaf(sg[3], ks1[gq], s[mt][3]);
+      }
+    }
+
+    // ---------------- mask the tail, online softmax over keys (rows)
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int mt = 0; mt < Cfg::kMt; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = s[mt][e] * a.scale_log2;
+        if (tail && key0 + mt * 16 + (e < 2 ? r0 : r1) >= kv_end) v = -INFINITY;
+        s[mt][e] = v;
+        mx[e & 1] = fmaxf(mx[e & 1], v);
+      }
+    float alpha[2], mu[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+      const float mn = fmaxf(m_run[c], mx[c]);
+      mu[c] = mn == -INFINITY ? 0.0f : mn;
+      alpha[c] = fast_exp2(m_run[c] - mu[c]);
+      m_run[c] = mn;
+      l_run[c] *= alpha[c];
+    }
+    uint32_t pb[Cfg::kMt][2];
+#pragma unroll
+    for (int mt = 0; mt < Cfg::kMt; ++mt) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        p[e] = fast_exp2(s[mt][e] - mu[e & 1]);
+        l_run[e & 1] += p[e];
+      }
+      pb[mt][0] = movmatrix_trans(pack_half2(p[0], p[1]));  // keys 0..7 -> k = 2t, 2t+1
+      pb[mt][1] = movmatrix_trans(pack_half2(p[2], p[3]));  // keys 8..15 -> k = 2t+8, 2t+9
+    }
+#pragma unroll
+    for (int i = 0; i < Cfg::kCm; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[1];
+      o[i][2] *= alpha[0];
+      o[i][3] *= alpha[1];
+    }
+
+    // ---------------- O^T += V'^T P^T, V' = code * scale in fp16
+#pragma unroll
+    for (int gv = 0; gv < G; ++gv) {
+      uint2 vsc[Cfg::kMt];
+#pragma unroll
+      for (int mt = 0; mt < Cfg::kMt; ++mt)
+        vsc[mt] = v_scales4<L>(st, mt * 16 + 4 * t, gv, tail, key0, kv_end);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int cm = gv * 2 + half;
+#pragma unroll
+        for (int mt = 0; mt < Cfg::kMt; ++mt) {
+          const uint32_t w0 = lds32(st + L::v_off(cm * 16 + g, mt * 16 + 4 * t));
+          const uint32_t w1 = lds32(st + L::v_off(cm * 16 + g + 8, mt * 16 + 4 * t));
+          uint32_t a0, a2, a1, a3;
+          codes4_to_half2(w0, a0, a2);  // channel g: keys 4t..4t+1 | 4t+2..4t+3
+          codes4_to_half2(w1, a1, a3);  // channel g + 8
+          a0 = hmul2_u32(a0, vsc[mt].x);
+          a2 = hmul2_u32(a2, vsc[mt].y);
+          a1 = hmul2_u32(a1, vsc[mt].x);
+          a3 = hmul2_u32(a3, vsc[mt].y);
+          mma_f16_16816(o[cm], a0, a1, a2, a3, pb[mt][0], pb[mt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+  }
+  if (timed_out && lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
+
+  // expsum of each head: sum over the 8 lanes that share t
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], off);
+
+  // ---------------- merge the 4 warps (field-major through shared memory)
+  constexpr int kFields = 4 + 4 * Cfg::kCm;
+  named_barrier(1, kConsumerWarps * 32);  // every stage consumed: reuse the ring
+  if (warp > 0) {
+    float *dst = smem_f + (warp - 1) * kFields * 32 + lane;
+    dst[0] = m_run[0];
+    dst[32] = m_run[1];
+    dst[64] = l_run[0];
+    dst[96] = l_run[1];
+#pragma unroll
+    for (int i = 0; i < Cfg::kCm; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[(4 + i * 4 + e) * 32] = o[i][e];
+  }
+  named_barrier(1, kConsumerWarps * 32);
+  if (warp > 0) return;
+#pragma unroll 1
+  for (int k = 0; k < kConsumerWarps - 1; ++k) {
+    const float *src = smem_f + k * kFields * 32 + lane;
+    float wa[2], wb[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const float mo = src[c * 32];
+      const float mn = fmaxf(m_run[c], mo);
+      const float muv = mn == -INFINITY ? 0.0f : mn;
+      wa[c] = fast_exp2(m_run[c] - muv);
+      wb[c] = fast_exp2(mo - muv);
+      m_run[c] = mn;
+      l_run[c] = l_run[c] * wa[c] + src[(2 + c) * 32] * wb[c];
+    }
+#pragma unroll
+    for (int i = 0; i < Cfg::kCm; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        o[i][e] = o[i][e] * wa[e & 1] + src[(4 + i * 4 + e) * 32] * wb[e & 1];
+  }
+
+  // ---------------- write: lane (g, t) holds channels cm*16 + g (+8) of heads 2t, 2t+1
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int hh = 2 * t + c;
+    if (hh >= a.qpk) continue;
+    const int qh = h * a.qpk + hh;
+    if (split) {
+      const int64_t prow = (static_cast<int64_t>(seq) * a.hq + qh) * a.num_splits + sigma;
+      float *dst = a.part_acc + prow * D;
+#pragma unroll
+      for (int cm = 0; cm < Cfg::kCm; ++cm) {
+        dst[cm * 16 + g] = o[cm][c];
+        dst[cm * 16 + g + 8] = o[cm][2 + c];
+      }
+      if (g == 0)
+        *reinterpret_cast<float2 *>(a.part_ml + prow * 2) = make_float2(m_run[c], l_run[c]);
+    } else {
+      const float inv = 1.0f / l_run[c];
+      uint16_t *dst = a.out + (static_cast<int64_t>(q_start) * a.hq + qh) * D;
+#pragma unroll
+      for (int cm = 0; cm < Cfg::kCm; ++cm) {
+        dst[cm * 16 + g] = __bfloat16_as_ushort(__float2bfloat16_rn(o[cm][c] * inv));
+        dst[cm * 16 + g + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(o[cm][2 + c] * inv));
+      }
+      if (g == 0 && a.lse)
+        a.lse[static_cast<int64_t>(q_start) * a.hq + qh] = (m_run[c] + log2f(l_run[c])) * kLn2;
+    }
+  }
+}
+
+template <int D, int BS>
+cudaError_t launch_decode_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                            cudaStream_t stream) {
+  using L = StageLayout<D, BS, DecodeCfg<D>::kTile>;
+  constexpr int kSmem = kStages * L::kBytes + 2 * kStages * 8 + 1024;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  dim3 grid(static_cast<unsigned>(a.num_seqs) * a.num_splits, a.hk);
+  decode_kernel<D, BS><<<grid, kThreads, kSmem, stream>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+int decode_tile(int d) { return d == 256 ? 32 : 64; }
+
+cudaError_t launch_decode(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int d,
+                          int bs, cudaStream_t stream) {
+#define PAQ8_DECODE_CASE(DD, BB) \
+  if (d == DD && bs == BB) return launch_decode_t<DD, BB>(a, tk, tv, stream);
+  PAQ8_DECODE_CASE(64, 16)
+  PAQ8_DECODE_CASE(64, 32)
+  PAQ8_DECODE_CASE(128, 16)
+  PAQ8_DECODE_CASE(128, 32)
+  PAQ8_DECODE_CASE(256, 16)
+  PAQ8_DECODE_CASE(256, 32)
+#undef PAQ8_DECODE_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace paq8

@@ -1,4 +1,5 @@
-// kv_store: quantize K/V rows to q8 and scatter them into the HND paged cache.
+// kv_store: quantize K/V rows to q8 and scatter them into the paged cache
+// (K pages token-major, V pages channel-major).
 //
 // q8 ("shared/attention_kit.py", quantize_q8): per (token, kv head, group of
 // 32 channels) s = max(max|x| / 127, 1e-8) in fp32, code =
@@ -10,8 +11,9 @@
 //
 // One thread per 8 channels of one (token, kv head) row of K and the same 8
 // of V: 16-byte loads of bf16, the group max over the 4 threads of a group by
-// warp shuffle, 8-byte code stores.  Memory bound: per (token, kv head) it
-// reads 4*D bytes and writes 2*(D + D/16) bytes.
+// warp shuffle, 8-byte K code stores and byte stores into the V page rows.
+// Memory bound: per (token, kv head) it reads 4*D bytes and writes
+// 2*(D + D/16) bytes.
 #include "common.cuh"
 #include "launch.h"
 
@@ -94,12 +96,19 @@ __global__ void __launch_bounds__(256) kv_store_kernel(
   const float sv = group_scale(av);
   const int64_t blk = slot / block_size;
   const int64_t off = slot % block_size;
-  const int64_t row = (blk * hk + h) * block_size + off;
+  const int64_t page = blk * hk + h;
+  const int64_t row = page * block_size + off;  // K: token-major page row
   *reinterpret_cast<uint2 *>(k_cache + row * D + cc * 8) = quantize8(xk, sk);
-  *reinterpret_cast<uint2 *>(v_cache + row * D + cc * 8) = quantize8(xv, sv);
+  // V: channel-major page, channel c of this token at (page * D + c) * bs + off
+  const uint2 vq = quantize8(xv, sv);
+  int8_t *vdst = v_cache + (page * D + cc * 8) * block_size + off;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    vdst[e * block_size] = static_cast<int8_t>(((e < 4 ? vq.x : vq.y) >> (8 * (e & 3))) & 0xffu);
   if ((cc & 3) == 0) {
     k_scale[row * kGroups + (cc >> 2)] = __half_as_ushort(__float2half_rn(sk));
-    v_scale[row * kGroups + (cc >> 2)] = __half_as_ushort(__float2half_rn(sv));
+    v_scale[(page * kGroups + (cc >> 2)) * block_size + off] =
+        __half_as_ushort(__float2half_rn(sv));
   }
 }
 

@@ -241,21 +241,29 @@ def make_workload(spec: Spec) -> Workload:
                     new_slots=new_slots, q=q)
 
 
-def empty_cache(num_blocks: int, hk: int, bs: int, d: int, device="cpu", canary: bool = True):
-    """HND cache tensors (k_cache, k_scale, v_cache, v_scale).
+def cache_shapes(num_blocks: int, hk: int, bs: int, d: int):
+    """Shapes of (k_cache, k_scale, v_cache, v_scale).
 
-    Codes [num_blocks, Hk, bs, D] int8, scales [num_blocks, Hk, bs, D/32]
-    stored as int16 bit patterns of fp16.  With ``canary`` the codes are filled
-    with -128 (a value the q8 format never produces) and the scales with
-    0xFFFF (an fp16 NaN), so untouched slots are visible."""
-    shape_c = (num_blocks, hk, bs, d)
-    shape_s = (num_blocks, hk, bs, d // 32)
+    K pages are token-major: codes [num_blocks, Hk, bs, D], scales
+    [num_blocks, Hk, bs, D/32].  V pages are channel-major: codes
+    [num_blocks, Hk, D, bs], scales [num_blocks, Hk, D/32, bs]."""
+    return ((num_blocks, hk, bs, d), (num_blocks, hk, bs, d // 32),
+            (num_blocks, hk, d, bs), (num_blocks, hk, d // 32, bs))
+
+
+def empty_cache(num_blocks: int, hk: int, bs: int, d: int, device="cpu", canary: bool = True):
+    """Cache tensors (k_cache, k_scale, v_cache, v_scale), shapes as in
+    ``cache_shapes``; scales stored as int16 bit patterns of fp16.  With
+    ``canary`` the codes are filled with -128 (a value the q8 format never
+    produces) and the scales with 0xFFFF (an fp16 NaN), so untouched slots are
+    visible."""
+    kc, ks, vc, vs = cache_shapes(num_blocks, hk, bs, d)
     fill_c = -128 if canary else 0
     fill_s = -1 if canary else 0
-    return (torch.full(shape_c, fill_c, dtype=torch.int8, device=device),
-            torch.full(shape_s, fill_s, dtype=torch.int16, device=device),
-            torch.full(shape_c, fill_c, dtype=torch.int8, device=device),
-            torch.full(shape_s, fill_s, dtype=torch.int16, device=device))
+    return (torch.full(kc, fill_c, dtype=torch.int8, device=device),
+            torch.full(ks, fill_s, dtype=torch.int16, device=device),
+            torch.full(vc, fill_c, dtype=torch.int8, device=device),
+            torch.full(vs, fill_s, dtype=torch.int16, device=device))
 
 
 def bf16_bits(t: torch.Tensor):

@@ -110,12 +110,25 @@ def test_empty_sequences_and_unowned_rows(cuda_device):
 
 
 def test_hints_only_steer_tiling(cuda_device):
-    # max_query_len / max_seq_len larger than needed, or a max_query_len of 1
-    # on a batch with prefill chunks, still give the same results
+    # a max_query_len above the real one, and a max_seq_len far above or below
+    # the real one, still give the same results
     w = inputs.make_workload(SMALL["mixed"])
-    H.check_workload(w, cuda_device, splits=(None,), max_query_len=1)
+    H.check_workload(w, cuda_device, splits=(None,), max_query_len=4 * w.max_query_len)
     H.check_workload(w, cuda_device, splits=(None, 16), max_seq_len=4 * w.max_seq_len)
     H.check_workload(w, cuda_device, splits=(16,), max_seq_len=64)
+
+
+def test_max_query_len_below_a_q_len_is_flagged(cuda_device):
+    # the decode-only path cannot serve a multi-token sequence: it says so
+    w = inputs.make_workload(SMALL["mixed"])
+    g = H.GpuState(w, cuda_device)
+    ws = torch.zeros(_lib.workspace_size(w.num_seqs, w.spec.hq, w.spec.d, 0), dtype=torch.uint8,
+                     device=cuda_device)
+    _lib.paged_attention(g.q, g.kc, g.ks, g.vc, g.vs, g.cu, g.seq_lens, g.block_table, 1,
+                         w.max_seq_len, workspace=ws)
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        _lib.check_status(ws)
+    assert e.value.bits == _lib.DEV_BAD_SEQ
 
 
 def test_no_lse_requested(cuda_device):

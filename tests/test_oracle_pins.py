@@ -43,17 +43,26 @@ def _bf16_bits(x: torch.Tensor) -> np.ndarray:
 
 
 def _rand_cache(rng, num_blocks, hk, bs, d, scale_lo=0.005, scale_hi=0.05):
-    kc = rng.integers(-127, 128, size=(num_blocks, hk, bs, d), dtype=np.int8)
-    vc = rng.integers(-127, 128, size=(num_blocks, hk, bs, d), dtype=np.int8)
-    ks = _f16_bits_numpy(rng.uniform(scale_lo, scale_hi, size=(num_blocks, hk, bs, d // 32)))
-    vs = _f16_bits_numpy(rng.uniform(scale_lo, scale_hi, size=(num_blocks, hk, bs, d // 32)))
+    kcs, kss, vcs, vss = inputs.cache_shapes(num_blocks, hk, bs, d)
+    kc = rng.integers(-127, 128, size=kcs, dtype=np.int8)
+    vc = rng.integers(-127, 128, size=vcs, dtype=np.int8)
+    ks = _f16_bits_numpy(rng.uniform(scale_lo, scale_hi, size=kss))
+    vs = _f16_bits_numpy(rng.uniform(scale_lo, scale_hi, size=vss))
     return kc, ks, vc, vs
 
 
 def _dequant(codes, scales):
-    """Reference dequantization with numpy (fp64): value = code * fp16 scale."""
+    """Reference dequantization with numpy (fp64): value = code * fp16 scale,
+    token-major pages [..., bs, D] with scales [..., bs, D/32]."""
     s = scales.view(np.float16).astype(np.float64)
     return codes.astype(np.float64) * np.repeat(s, 32, axis=-1)
+
+
+def _token_major_v(vc, vs):
+    """Channel-major V pages [nb, hk, D, bs] / [nb, hk, D/32, bs] viewed
+    token-major, for the numpy references."""
+    return (np.ascontiguousarray(vc.transpose(0, 1, 3, 2)),
+            np.ascontiguousarray(vs.transpose(0, 1, 3, 2)))
 
 
 def _problem(rng, q_lens, seq_lens, hq, hk, d, bs, spare=3, q_scale=1.0):
@@ -81,8 +90,11 @@ def _run(p, scale, rows=None):
 
 
 def _gather(p, codes, scales, s, L):
-    """Logical [L, Hk, D] fp64 of sequence s (numpy gather through the table)."""
+    """Logical [L, Hk, D] fp64 of sequence s (numpy gather through the table).
+    V pages (channel-major) are recognised by their shape and transposed."""
     bs = p["bs"]
+    if codes.shape[2] != bs:  # V: [nb, hk, D, bs] (D >= 64 > bs)
+        codes, scales = _token_major_v(codes, scales)
     j = np.arange(L)
     blk = p["bt"][s, j // bs]
     off = j % bs
@@ -364,7 +376,7 @@ def test_causal_limit_is_bottom_right_aligned():
     s = 0
     j = np.arange(L)
     blk = p["bt"][s, j // 16]
-    p["vc"][blk, 0, j % 16, 0] = j.astype(np.int8)
+    p["vc"][blk, 0, 0, j % 16] = j.astype(np.int8)   # V pages are channel-major
     p["vs"][:] = _f16_bits_numpy(np.full(p["vs"].shape, 1.0))
     out, _ = _run(p, 1.0)
     out = out.reshape(ql, 2, 32)
