@@ -16,8 +16,9 @@
 // channel-major V pages (4 consecutive keys per 32-bit load) and is scaled to
 // fp16.  P^T reaches the B-operand layout with one movmatrix per 8x8 block.
 //
-// CTA = 4 consumer warps taking alternate 64-key tiles (32 for D = 256) with
-// private softmax states, merged at the end, plus one TMA producer warp.
+// CTA = 4 consumer warps, each taking one 16-key block of every 64-key tile
+// (D = 256: 32-key tiles, two warps per tile, pairs alternate tiles), with
+// private softmax states merged at the end, plus one TMA producer warp.
 // Grid: (num_seqs * num_splits, num_kv_heads); sequence and segment come
 // straight from blockIdx.x.
 #include "attn_common.cuh"
@@ -56,6 +57,8 @@ template <int D>
 struct DecodeCfg {
   static constexpr int kTile = D == 256 ? 32 : 64;
   static constexpr int kMt = kTile / 16;   // 16-key blocks per tile
+  static constexpr int kWpt = kMt < kConsumerWarps ? kMt : kConsumerWarps;  // warps per tile
+  static constexpr int kKg = kConsumerWarps / kWpt;  // tile groups (alternate tiles)
   static constexpr int kCm = D / 16;       // 16-channel blocks of the output
   static constexpr int G = D / 32;
 };
@@ -68,6 +71,9 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
   using L = StageLayout<D, BS, Cfg::kTile>;
   constexpr int G = Cfg::G;
   constexpr int kTile = Cfg::kTile;
+  constexpr int kWpt = Cfg::kWpt;
+  constexpr int kKg = Cfg::kKg;
+  static_assert(kStages % kKg == 0, "a stage always feeds the same tile group");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   float *smem_f = reinterpret_cast<float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);  // each stage is consumed by one warp
+      mbar_init(bar_empty + 8 * s, kWpt);  // every warp of the tile group reads it
     }
     fence_barrier_init();
   }
@@ -161,27 +167,31 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[i][e] = 0.0f;
 
+  // Warp w takes the 16-key block mt = w % kWpt of every tile of its tile
+  // group (w / kWpt): all warps read every stage, so the whole ring is in
+  // flight for each of them.
+  const int my_mt = warp % kWpt;
+  const int kg = warp / kWpt;
   bool timed_out = false;
-  for (int it = warp; it < n_iter; it += kConsumerWarps) {
+  for (int it = kg; it < n_iter; it += kKg) {
     const int stage = it % kStages;
     if (!mbar_wait(bar_full + 8 * stage, (it / kStages) & 1)) {
       timed_out = true;
       break;
     }
     const uint32_t st = smem_base + stage * L::kBytes;
-    const int key0 = (tile_lo + it) * kTile;
-    const bool tail = key0 + kTile > kv_end;
+    const int key0 = (tile_lo + it) * kTile + my_mt * 16;  // first key of this warp's block
+    const bool tail = key0 + 16 > kv_end;
 
     // ---------------- S^T = K Q^T with exact codes, scaled per group
-    float s[Cfg::kMt][4];
-#pragma unroll
-    for (int mt = 0; mt < Cfg::kMt; ++mt) {
-      const int k0 = mt * 16 + r0, k1 = mt * 16 + r1;
+    float s[4];
+    {
+      const int k0 = my_mt * 16 + r0, k1 = my_mt * 16 + r1;
       float ks0[G], ks1[G];
       load_scales_row<G>(st + L::ks_off(k0, 0), ks0);
       load_scales_row<G>(st + L::ks_off(k1, 0), ks1);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[mt][e] = 0.0f;
+      for (int e = 0; e < 4; ++e) s[e] = 0.0f;
 #pragma unroll
       for (int gq = 0; gq < G; ++gq) {
         const uint2 c0 = lds64(st + L::k_off(k0, gq * 32 + t * 8));
@@ -194,79 +204,72 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
         float sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         mma_f16_16816(sg, a00, a01, a02, a03, qb[gq][0][0], qb[gq][0][1]);
         mma_f16_16816(sg, a10, a11, a12, a13, qb[gq][1][0], qb[gq][1][1]);
-        s[mt][0] = fmaf(sg[0], ks0[gq], s[mt][0]);
-        s[mt][1] = fmaf(sg[1], ks0[gq], s[mt][1]);
-        s[mt][2] = fmaf(sg[2], ks1[gq], s[mt][2]);
-        s[mt][3] = fmaf(sg[3], ks1[gq], s[mt][3]);
+        s[0] = fmaf(sg[0], ks0[gq], s[0]);
+        s[1] = fmaf(sg[1], ks0[gq], s[1]);
+        s[2] = fmaf(sg[2], ks1[gq], s[2]);
+        s[3] = fmaf(sg[3], ks1[gq], s[3]);
       }
     }
 
     // ---------------- mask the tail, online softmax over keys (rows)
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int mt = 0; mt < Cfg::kMt; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = s[mt][e] * a.scale_log2;
-        if (tail && key0 + mt * 16 + (e < 2 ? r0 : r1) >= kv_end) v = -INFINITY;
-        s[mt][e] = v;
-        mx[e & 1] = fmaxf(mx[e & 1], v);
-      }
+    for (int e = 0; e < 4; ++e) {
+      float v = s[e] * a.scale_log2;
+      if (tail && key0 + (e < 2 ? r0 : r1) >= kv_end) v = -INFINITY;
+      s[e] = v;
+      mx[e & 1] = fmaxf(mx[e & 1], v);
+    }
     float alpha[2], mu[2];
+    bool grew = false;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1)
         mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
       const float mn = fmaxf(m_run[c], mx[c]);
+      grew |= mn != m_run[c];
       mu[c] = mn == -INFINITY ? 0.0f : mn;
       alpha[c] = fast_exp2(m_run[c] - mu[c]);
       m_run[c] = mn;
-      l_run[c] *= alpha[c];
     }
-    uint32_t pb[Cfg::kMt][2];
+    float p[4];
 #pragma unroll
-    for (int mt = 0; mt < Cfg::kMt; ++mt) {
-      float p[4];
+    for (int e = 0; e < 4; ++e) p[e] = fast_exp2(s[e] - mu[e & 1]);
+    const uint32_t pb0 = movmatrix_trans(pack_half2(p[0], p[1]));  // keys 0..7 -> k 2t, 2t+1
+    const uint32_t pb1 = movmatrix_trans(pack_half2(p[2], p[3]));  // keys 8..15 -> k 2t+8, 2t+9
+    // rescale only when some head's running max moved (alpha == 1 otherwise)
+    if (__any_sync(0xffffffffu, grew)) {
+      l_run[0] *= alpha[0];
+      l_run[1] *= alpha[1];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        p[e] = fast_exp2(s[mt][e] - mu[e & 1]);
-        l_run[e & 1] += p[e];
+      for (int i = 0; i < Cfg::kCm; ++i) {
+        o[i][0] *= alpha[0];
+        o[i][1] *= alpha[1];
+        o[i][2] *= alpha[0];
+        o[i][3] *= alpha[1];
       }
-      pb[mt][0] = movmatrix_trans(pack_half2(p[0], p[1]));  // keys 0..7 -> k = 2t, 2t+1
-      pb[mt][1] = movmatrix_trans(pack_half2(p[2], p[3]));  // keys 8..15 -> k = 2t+8, 2t+9
     }
-#pragma unroll
-    for (int i = 0; i < Cfg::kCm; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[1];
-      o[i][2] *= alpha[0];
-      o[i][3] *= alpha[1];
-    }
+    l_run[0] += p[0] + p[2];
+    l_run[1] += p[1] + p[3];
 
     // ---------------- O^T += V'^T P^T, V' = code * scale in fp16
 #pragma unroll
     for (int gv = 0; gv < G; ++gv) {
-      uint2 vsc[Cfg::kMt];
-#pragma unroll
-      for (int mt = 0; mt < Cfg::kMt; ++mt)
-        vsc[mt] = v_scales4<L>(st, mt * 16 + 4 * t, gv, tail, key0, kv_end);
+      const uint2 vsc = v_scales4<L>(st, my_mt * 16 + 4 * t, gv, tail, key0 - my_mt * 16, kv_end);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cm = gv * 2 + half;
-#pragma unroll
-        for (int mt = 0; mt < Cfg::kMt; ++mt) {
-          const uint32_t w0 = lds32(st + L::v_off(cm * 16 + g, mt * 16 + 4 * t));
-          const uint32_t w1 = lds32(st + L::v_off(cm * 16 + g + 8, mt * 16 + 4 * t));
-          uint32_t a0, a2, a1, a3;
-          codes4_to_half2(w0, a0, a2);  // channel g: keys 4t..4t+1 | 4t+2..4t+3
-          codes4_to_half2(w1, a1, a3);  // channel g + 8
-          a0 = hmul2_u32(a0, vsc[mt].x);
-          a2 = hmul2_u32(a2, vsc[mt].y);
-          a1 = hmul2_u32(a1, vsc[mt].x);
-          a3 = hmul2_u32(a3, vsc[mt].y);
-          mma_f16_16816(o[cm], a0, a1, a2, a3, pb[mt][0], pb[mt][1]);
-        }
+        const uint32_t w0 = lds32(st + L::v_off(cm * 16 + g, my_mt * 16 + 4 * t));
+        const uint32_t w1 = lds32(st + L::v_off(cm * 16 + g + 8, my_mt * 16 + 4 * t));
+        uint32_t a0, a2, a1, a3;
+        codes4_to_half2(w0, a0, a2);  // channel g: keys 4t..4t+1 | 4t+2..4t+3
+        codes4_to_half2(w1, a1, a3);  // channel g + 8
+        a0 = hmul2_u32(a0, vsc.x);
+        a2 = hmul2_u32(a2, vsc.y);
+        a1 = hmul2_u32(a1, vsc.x);
+        a3 = hmul2_u32(a3, vsc.y);
+        mma_f16_16816(o[cm], a0, a1, a2, a3, pb0, pb1);
       }
     }
     __syncwarp();
