@@ -4,9 +4,12 @@
 // One call may launch up to three kernels on the caller's stream:
 //  * decode_kernel  -- single-token sequences when Hq/Hk <= 8 (swap-AB form),
 //                      split into KV segments (the pages' 3D kernel);
-//  * prefill_kernel -- every other sequence, in q-blocks of 64/qpk tokens
-//                      (the pages' unified 2D kernel); it also takes the
-//                      single-token rows when Hq/Hk > 8;
+//  * prefill_tc_kernel -- multi-token sequences on tcgen05/TMEM, q-blocks of
+//                      128/qpk tokens (D = 64, 128 with Hq/Hk <= 8);
+//  * prefill_kernel -- otherwise every other sequence on mma.sync, in
+//                      q-blocks of 64/qpk tokens (the pages' unified 2D
+//                      kernel); it also takes the single-token rows when
+//                      Hq/Hk > 8;
 //  * reduce_kernel  -- merges the segment triples of split rows by
 //                      log-sum-exp (the pages' reduce_segments step).
 // A batch that holds only decode rows (max_query_len == 1) launches no
@@ -20,6 +23,9 @@ cudaError_t launch_decode(const AttnArgs &a, const CUtensorMap &tk, const CUtens
                           int bs, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                            int d, int bs, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                              int d, int bs, cudaStream_t stream);
+bool prefill_tc_supported(int d);
 int decode_tile(int d);
 constexpr int kPrefillTile = 64;
 
@@ -180,7 +186,17 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     cudaError_t e = launch_decode(a, tk, tv, L.d, L.bs, stream);
     if (e != cudaSuccess) return e;
   }
-  if (use_prefill) {
+  // tcgen05 prefill for multi-token sequences when the decode kernel takes the
+  // single-token ones; the mma.sync kernel otherwise (D = 256, Hq/Hk > 8)
+  const bool use_tc = use_decode && prefill_tc_supported(L.d);
+  if (use_prefill && use_tc) {
+    AttnArgs p = a;
+    p.block_q = 128 / a.qpk;
+    p.n_qblocks = L.num_tokens / p.block_q + L.num_seqs;
+    p.skip_single = 1;
+    cudaError_t e = launch_prefill_tc(p, tk, tv, L.d, L.bs, stream);
+    if (e != cudaSuccess) return e;
+  } else if (use_prefill) {
     AttnArgs p = a;
     p.block_q = L.max_query_len <= 1 ? 1 : (64 / a.qpk > 0 ? 64 / a.qpk : 1);
     p.n_qblocks = p.block_q == 1 ? L.num_tokens : L.num_tokens / p.block_q + L.num_seqs;

@@ -89,6 +89,30 @@ struct StageLayout {
   }
 };
 
+// Warp-cooperative search for the sequence owning q-block `target`: the last
+// s with key(s) <= target, key(s) = cu[s] / block_q + s (cu[s] when
+// block_q == 1).  The pages use a binary search over the same keys
+// (_find_seq_idx); here each round samples 32 candidates at once.
+__device__ __forceinline__ int find_seq(const int32_t *cu, int num_seqs, int block_q,
+                                        int target, int lane) {
+  int lo = 0, hi = num_seqs;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    bool le = false;
+    if (idx < hi) {
+      const int v = cu[idx];
+      const int key = block_q == 1 ? v : v / block_q + idx;
+      le = key <= target;
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, le);
+    const int k = ball ? 31 - __clz(ball) : 0;
+    lo = lo + k * step;
+    hi = min(hi, lo + step);
+  }
+  return lo;
+}
+
 // MMA k index -> key within a 16-key block.  A lane reads 4 consecutive keys
 // of one V channel (a 32-bit word): keys 4t..4t+1 serve k = 2t, 2t+1 and keys
 // 4t+2..4t+3 serve k = 2t+8, 2t+9.  K rows and scores follow the same order.
@@ -97,9 +121,10 @@ __device__ __forceinline__ int perm16(int k) {
 }
 
 // The producer warp: walks tiles [tile_lo, tile_lo + n_iter) of sequence
-// `seq`, kv head h, staging each tile's pages through the mbarrier ring.
+// `seq`, kv head h, staging each tile's pages through an NST-stage mbarrier
+// ring (stage s at smem_base + s * L::kBytes).
 // Block-table entries are read 32 pages at a time, one per lane.
-template <class L, int BS>
+template <class L, int BS, int NST = kStages>
 __device__ __forceinline__ void produce_tiles(const AttnArgs &a, const CUtensorMap *tmap_k,
                                               const CUtensorMap *tmap_v, uint32_t smem_base,
                                               uint32_t bar_full, uint32_t bar_empty, int seq,
@@ -110,10 +135,10 @@ __device__ __forceinline__ void produce_tiles(const AttnArgs &a, const CUtensorM
   int page_base = -(1 << 30);
   int my_blk = -1;
   for (int it = 0; it < n_iter; ++it) {
-    const int stage = it % kStages;
-    if (it >= kStages) {
+    const int stage = it % NST;
+    if (it >= NST) {
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / kStages) - 1) & 1);
+      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / NST) - 1) & 1);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);

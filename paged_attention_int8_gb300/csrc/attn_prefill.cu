@@ -33,30 +33,6 @@ struct AttnCfg {
   static_assert(3 * kMergeFields * 32 * 4 <= kStages * L::kBytes, "merge area");
 };
 
-// Warp-cooperative search for the sequence owning q-block `target`: the last
-// s with key(s) <= target, key(s) = cu[s] / block_q + s (cu[s] when
-// block_q == 1).  The pages use a binary search over the same keys
-// (_find_seq_idx); here each round samples 32 candidates at once.
-__device__ __forceinline__ int find_seq(const int32_t *cu, int num_seqs, int block_q,
-                                        int target, int lane) {
-  int lo = 0, hi = num_seqs;
-  while (hi - lo > 1) {
-    const int step = (hi - lo + 31) / 32;
-    const int idx = lo + lane * step;
-    bool le = false;
-    if (idx < hi) {
-      const int v = cu[idx];
-      const int key = block_q == 1 ? v : v / block_q + idx;
-      le = key <= target;
-    }
-    const unsigned ball = __ballot_sync(0xffffffffu, le);
-    const int k = ball ? 31 - __clz(ball) : 0;
-    lo = lo + k * step;
-    hi = min(hi, lo + step);
-  }
-  return lo;
-}
-
 template <int D, int BS>
 __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant__ AttnArgs a,
                                                            const __grid_constant__ CUtensorMap tmap_k,

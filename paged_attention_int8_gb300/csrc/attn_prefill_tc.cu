@@ -1,0 +1,441 @@
+// Prefill kernel on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// Computes, for a q-block of 128 rows (BLOCK_Q = 128 / qpk tokens x the qpk
+// q heads of one kv head, the GQA row tile of
+// "triton_turboquant_unified_attention.py"):
+//   out = softmax_j(scale * q . k_j) v_j over keys j <= seq_len - q_len + i,
+//   lse = ln sum_j exp(scale * q . k_j),
+// over the dequantized q8 pages, in 64-key tiles with an online softmax.
+//
+// Exact scores with one accumulator: each dequantized key value
+// k = code * scale (exact in fp32, 7 x 11 significant bits) is split into two
+// fp16 parts, hi = fp16(k) and lo = fp16(k - hi) (computed by one fp16 FMA,
+// exact while |k| >= 2^-7; below that the error is under 2^-25), and
+// S = Q K_hi^T + Q K_lo^T accumulates both in the same TMEM columns.  q is
+// rounded to fp16 (exact in the normal range).  V is dequantized to fp16
+// (one rounding); P is fp16; the accumulators are fp32 in TMEM.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer: int8 K/V pages + fp16 scales -> 3-stage ring
+//   warp 1      MMA issuer (one thread) and owner of the TMEM allocation
+//   warps 2-5   dequant: int8 ring stage -> fp16 K_hi, K_lo, V' tiles in the
+//               canonical 128-byte-swizzle K-major layout (2-stage ring)
+//   warps 6-9   softmax: one q row per thread (its TMEM lane); load q; per
+//               tile read S from TMEM, online softmax, write P (fp16) to shared
+//               memory; rescale O in TMEM only when a row max rises by more
+//               than 2^8 (exact: the final division uses the same max); the
+//               epilogue reads O from TMEM
+// TMEM: S double-buffered (2 x 64 columns) + O (D columns).
+#include "attn_common.cuh"
+#include "tcgen05.cuh"
+
+namespace paq8 {
+
+template <int D, int BS>
+struct TcCfg {
+  static constexpr int kTile = 64;
+  static constexpr int kM = 128;
+  static constexpr int kSt = 3;
+  static constexpr int kCv = 2;
+  using L = StageLayout<D, BS, kTile>;
+  static constexpr int kKBytes = kTile * D * 2;  // one of K_hi, K_lo: [D/64][64 keys][128 B]
+  static constexpr int kVBytes = D * kTile * 2;  // V': [D rows][64 keys] (one 128-byte chunk)
+  static constexpr int kCvBytes = 2 * kKBytes + kVBytes;
+  static constexpr int kQBytes = kM * D * 2;
+  static constexpr int kPBytes = kM * kTile * 2;
+  static constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
+  static constexpr int kCvOff = align1k(kSt * L::kBytes);
+  static constexpr int kQOff = kCvOff + kCv * kCvBytes;
+  static constexpr int kPOff = kQOff + kQBytes;
+  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kSmem = kBarOff + 256 + 1024;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kOCol = 128;
+  static constexpr float kRescaleThreshold = 8.0f;  // log2 units
+  static_assert(D == 64 || D == 128, "tcgen05 prefill handles D = 64, 128");
+  static_assert(kSmem <= 232448, "shared memory");
+};
+
+// barrier indices (8 bytes each, from kBarOff)
+enum : int {
+  kBarStFull = 0,     // [3] producer -> dequant (tx bytes)
+  kBarStEmpty = 3,    // [3] dequant -> producer (4 warps)
+  kBarCvFull = 6,     // [2] dequant -> MMA (4 warps)
+  kBarCvEmpty = 8,    // [2] MMA commit -> dequant
+  kBarSFull = 10,     // [2] MMA commit -> softmax
+  kBarSEmpty = 12,    // [2] softmax -> MMA (4 warps)
+  kBarPFull = 14,     // [2] softmax -> MMA (4 warps)
+  kBarPEmpty = 16,    // [2] MMA commit -> softmax
+  kBarODone = 18,     // MMA commit after the last PV -> softmax
+  kBarQFull = 19,     // softmax (q written) -> MMA (4 warps)
+  kNumBars = 20
+};
+
+template <int D, int BS>
+__global__ void __launch_bounds__(320, 1)
+    prefill_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
+  using C = TcCfg<D, BS>;
+  using L = typename C::L;
+  constexpr int G = D / 32;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (smem_base - smem_u32(smem_raw));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+
+  // ---- q-block (heaviest first: later q-blocks see more keys)
+  const int bx = a.n_qblocks - 1 - static_cast<int>(blockIdx.x);
+  const int seq = find_seq(a.cu_seqlens_q, a.num_seqs, a.block_q, bx, lane);
+  const int q_start = a.cu_seqlens_q[seq];
+  const int q_end = a.cu_seqlens_q[seq + 1];
+  const int q_len = q_end - q_start;
+  const int tok0 = (bx - (q_start / a.block_q + seq)) * a.block_q;
+  if (tok0 >= q_len) return;
+  if (q_len == 1 && a.skip_single) return;
+  if (q_end > a.num_tokens || q_start < 0) {
+    if (threadIdx.x == 0) flag_status(a.status, PA_DEV_BAD_SEQ);
+    return;
+  }
+  const int seq_len = a.seq_lens[seq];
+  const int ctx = seq_len - q_len;
+  if (ctx < 0) {
+    if (threadIdx.x == 0 && tok0 == 0) flag_status(a.status, PA_DEV_BAD_SEQ);
+    return;
+  }
+  const int n_tok = min(a.block_q, q_len - tok0);
+  const int n_rows = n_tok * a.qpk;
+  const int kv_end = ctx + tok0 + n_tok;
+  const int nt = (kv_end + C::kTile - 1) / C::kTile;
+
+  const uint32_t bars = smem_base + C::kBarOff;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint32_t tmem_slot = bars + 8 * kNumBars;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kSt; ++s) {
+      mbar_init(bar(kBarStFull + s), 1);
+      mbar_init(bar(kBarStEmpty + s), 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarCvFull + s), 4);
+      mbar_init(bar(kBarCvEmpty + s), 1);
+      mbar_init(bar(kBarSFull + s), 1);
+      mbar_init(bar(kBarSEmpty + s), 4);
+      mbar_init(bar(kBarPFull + s), 4);
+      mbar_init(bar(kBarPEmpty + s), 1);
+    }
+    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarQFull), 4);
+    fence_barrier_init();
+  }
+  if (warp == 1) tc::alloc(tmem_slot, C::kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kBarOff + 8 * kNumBars);
+  bool ok = true;
+
+  if (warp == 0) {
+    // ============================================================ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
+    produce_tiles<L, BS, C::kSt>(a, &tmap_k, &tmap_v, smem_base, bar(kBarStFull),
+                                 bar(kBarStEmpty), seq, h, 0, nt, kv_end, lane);
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = tc::idesc_f16(128, 64);
+      constexpr uint32_t id_pv = tc::idesc_f16(128, D);
+      const uint32_t q_addr = smem_base + C::kQOff;
+      auto issue_pv = [&](int i) -> bool {
+        const int pb = i & 1, cb = i % C::kCv;
+        if (!mbar_wait(bar(kBarPFull + pb), (i >> 1) & 1)) return false;
+        tc::fence_after();
+        const uint32_t p_addr = smem_base + C::kPOff + pb * C::kPBytes;
+        const uint32_t v_addr = smem_base + C::kCvOff + cb * C::kCvBytes + 2 * C::kKBytes;
+#pragma unroll
+        for (int ks = 0; ks < C::kTile / 16; ++ks)
+          tc::mma_f16(tmem + C::kOCol, tc::desc_sw128(p_addr + ks * 32),
+                      tc::desc_sw128(v_addr + ks * 32), id_pv, (i > 0 || ks > 0) ? 1u : 0u);
+        tc::commit(bar(kBarPEmpty + pb));
+        tc::commit(bar(kBarCvEmpty + cb));
+        return true;
+      };
+      ok = mbar_wait(bar(kBarQFull), 0);
+      for (int j = 0; ok && j < nt; ++j) {
+        const int cb = j % C::kCv, sb = j & 1;
+        if (!mbar_wait(bar(kBarCvFull + cb), (j / C::kCv) & 1)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait(bar(kBarSEmpty + sb), ((j - 2) >> 1) & 1)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t k_addr = smem_base + C::kCvOff + cb * C::kCvBytes;
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t qa = q_addr + (ks >> 2) * (128 * 128) + (ks & 3) * 32;
+            const uint32_t ka = k_addr + part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
+            tc::mma_f16(tmem + sb * 64, tc::desc_sw128(qa), tc::desc_sw128(ka), id_qk,
+                        (part > 0 || ks > 0) ? 1u : 0u);
+          }
+        tc::commit(bar(kBarSFull + sb));
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && issue_pv(nt - 1)) tc::commit(bar(kBarODone));
+      else ok = false;
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ============================================================ dequant
+    const int t = threadIdx.x - 64;  // 0..127
+    for (int j = 0; j < nt; ++j) {
+      const int sb = j % C::kSt, cb = j % C::kCv;
+      if (!mbar_wait(bar(kBarStFull + sb), (j / C::kSt) & 1)) { ok = false; break; }
+      if (j >= C::kCv && !mbar_wait(bar(kBarCvEmpty + cb), ((j - C::kCv) / C::kCv) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t st = smem_base + sb * L::kBytes;
+      const uint32_t cv = smem_base + C::kCvOff + cb * C::kCvBytes;
+      const int key0 = j * C::kTile;
+      const bool tail = key0 + C::kTile > kv_end;
+      // ---- K: thread -> key r, D/2 channels from c0; hi and lo parts
+      {
+        const int r = t & 63;
+        const int c0 = (t >> 6) * (D / 2);
+        const bool dead = tail && key0 + r >= kv_end;  // stale bytes: write zeros
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 16) {
+          const uint4 codes = lds128(st + L::k_off(r, c0 + c));
+          const uint32_t sbits = lds16(st + L::ks_off(r, (c0 + c) / 32));
+          const uint32_t s2 = dead ? 0u : (sbits | (sbits << 16));
+          uint32_t hw[8], lw[8];
+          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t lo, hi;
+            codes4_to_half2(cw[i], lo, hi);
+            hw[2 * i] = hmul2_u32(lo, s2);
+            hw[2 * i + 1] = hmul2_u32(hi, s2);
+            uint32_t nh0 = hw[2 * i] ^ 0x80008000u, nh1 = hw[2 * i + 1] ^ 0x80008000u;
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i]) : "r"(lo), "r"(s2), "r"(nh0));
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i + 1]) : "r"(hi), "r"(s2), "r"(nh1));
+          }
+          const int c16 = (c0 + c) / 8;
+          sts128(cv + tc::sw128_chunk(r, c16, 64), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+          sts128(cv + tc::sw128_chunk(r, c16 + 1, 64), make_uint4(hw[4], hw[5], hw[6], hw[7]));
+          sts128(cv + C::kKBytes + tc::sw128_chunk(r, c16, 64),
+                 make_uint4(lw[0], lw[1], lw[2], lw[3]));
+          sts128(cv + C::kKBytes + tc::sw128_chunk(r, c16 + 1, 64),
+                 make_uint4(lw[4], lw[5], lw[6], lw[7]));
+        }
+      }
+      // ---- V: thread -> channel ch, 64 * D / 128 keys from k0
+      {
+        constexpr int KPT = 64 * D / 128;
+        const int ch = t % D;
+        const int k0 = (t / D) * KPT;
+        const uint32_t vrow = cv + 2 * C::kKBytes;
+#pragma unroll
+        for (int k = 0; k < KPT; k += 16) {
+          const int key = k0 + k;  // 16 keys: one 16-byte load of codes
+          const uint4 codes = lds128(st + L::v_off(ch, key));
+          const uint4 s01 = lds128(st + L::vs_off(key, ch / 32));
+          const uint4 s23 = lds128(st + L::vs_off(key + 8, ch / 32));
+          uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
+          if (tail) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (key0 + key + 2 * i >= kv_end) sc[i] &= 0xffff0000u;
+              if (key0 + key + 2 * i + 1 >= kv_end) sc[i] &= 0x0000ffffu;
+            }
+          }
+          uint32_t o[8];
+          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t lo, hi;
+            codes4_to_half2(cw[i], lo, hi);
+            o[2 * i] = hmul2_u32(lo, sc[2 * i]);
+            o[2 * i + 1] = hmul2_u32(hi, sc[2 * i + 1]);
+          }
+          sts128(vrow + tc::sw128_chunk(ch, key / 8, D), make_uint4(o[0], o[1], o[2], o[3]));
+          sts128(vrow + tc::sw128_chunk(ch, key / 8 + 1, D), make_uint4(o[4], o[5], o[6], o[7]));
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kBarCvFull + cb));
+        mbar_arrive(bar(kBarStEmpty + sb));
+      }
+    }
+  } else {
+    // ============================================================ softmax
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool valid = row < n_rows;
+    const int tq = valid ? row / a.qpk : 0;
+    const int hh = h * a.qpk + (valid ? row % a.qpk : 0);
+    const int limit = valid ? ctx + tok0 + tq : kv_end - 1;
+    // q row -> fp16, K-major SW128 [D/64][128 rows][128 B]
+    {
+      const uint16_t *src = a.q + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
+      const uint32_t q_addr = smem_base + C::kQOff;
+#pragma unroll
+      for (int c16 = 0; c16 < D / 8; ++c16) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) v = *reinterpret_cast<const uint4 *>(src + c16 * 8);
+        const uint4 f = make_uint4(pack_half2(bf16_lo(v.x), bf16_hi(v.x)),
+                                   pack_half2(bf16_lo(v.y), bf16_hi(v.y)),
+                                   pack_half2(bf16_lo(v.z), bf16_hi(v.z)),
+                                   pack_half2(bf16_lo(v.w), bf16_hi(v.w)));
+        sts128(q_addr + tc::sw128_chunk(row, c16, 128), f);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarQFull));
+    }
+    float m_used = -INFINITY;  // max the accumulator is scaled to (log2 units)
+    float l = 0.0f;
+    bool o_started = false;
+    for (int j = 0; j < nt; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(bar(kBarSFull + sb), (j >> 1) & 1)) { ok = false; break; }
+      tc::fence_after();
+      uint32_t sr[2][32];
+      tc::ld32(t_lane + sb * 64, sr[0]);
+      tc::ld32(t_lane + sb * 64 + 32, sr[1]);
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
+      const int key0 = j * C::kTile;
+      const bool need_mask = key0 + C::kTile - 1 > limit;
+      float s[64];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float v = __uint_as_float(sr[c >> 5][c & 31]) * a.scale_log2;
+        if (need_mask && key0 + c > limit) v = -INFINITY;
+        s[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
+      if (__any_sync(0xffffffffu, rescale && o_started)) {
+        // O holds tiles < j: wait for the PV of tile j - 1, then scale it in TMEM
+        if (!mbar_wait(bar(kBarPEmpty + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+        tc::fence_after();
+        const float f = rescale ? fast_exp2(m_used - m_new) : 1.0f;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t orr[32];
+          tc::ld32(t_lane + C::kOCol + cb * 32, orr);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
+          tc::st32(t_lane + C::kOCol + cb * 32, orr);
+        }
+        tc::wait_st();
+        tc::fence_before();
+      }
+      if (rescale) {
+        l *= fast_exp2(m_used - m_new);  // 0 on the first tile (m_used = -inf)
+        m_used = m_new;
+      }
+      // P = 2^(s - m_used) <= 2^8, fp16
+      uint32_t pw[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = fast_exp2(s[c] - m_used), p1 = fast_exp2(s[c + 1] - m_used);
+        l += p0 + p1;
+        pw[c >> 1] = pack_half2(p0, p1);
+      }
+      if (j >= 2 && !mbar_wait(bar(kBarPEmpty + sb), ((j - 2) >> 1) & 1)) { ok = false; break; }
+      const uint32_t p_addr = smem_base + C::kPOff + sb * C::kPBytes;
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16)
+        sts128(p_addr + tc::sw128_chunk(row, c16, 128),
+               make_uint4(pw[4 * c16], pw[4 * c16 + 1], pw[4 * c16 + 2], pw[4 * c16 + 3]));
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPFull + sb));
+      o_started = true;
+    }
+    // ---- epilogue: O / l -> bf16, lse
+    if (ok && mbar_wait(bar(kBarODone), 0)) {
+      tc::fence_after();
+      const float inv = 1.0f / l;
+      uint16_t *dst = a.out + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t orr[32];
+        tc::ld32(t_lane + C::kOCol + cb * 32, orr);
+        tc::wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf162(__uint_as_float(orr[i]) * inv, __uint_as_float(orr[i + 1]) * inv);
+            w.y = pack_bf162(__uint_as_float(orr[i + 2]) * inv, __uint_as_float(orr[i + 3]) * inv);
+            w.z = pack_bf162(__uint_as_float(orr[i + 4]) * inv, __uint_as_float(orr[i + 5]) * inv);
+            w.w = pack_bf162(__uint_as_float(orr[i + 6]) * inv, __uint_as_float(orr[i + 7]) * inv);
+            *reinterpret_cast<uint4 *>(dst + cb * 32 + i) = w;
+          }
+        }
+      }
+      if (valid && a.lse)
+        a.lse[static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh] = (m_used + log2f(l)) * kLn2;
+    } else {
+      ok = false;
+    }
+  }
+  if (!ok && lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
+
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int BS>
+static cudaError_t launch_prefill_tc_t(const AttnArgs &a, const CUtensorMap &tk,
+                                       const CUtensorMap &tv, cudaStream_t stream) {
+  using C = TcCfg<D, BS>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, BS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  dim3 grid(static_cast<unsigned>(a.n_qblocks), static_cast<unsigned>(a.hk), 1);
+  prefill_tc_kernel<D, BS><<<grid, 320, C::kSmem, stream>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+bool prefill_tc_supported(int d) { return d == 64 || d == 128; }
+
+cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                              int d, int bs, cudaStream_t stream) {
+#define PAQ8_TC_CASE(DD, BB) \
+  if (d == DD && bs == BB) return launch_prefill_tc_t<DD, BB>(a, tk, tv, stream);
+  PAQ8_TC_CASE(64, 16)
+  PAQ8_TC_CASE(64, 32)
+  PAQ8_TC_CASE(128, 16)
+  PAQ8_TC_CASE(128, 32)
+#undef PAQ8_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace paq8
