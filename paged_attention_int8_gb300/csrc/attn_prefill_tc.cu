@@ -16,16 +16,17 @@
 // (one rounding); P is fp16; the accumulators are fp32 in TMEM.
 //
 // Warp roles (320 threads):
-//   warp 0      TMA producer: int8 K/V pages + fp16 scales -> 3-stage ring
+//   warp 0      TMA producer: int8 K/V pages + fp16 scales -> 4-stage ring
 //   warp 1      MMA issuer (one thread) and owner of the TMEM allocation
-//   warps 2-5   dequant: int8 ring stage -> fp16 K_hi, K_lo, V' tiles in the
-//               canonical 128-byte-swizzle K-major layout (2-stage ring)
+//   warps 2-5   dequant: ring stage -> fp16 K_hi/K_lo (2-slot K ring, freed
+//               when its QK MMAs complete) and V' (2-slot V ring, freed when
+//               its PV MMAs complete), canonical 128-byte-swizzle K-major
 //   warps 6-9   softmax: one q row per thread (its TMEM lane); load q; per
-//               tile read S from TMEM, online softmax, write P (fp16) to shared
-//               memory; rescale O in TMEM only when a row max rises by more
-//               than 2^8 (exact: the final division uses the same max); the
-//               epilogue reads O from TMEM
-// TMEM: S double-buffered (2 x 64 columns) + O (D columns).
+//               tile read S from TMEM, online softmax, write P (fp16) back into
+//               the same TMEM columns as the PV MMA's A operand; rescale O in
+//               TMEM only when a row max rises by more than 2^8 (exact: the
+//               final division uses the same max); the epilogue reads O
+// TMEM: two 64-column S/P buffers + O (D columns).
 #include "attn_common.cuh"
 #include "tcgen05.cuh"
 
@@ -35,22 +36,20 @@ template <int D, int BS>
 struct TcCfg {
   static constexpr int kTile = 64;
   static constexpr int kM = 128;
-  static constexpr int kSt = 3;
-  static constexpr int kCv = 2;
+  static constexpr int kSt = 4;  // int8 staging stages (TMA)
   using L = StageLayout<D, BS, kTile>;
   static constexpr int kKBytes = kTile * D * 2;  // one of K_hi, K_lo: [D/64][64 keys][128 B]
-  static constexpr int kVBytes = D * kTile * 2;  // V': [D rows][64 keys] (one 128-byte chunk)
-  static constexpr int kCvBytes = 2 * kKBytes + kVBytes;
+  static constexpr int kKSlot = 2 * kKBytes;     // K ring slot: hi then lo
+  static constexpr int kVBytes = D * kTile * 2;  // V' ring slot: [D rows][64 keys]
   static constexpr int kQBytes = kM * D * 2;
-  static constexpr int kPBytes = kM * kTile * 2;
   static constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
-  static constexpr int kCvOff = align1k(kSt * L::kBytes);
-  static constexpr int kQOff = kCvOff + kCv * kCvBytes;
-  static constexpr int kPOff = kQOff + kQBytes;
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kKOff = align1k(kSt * L::kBytes);
+  static constexpr int kVOff = kKOff + 2 * kKSlot;
+  static constexpr int kQOff = kVOff + 2 * kVBytes;
+  static constexpr int kBarOff = kQOff + kQBytes;
   static constexpr int kSmem = kBarOff + 256 + 1024;
   static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kOCol = 128;
+  static constexpr uint32_t kOCol = 128;  // S/P buffers at columns 0 and 64
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
   static_assert(D == 64 || D == 128, "tcgen05 prefill handles D = 64, 128");
   static_assert(kSmem <= 232448, "shared memory");
@@ -58,17 +57,17 @@ struct TcCfg {
 
 // barrier indices (8 bytes each, from kBarOff)
 enum : int {
-  kBarStFull = 0,     // [3] producer -> dequant (tx bytes)
-  kBarStEmpty = 3,    // [3] dequant -> producer (4 warps)
-  kBarCvFull = 6,     // [2] dequant -> MMA (4 warps)
-  kBarCvEmpty = 8,    // [2] MMA commit -> dequant
-  kBarSFull = 10,     // [2] MMA commit -> softmax
-  kBarSEmpty = 12,    // [2] softmax -> MMA (4 warps)
-  kBarPFull = 14,     // [2] softmax -> MMA (4 warps)
-  kBarPEmpty = 16,    // [2] MMA commit -> softmax
-  kBarODone = 18,     // MMA commit after the last PV -> softmax
-  kBarQFull = 19,     // softmax (q written) -> MMA (4 warps)
-  kNumBars = 20
+  kBarStFull = 0,    // [4] producer -> dequant (tx bytes)
+  kBarStEmpty = 4,   // [4] dequant -> producer (4 warps)
+  kBarKFull = 8,     // [2] dequant -> MMA (4 warps)
+  kBarKEmpty = 10,   // [2] commit after QK -> dequant
+  kBarVFull = 12,    // [2] dequant -> MMA (4 warps)
+  kBarVEmpty = 14,   // [2] commit after PV -> dequant
+  kBarSFull = 16,    // [2] commit after QK -> softmax
+  kBarPFull = 18,    // [2] softmax (P in TMEM) -> MMA (4 warps)
+  kBarPvDone = 20,   // [2] commit after PV -> MMA (S/P buffer reuse), softmax (O ready)
+  kBarQFull = 22,    // softmax (q written) -> MMA (4 warps)
+  kNumBars = 23
 };
 
 template <int D, int BS>
@@ -77,7 +76,6 @@ __global__ void __launch_bounds__(320, 1)
                       const __grid_constant__ CUtensorMap tmap_v) {
   using C = TcCfg<D, BS>;
   using L = typename C::L;
-  constexpr int G = D / 32;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (smem_base - smem_u32(smem_raw));
@@ -119,14 +117,14 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(kBarStEmpty + s), 4);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarCvFull + s), 4);
-      mbar_init(bar(kBarCvEmpty + s), 1);
+      mbar_init(bar(kBarKFull + s), 4);
+      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarVFull + s), 4);
+      mbar_init(bar(kBarVEmpty + s), 1);
       mbar_init(bar(kBarSFull + s), 1);
-      mbar_init(bar(kBarSEmpty + s), 4);
       mbar_init(bar(kBarPFull + s), 4);
-      mbar_init(bar(kBarPEmpty + s), 1);
+      mbar_init(bar(kBarPvDone + s), 1);
     }
-    mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarQFull), 4);
     fence_barrier_init();
   }
@@ -152,58 +150,57 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t id_pv = tc::idesc_f16(128, D);
       const uint32_t q_addr = smem_base + C::kQOff;
       auto issue_pv = [&](int i) -> bool {
-        const int pb = i & 1, cb = i % C::kCv;
-        if (!mbar_wait(bar(kBarPFull + pb), (i >> 1) & 1)) return false;
+        const int b = i & 1;
+        if (!mbar_wait(bar(kBarPFull + b), (i >> 1) & 1)) return false;
+        if (!mbar_wait(bar(kBarVFull + b), (i >> 1) & 1)) return false;
         tc::fence_after();
-        const uint32_t p_addr = smem_base + C::kPOff + pb * C::kPBytes;
-        const uint32_t v_addr = smem_base + C::kCvOff + cb * C::kCvBytes + 2 * C::kKBytes;
+        const uint32_t v_addr = smem_base + C::kVOff + b * C::kVBytes;
 #pragma unroll
         for (int ks = 0; ks < C::kTile / 16; ++ks)
-          tc::mma_f16(tmem + C::kOCol, tc::desc_sw128(p_addr + ks * 32),
-                      tc::desc_sw128(v_addr + ks * 32), id_pv, (i > 0 || ks > 0) ? 1u : 0u);
-        tc::commit(bar(kBarPEmpty + pb));
-        tc::commit(bar(kBarCvEmpty + cb));
+          tc::mma_f16_ts(tmem + C::kOCol, tmem + b * 64 + ks * 8, tc::desc_sw128(v_addr + ks * 32),
+                         id_pv, (i > 0 || ks > 0) ? 1u : 0u);
+        tc::commit(bar(kBarPvDone + b));
+        tc::commit(bar(kBarVEmpty + b));
         return true;
       };
       ok = mbar_wait(bar(kBarQFull), 0);
       for (int j = 0; ok && j < nt; ++j) {
-        const int cb = j % C::kCv, sb = j & 1;
-        if (!mbar_wait(bar(kBarCvFull + cb), (j / C::kCv) & 1)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(bar(kBarSEmpty + sb), ((j - 2) >> 1) & 1)) { ok = false; break; }
+        const int b = j & 1;
+        if (!mbar_wait(bar(kBarKFull + b), (j >> 1) & 1)) { ok = false; break; }
+        // S/P buffer b is free once the PV of tile j - 2 has read its P
+        if (j >= 2 && !mbar_wait(bar(kBarPvDone + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        const uint32_t k_addr = smem_base + C::kCvOff + cb * C::kCvBytes;
+        const uint32_t k_addr = smem_base + C::kKOff + b * C::kKSlot;
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t qa = q_addr + (ks >> 2) * (128 * 128) + (ks & 3) * 32;
             const uint32_t ka = k_addr + part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
-            tc::mma_f16(tmem + sb * 64, tc::desc_sw128(qa), tc::desc_sw128(ka), id_qk,
+            tc::mma_f16(tmem + b * 64, tc::desc_sw128(qa), tc::desc_sw128(ka), id_qk,
                         (part > 0 || ks > 0) ? 1u : 0u);
           }
-        tc::commit(bar(kBarSFull + sb));
+        tc::commit(bar(kBarSFull + b));
+        tc::commit(bar(kBarKEmpty + b));
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
-      if (ok && issue_pv(nt - 1)) tc::commit(bar(kBarODone));
-      else ok = false;
+      if (ok && !issue_pv(nt - 1)) ok = false;
     }
     __syncwarp();
   } else if (warp < 6) {
     // ============================================================ dequant
     const int t = threadIdx.x - 64;  // 0..127
+#pragma unroll 1
     for (int j = 0; j < nt; ++j) {
-      const int sb = j % C::kSt, cb = j % C::kCv;
+      const int sb = j % C::kSt, b = j & 1;
       if (!mbar_wait(bar(kBarStFull + sb), (j / C::kSt) & 1)) { ok = false; break; }
-      if (j >= C::kCv && !mbar_wait(bar(kBarCvEmpty + cb), ((j - C::kCv) / C::kCv) & 1)) {
-        ok = false;
-        break;
-      }
       const uint32_t st = smem_base + sb * L::kBytes;
-      const uint32_t cv = smem_base + C::kCvOff + cb * C::kCvBytes;
       const int key0 = j * C::kTile;
       const bool tail = key0 + C::kTile > kv_end;
       // ---- K: thread -> key r, D/2 channels from c0; hi and lo parts
+      if (j >= 2 && !mbar_wait(bar(kBarKEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
       {
+        const uint32_t kdst = smem_base + C::kKOff + b * C::kKSlot;
         const int r = t & 63;
         const int c0 = (t >> 6) * (D / 2);
         const bool dead = tail && key0 + r >= kv_end;  // stale bytes: write zeros
@@ -212,33 +209,41 @@ __global__ void __launch_bounds__(320, 1)
           const uint4 codes = lds128(st + L::k_off(r, c0 + c));
           const uint32_t sbits = lds16(st + L::ks_off(r, (c0 + c) / 32));
           const uint32_t s2 = dead ? 0u : (sbits | (sbits << 16));
+          const uint32_t ns2 = s2 ^ 0x80008000u;  // -scale
           uint32_t hw[8], lw[8];
           const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint32_t lo, hi;
             codes4_to_half2(cw[i], lo, hi);
+            // hi = fp16(code * s); lo = fp16(code * s - hi), exact: -lo' = code*(-s) + hi
             hw[2 * i] = hmul2_u32(lo, s2);
             hw[2 * i + 1] = hmul2_u32(hi, s2);
-            uint32_t nh0 = hw[2 * i] ^ 0x80008000u, nh1 = hw[2 * i + 1] ^ 0x80008000u;
-            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i]) : "r"(lo), "r"(s2), "r"(nh0));
-            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i + 1]) : "r"(hi), "r"(s2), "r"(nh1));
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i]) : "r"(lo), "r"(ns2), "r"(hw[2 * i]));
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i + 1]) : "r"(hi), "r"(ns2), "r"(hw[2 * i + 1]));
           }
+          // lw holds hi - code*s = -lo (one rounding); flip the sign (exact)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) lw[i] ^= 0x80008000u;
           const int c16 = (c0 + c) / 8;
-          sts128(cv + tc::sw128_chunk(r, c16, 64), make_uint4(hw[0], hw[1], hw[2], hw[3]));
-          sts128(cv + tc::sw128_chunk(r, c16 + 1, 64), make_uint4(hw[4], hw[5], hw[6], hw[7]));
-          sts128(cv + C::kKBytes + tc::sw128_chunk(r, c16, 64),
+          sts128(kdst + tc::sw128_chunk(r, c16, 64), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+          sts128(kdst + tc::sw128_chunk(r, c16 + 1, 64), make_uint4(hw[4], hw[5], hw[6], hw[7]));
+          sts128(kdst + C::kKBytes + tc::sw128_chunk(r, c16, 64),
                  make_uint4(lw[0], lw[1], lw[2], lw[3]));
-          sts128(cv + C::kKBytes + tc::sw128_chunk(r, c16 + 1, 64),
+          sts128(kdst + C::kKBytes + tc::sw128_chunk(r, c16 + 1, 64),
                  make_uint4(lw[4], lw[5], lw[6], lw[7]));
         }
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarKFull + b));
       // ---- V: thread -> channel ch, 64 * D / 128 keys from k0
+      if (j >= 2 && !mbar_wait(bar(kBarVEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
       {
         constexpr int KPT = 64 * D / 128;
         const int ch = t % D;
         const int k0 = (t / D) * KPT;
-        const uint32_t vrow = cv + 2 * C::kKBytes;
+        const uint32_t vrow = smem_base + C::kVOff + b * C::kVBytes;
 #pragma unroll
         for (int k = 0; k < KPT; k += 16) {
           const int key = k0 + k;  // 16 keys: one 16-byte load of codes
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(320, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(kBarCvFull + cb));
+        mbar_arrive(bar(kBarVFull + b));
         mbar_arrive(bar(kBarStEmpty + sb));
       }
     }
@@ -282,6 +287,7 @@ __global__ void __launch_bounds__(320, 1)
     const int tq = valid ? row / a.qpk : 0;
     const int hh = h * a.qpk + (valid ? row % a.qpk : 0);
     const int limit = valid ? ctx + tok0 + tq : kv_end - 1;
+    const float sl2 = a.scale_log2;
     // q row -> fp16, K-major SW128 [D/64][128 rows][128 B]
     {
       const uint16_t *src = a.q + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
@@ -302,37 +308,44 @@ __global__ void __launch_bounds__(320, 1)
     }
     float m_used = -INFINITY;  // max the accumulator is scaled to (log2 units)
     float l = 0.0f;
-    bool o_started = false;
+#pragma unroll 1
     for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(bar(kBarSFull + sb), (j >> 1) & 1)) { ok = false; break; }
+      const int b = j & 1;
+      if (!mbar_wait(bar(kBarSFull + b), (j >> 1) & 1)) { ok = false; break; }
       tc::fence_after();
-      uint32_t sr[2][32];
-      tc::ld32(t_lane + sb * 64, sr[0]);
-      tc::ld32(t_lane + sb * 64 + 32, sr[1]);
+      uint32_t sr[64];
+      tc::ld32(t_lane + b * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tc::ld32(t_lane + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
       const int key0 = j * C::kTile;
       const bool need_mask = key0 + C::kTile - 1 > limit;
-      float s[64];
+      // tile max of the scaled scores (scale > 0 typical; a negative scale
+      // flips max and min)
       float mx = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float v = __uint_as_float(sr[c >> 5][c & 31]) * a.scale_log2;
-        if (need_mask && key0 + c > limit) v = -INFINITY;
-        s[c] = v;
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < 64; ++c) {
+          const float v = key0 + c > limit ? -INFINITY : __uint_as_float(sr[c]) * sl2;
+          mx = fmaxf(mx, v);
+          sr[c] = __float_as_uint(v);
+        }
+      } else {
+        float hi = -INFINITY, lo = INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          hi = fmaxf(hi, __uint_as_float(sr[c]));
+          lo = fminf(lo, __uint_as_float(sr[c]));
+        }
+        mx = sl2 >= 0.0f ? hi * sl2 : lo * sl2;
       }
       const float m_new = fmaxf(m_used, mx);
       const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
-      if (__any_sync(0xffffffffu, rescale && o_started)) {
+      if (__any_sync(0xffffffffu, rescale && j > 0)) {
         // O holds tiles < j: wait for the PV of tile j - 1, then scale it in TMEM
-        if (!mbar_wait(bar(kBarPEmpty + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(bar(kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
         const float f = rescale ? fast_exp2(m_used - m_new) : 1.0f;
-#pragma unroll
+#pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t orr[32];
           tc::ld32(t_lane + C::kOCol + cb * 32, orr);
@@ -342,38 +355,42 @@ __global__ void __launch_bounds__(320, 1)
           tc::st32(t_lane + C::kOCol + cb * 32, orr);
         }
         tc::wait_st();
-        tc::fence_before();
       }
       if (rescale) {
         l *= fast_exp2(m_used - m_new);  // 0 on the first tile (m_used = -inf)
         m_used = m_new;
       }
-      // P = 2^(s - m_used) <= 2^8, fp16
+      // P = 2^(s * scale - m_used) <= 2^8, fp16, into the S buffer's TMEM columns
       uint32_t pw[32];
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = fast_exp2(s[c] - m_used), p1 = fast_exp2(s[c + 1] - m_used);
-        l += p0 + p1;
-        pw[c >> 1] = pack_half2(p0, p1);
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
+          const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
+          l += p0 + p1;
+          pw[c >> 1] = pack_half2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_used));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_used));
+          l += p0 + p1;
+          pw[c >> 1] = pack_half2(p0, p1);
+        }
       }
-      if (j >= 2 && !mbar_wait(bar(kBarPEmpty + sb), ((j - 2) >> 1) & 1)) { ok = false; break; }
-      const uint32_t p_addr = smem_base + C::kPOff + sb * C::kPBytes;
-#pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16)
-        sts128(p_addr + tc::sw128_chunk(row, c16, 128),
-               make_uint4(pw[4 * c16], pw[4 * c16 + 1], pw[4 * c16 + 2], pw[4 * c16 + 3]));
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::st32(t_lane + b * 64, pw);
+      tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + sb));
-      o_started = true;
+      if (lane == 0) mbar_arrive(bar(kBarPFull + b));
     }
     // ---- epilogue: O / l -> bf16, lse
-    if (ok && mbar_wait(bar(kBarODone), 0)) {
+    if (ok && mbar_wait(bar(kBarPvDone + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1)) {
       tc::fence_after();
       const float inv = 1.0f / l;
       uint16_t *dst = a.out + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         uint32_t orr[32];
         tc::ld32(t_lane + C::kOCol + cb * 32, orr);
