@@ -5,7 +5,7 @@
 //  * decode_kernel  -- single-token sequences when Hq/Hk <= 8 (swap-AB form),
 //                      split into KV segments (the pages' 3D kernel);
 //  * prefill_tc_kernel -- multi-token sequences on tcgen05/TMEM, q-blocks of
-//                      128/qpk tokens (D = 64, 128 with Hq/Hk <= 8);
+//                      256/qpk tokens (D = 64, 128 with Hq/Hk <= 8);
 //  * prefill_kernel -- otherwise every other sequence on mma.sync, in
 //                      q-blocks of 64/qpk tokens (the pages' unified 2D
 //                      kernel); it also takes the single-token rows when
@@ -26,6 +26,7 @@ cudaError_t launch_prefill(const AttnArgs &a, const CUtensorMap &tk, const CUten
 cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                               int d, int bs, cudaStream_t stream);
 bool prefill_tc_supported(int d);
+int prefill_tc_rows();
 int decode_tile(int d);
 constexpr int kPrefillTile = 64;
 
@@ -191,7 +192,7 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   const bool use_tc = use_decode && prefill_tc_supported(L.d);
   if (use_prefill && use_tc) {
     AttnArgs p = a;
-    p.block_q = 128 / a.qpk;
+    p.block_q = prefill_tc_rows() / a.qpk;
     p.n_qblocks = L.num_tokens / p.block_q + L.num_seqs;
     p.skip_single = 1;
     cudaError_t e = launch_prefill_tc(p, tk, tv, L.d, L.bs, stream);

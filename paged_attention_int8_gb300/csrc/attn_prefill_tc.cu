@@ -1,6 +1,6 @@
 // Prefill kernel on the 5th-generation tensor cores (tcgen05, TMEM).
 //
-// Computes, for a q-block of 128 rows (BLOCK_Q = 128 / qpk tokens x the qpk
+// Computes, for a q-block of 256 rows (BLOCK_Q = 256 / qpk tokens x the qpk
 // q heads of one kv head, the GQA row tile of
 // "triton_turboquant_unified_attention.py"):
 //   out = softmax_j(scale * q . k_j) v_j over keys j <= seq_len - q_len + i,
@@ -9,24 +9,30 @@
 //
 // Exact scores with one accumulator: each dequantized key value
 // k = code * scale (exact in fp32, 7 x 11 significant bits) is split into two
-// fp16 parts, hi = fp16(k) and lo = fp16(k - hi) (computed by one fp16 FMA,
-// exact while |k| >= 2^-7; below that the error is under 2^-25), and
+// fp16 parts, hi = fp16(k) and lo = fp16(k - hi) (one fp16 FMA, exact while
+// |k| >= 2^-7; below that the error is under 2^-25), and
 // S = Q K_hi^T + Q K_lo^T accumulates both in the same TMEM columns.  q is
 // rounded to fp16 (exact in the normal range).  V is dequantized to fp16
 // (one rounding); P is fp16; the accumulators are fp32 in TMEM.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: int8 K/V pages + fp16 scales -> 4-stage ring
-//   warp 1      MMA issuer (one thread) and owner of the TMEM allocation
-//   warps 2-5   dequant: ring stage -> fp16 K_hi/K_lo (2-slot K ring, freed
-//               when its QK MMAs complete) and V' (2-slot V ring, freed when
-//               its PV MMAs complete), canonical 128-byte-swizzle K-major
-//   warps 6-9   softmax: one q row per thread (its TMEM lane); load q; per
-//               tile read S from TMEM, online softmax, write P (fp16) back into
-//               the same TMEM columns as the PV MMA's A operand; rescale O in
-//               TMEM only when a row max rises by more than 2^8 (exact: the
-//               final division uses the same max); the epilogue reads O
-// TMEM: two 64-column S/P buffers + O (D columns).
+// The 256 rows are two 128-row halves (the MMA's M) that share every
+// converted K/V tile, so the int8 -> fp16 work per FLOP is halved.
+// Warp roles (448 threads):
+//   warp 0      TMA producer: int8 K/V pages + fp16 scales -> 3-stage ring
+//   warp 1      MMA issuer (one thread: QK of tile j for both halves, then PV
+//               of tile j - 1) and owner of the TMEM allocation
+//   warps 2-3   K dequant: ring stage -> fp16 K_hi/K_lo (2-slot K ring, a
+//               slot freed when both halves' QK MMAs complete)
+//   warps 4-5   V dequant: ring stage -> fp16 V' (2-slot V ring, freed when
+//               both halves' PV MMAs complete); both in the canonical
+//               128-byte-swizzle K-major layout
+//   warps 6-9   softmax of half 0, warps 10-13 of half 1: one q row per
+//               thread (its TMEM lane); load q; per tile read S from TMEM,
+//               online softmax, write P (fp16) back into the same TMEM columns
+//               as the PV MMA's A operand; rescale O in TMEM only when a row
+//               max rises by more than 2^8 (exact: the final division uses the
+//               same max); the epilogue reads O
+// TMEM (512 columns): per half, two 64-column S/P buffers + O (D columns).
 #include "attn_common.cuh"
 #include "tcgen05.cuh"
 
@@ -35,43 +41,46 @@ namespace paq8 {
 template <int D, int BS>
 struct TcCfg {
   static constexpr int kTile = 64;
-  static constexpr int kM = 128;
-  static constexpr int kSt = 4;  // int8 staging stages (TMA)
+  static constexpr int kHalves = 2;
+  static constexpr int kRows = 128 * kHalves;
+  static constexpr int kSt = 3;  // int8 staging stages (TMA)
+  static constexpr int kWarps = 14;
   using L = StageLayout<D, BS, kTile>;
   static constexpr int kKBytes = kTile * D * 2;  // one of K_hi, K_lo: [D/64][64 keys][128 B]
   static constexpr int kKSlot = 2 * kKBytes;     // K ring slot: hi then lo
   static constexpr int kVBytes = D * kTile * 2;  // V' ring slot: [D rows][64 keys]
-  static constexpr int kQBytes = kM * D * 2;
+  static constexpr int kQHalf = 128 * D * 2;     // one half's q: [D/64][128 rows][128 B]
   static constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
   static constexpr int kKOff = align1k(kSt * L::kBytes);
   static constexpr int kVOff = kKOff + 2 * kKSlot;
   static constexpr int kQOff = kVOff + 2 * kVBytes;
-  static constexpr int kBarOff = kQOff + kQBytes;
+  static constexpr int kBarOff = kQOff + kHalves * kQHalf;
   static constexpr int kSmem = kBarOff + 256 + 1024;
-  static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kOCol = 128;  // S/P buffers at columns 0 and 64
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kHalfCols = 256;  // per half: S/P at +0, +64; O at +128
+  static constexpr uint32_t kOCol = 128;
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
   static_assert(D == 64 || D == 128, "tcgen05 prefill handles D = 64, 128");
   static_assert(kSmem <= 232448, "shared memory");
 };
 
-// barrier indices (8 bytes each, from kBarOff)
+// barrier indices (8 bytes each, from kBarOff); [half][b] = base + 2 half + b
 enum : int {
-  kBarStFull = 0,    // [4] producer -> dequant (tx bytes)
-  kBarStEmpty = 4,   // [4] dequant -> producer (4 warps)
-  kBarKFull = 8,     // [2] dequant -> MMA (4 warps)
-  kBarKEmpty = 10,   // [2] commit after QK -> dequant
-  kBarVFull = 12,    // [2] dequant -> MMA (4 warps)
-  kBarVEmpty = 14,   // [2] commit after PV -> dequant
-  kBarSFull = 16,    // [2] commit after QK -> softmax
-  kBarPFull = 18,    // [2] softmax (P in TMEM) -> MMA (4 warps)
-  kBarPvDone = 20,   // [2] commit after PV -> MMA (S/P buffer reuse), softmax (O ready)
-  kBarQFull = 22,    // softmax (q written) -> MMA (4 warps)
-  kNumBars = 23
+  kBarStFull = 0,    // [3] producer -> dequant (tx bytes)
+  kBarStEmpty = 3,   // [3] dequant -> producer (4 warps)
+  kBarKFull = 6,     // [2] K dequant -> MMA (2 warps)
+  kBarKEmpty = 8,    // [2] commit after both halves' QK -> K dequant
+  kBarVFull = 10,    // [2] V dequant -> MMA (2 warps)
+  kBarVEmpty = 12,   // [2] commit after both halves' PV -> V dequant
+  kBarSFull = 14,    // [2][2] commit after QK -> softmax of the half
+  kBarPFull = 18,    // [2][2] softmax (P in TMEM) -> MMA (4 warps)
+  kBarPvDone = 22,   // [2][2] commit after PV -> MMA (S/P reuse), softmax (O ready)
+  kBarQFull = 26,    // softmax (q written) -> MMA (8 warps)
+  kNumBars = 27
 };
 
 template <int D, int BS>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     prefill_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
   using C = TcCfg<D, BS>;
@@ -107,6 +116,8 @@ __global__ void __launch_bounds__(320, 1)
   const int n_rows = n_tok * a.qpk;
   const int kv_end = ctx + tok0 + n_tok;
   const int nt = (kv_end + C::kTile - 1) / C::kTile;
+  // half 1 holds no valid row when the block is short: it is then skipped
+  const int halves = n_rows > 128 ? 2 : 1;
 
   const uint32_t bars = smem_base + C::kBarOff;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
@@ -117,15 +128,17 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(kBarStEmpty + s), 4);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarKFull + s), 4);
+      mbar_init(bar(kBarKFull + s), 2);
       mbar_init(bar(kBarKEmpty + s), 1);
-      mbar_init(bar(kBarVFull + s), 4);
+      mbar_init(bar(kBarVFull + s), 2);
       mbar_init(bar(kBarVEmpty + s), 1);
+    }
+    for (int s = 0; s < 4; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarPFull + s), 4);
       mbar_init(bar(kBarPvDone + s), 1);
     }
-    mbar_init(bar(kBarQFull), 4);
+    mbar_init(bar(kBarQFull), 8);
     fence_barrier_init();
   }
   if (warp == 1) tc::alloc(tmem_slot, C::kTmemCols);
@@ -148,18 +161,20 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t id_qk = tc::idesc_f16(128, 64);
       constexpr uint32_t id_pv = tc::idesc_f16(128, D);
-      const uint32_t q_addr = smem_base + C::kQOff;
       auto issue_pv = [&](int i) -> bool {
         const int b = i & 1;
-        if (!mbar_wait(bar(kBarPFull + b), (i >> 1) & 1)) return false;
         if (!mbar_wait(bar(kBarVFull + b), (i >> 1) & 1)) return false;
-        tc::fence_after();
         const uint32_t v_addr = smem_base + C::kVOff + b * C::kVBytes;
+        for (int hf = 0; hf < halves; ++hf) {
+          if (!mbar_wait(bar(kBarPFull + 2 * hf + b), (i >> 1) & 1)) return false;
+          tc::fence_after();
+          const uint32_t base = tmem + hf * C::kHalfCols;
 #pragma unroll
-        for (int ks = 0; ks < C::kTile / 16; ++ks)
-          tc::mma_f16_ts(tmem + C::kOCol, tmem + b * 64 + ks * 8, tc::desc_sw128(v_addr + ks * 32),
-                         id_pv, (i > 0 || ks > 0) ? 1u : 0u);
-        tc::commit(bar(kBarPvDone + b));
+          for (int ks = 0; ks < C::kTile / 16; ++ks)
+            tc::mma_f16_ts(base + C::kOCol, base + b * 64 + ks * 8,
+                           tc::desc_sw128(v_addr + ks * 32), id_pv, (i > 0 || ks > 0) ? 1u : 0u);
+          tc::commit(bar(kBarPvDone + 2 * hf + b));
+        }
         tc::commit(bar(kBarVEmpty + b));
         return true;
       };
@@ -167,20 +182,27 @@ __global__ void __launch_bounds__(320, 1)
       for (int j = 0; ok && j < nt; ++j) {
         const int b = j & 1;
         if (!mbar_wait(bar(kBarKFull + b), (j >> 1) & 1)) { ok = false; break; }
-        // S/P buffer b is free once the PV of tile j - 2 has read its P
-        if (j >= 2 && !mbar_wait(bar(kBarPvDone + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
-        tc::fence_after();
         const uint32_t k_addr = smem_base + C::kKOff + b * C::kKSlot;
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t qa = q_addr + (ks >> 2) * (128 * 128) + (ks & 3) * 32;
-            const uint32_t ka = k_addr + part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
-            tc::mma_f16(tmem + b * 64, tc::desc_sw128(qa), tc::desc_sw128(ka), id_qk,
-                        (part > 0 || ks > 0) ? 1u : 0u);
+        for (int hf = 0; hf < halves; ++hf) {
+          // S/P buffer b of this half is free once the PV of tile j - 2 read its P
+          if (j >= 2 && !mbar_wait(bar(kBarPvDone + 2 * hf + b), ((j - 2) >> 1) & 1)) {
+            ok = false;
+            break;
           }
-        tc::commit(bar(kBarSFull + b));
+          tc::fence_after();
+          const uint32_t q_addr = smem_base + C::kQOff + hf * C::kQHalf;
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t qa = q_addr + (ks >> 2) * (128 * 128) + (ks & 3) * 32;
+              const uint32_t ka = k_addr + part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
+              tc::mma_f16(tmem + hf * C::kHalfCols + b * 64, tc::desc_sw128(qa),
+                          tc::desc_sw128(ka), id_qk, (part > 0 || ks > 0) ? 1u : 0u);
+            }
+          tc::commit(bar(kBarSFull + 2 * hf + b));
+        }
+        if (!ok) break;
         tc::commit(bar(kBarKEmpty + b));
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
@@ -189,7 +211,10 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp < 6) {
     // ============================================================ dequant
-    const int t = threadIdx.x - 64;  // 0..127
+    // warps 2-3: K (hi and lo parts), thread = one key row, all D channels
+    // warps 4-5: V', thread = D / 64 channel rows, all 64 keys
+    const bool k_side = warp < 4;
+    const int t = threadIdx.x - (k_side ? 64 : 128);  // 0..63
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int sb = j % C::kSt, b = j & 1;
@@ -197,17 +222,15 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t st = smem_base + sb * L::kBytes;
       const int key0 = j * C::kTile;
       const bool tail = key0 + C::kTile > kv_end;
-      // ---- K: thread -> key r, D/2 channels from c0; hi and lo parts
-      if (j >= 2 && !mbar_wait(bar(kBarKEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
-      {
+      if (k_side) {
+        if (j >= 2 && !mbar_wait(bar(kBarKEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
         const uint32_t kdst = smem_base + C::kKOff + b * C::kKSlot;
-        const int r = t & 63;
-        const int c0 = (t >> 6) * (D / 2);
+        const int r = t;
         const bool dead = tail && key0 + r >= kv_end;  // stale bytes: write zeros
-#pragma unroll
-        for (int c = 0; c < D / 2; c += 16) {
-          const uint4 codes = lds128(st + L::k_off(r, c0 + c));
-          const uint32_t sbits = lds16(st + L::ks_off(r, (c0 + c) / 32));
+#pragma unroll 2
+        for (int c = 0; c < D; c += 16) {
+          const uint4 codes = lds128(st + L::k_off(r, c));
+          const uint32_t sbits = lds16(st + L::ks_off(r, c / 32));
           const uint32_t s2 = dead ? 0u : (sbits | (sbits << 16));
           const uint32_t ns2 = s2 ^ 0x80008000u;  // -scale
           uint32_t hw[8], lw[8];
@@ -216,16 +239,17 @@ __global__ void __launch_bounds__(320, 1)
           for (int i = 0; i < 4; ++i) {
             uint32_t lo, hi;
             codes4_to_half2(cw[i], lo, hi);
-            // hi = fp16(code * s); lo = fp16(code * s - hi), exact: -lo' = code*(-s) + hi
+            // hi = fp16(code * s); code * (-s) + hi = -(code * s - hi), one rounding
             hw[2 * i] = hmul2_u32(lo, s2);
             hw[2 * i + 1] = hmul2_u32(hi, s2);
             asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i]) : "r"(lo), "r"(ns2), "r"(hw[2 * i]));
-            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i + 1]) : "r"(hi), "r"(ns2), "r"(hw[2 * i + 1]));
+            asm("fma.rn.f16x2 %0, %1, %2, %3;"
+                : "=r"(lw[2 * i + 1])
+                : "r"(hi), "r"(ns2), "r"(hw[2 * i + 1]));
           }
-          // lw holds hi - code*s = -lo (one rounding); flip the sign (exact)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) lw[i] ^= 0x80008000u;
-          const int c16 = (c0 + c) / 8;
+          for (int i = 0; i < 8; ++i) lw[i] ^= 0x80008000u;  // lo = -(hi - code * s), exact
+          const int c16 = c / 8;
           sts128(kdst + tc::sw128_chunk(r, c16, 64), make_uint4(hw[0], hw[1], hw[2], hw[3]));
           sts128(kdst + tc::sw128_chunk(r, c16 + 1, 64), make_uint4(hw[4], hw[5], hw[6], hw[7]));
           sts128(kdst + C::kKBytes + tc::sw128_chunk(r, c16, 64),
@@ -233,66 +257,69 @@ __global__ void __launch_bounds__(320, 1)
           sts128(kdst + C::kKBytes + tc::sw128_chunk(r, c16 + 1, 64),
                  make_uint4(lw[4], lw[5], lw[6], lw[7]));
         }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarKFull + b));
-      // ---- V: thread -> channel ch, 64 * D / 128 keys from k0
-      if (j >= 2 && !mbar_wait(bar(kBarVEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
-      {
-        constexpr int KPT = 64 * D / 128;
-        const int ch = t % D;
-        const int k0 = (t / D) * KPT;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(kBarKFull + b));
+          mbar_arrive(bar(kBarStEmpty + sb));
+        }
+      } else {
+        if (j >= 2 && !mbar_wait(bar(kBarVEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
         const uint32_t vrow = smem_base + C::kVOff + b * C::kVBytes;
 #pragma unroll
-        for (int k = 0; k < KPT; k += 16) {
-          const int key = k0 + k;  // 16 keys: one 16-byte load of codes
-          const uint4 codes = lds128(st + L::v_off(ch, key));
-          const uint4 s01 = lds128(st + L::vs_off(key, ch / 32));
-          const uint4 s23 = lds128(st + L::vs_off(key + 8, ch / 32));
-          uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
-          if (tail) {
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int ch = t + 64 * cc;
+#pragma unroll 2
+          for (int key = 0; key < C::kTile; key += 16) {  // 16 keys: one 16-byte load
+            const uint4 codes = lds128(st + L::v_off(ch, key));
+            const uint4 s01 = lds128(st + L::vs_off(key, ch / 32));
+            const uint4 s23 = lds128(st + L::vs_off(key + 8, ch / 32));
+            uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
+            if (tail) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (key0 + key + 2 * i >= kv_end) sc[i] &= 0xffff0000u;
-              if (key0 + key + 2 * i + 1 >= kv_end) sc[i] &= 0x0000ffffu;
+              for (int i = 0; i < 8; ++i) {
+                if (key0 + key + 2 * i >= kv_end) sc[i] &= 0xffff0000u;
+                if (key0 + key + 2 * i + 1 >= kv_end) sc[i] &= 0x0000ffffu;
+              }
             }
-          }
-          uint32_t o[8];
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+            uint32_t o[8];
+            const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t lo, hi;
-            codes4_to_half2(cw[i], lo, hi);
-            o[2 * i] = hmul2_u32(lo, sc[2 * i]);
-            o[2 * i + 1] = hmul2_u32(hi, sc[2 * i + 1]);
+            for (int i = 0; i < 4; ++i) {
+              uint32_t lo, hi;
+              codes4_to_half2(cw[i], lo, hi);
+              o[2 * i] = hmul2_u32(lo, sc[2 * i]);
+              o[2 * i + 1] = hmul2_u32(hi, sc[2 * i + 1]);
+            }
+            sts128(vrow + tc::sw128_chunk(ch, key / 8, D), make_uint4(o[0], o[1], o[2], o[3]));
+            sts128(vrow + tc::sw128_chunk(ch, key / 8 + 1, D), make_uint4(o[4], o[5], o[6], o[7]));
           }
-          sts128(vrow + tc::sw128_chunk(ch, key / 8, D), make_uint4(o[0], o[1], o[2], o[3]));
-          sts128(vrow + tc::sw128_chunk(ch, key / 8 + 1, D), make_uint4(o[4], o[5], o[6], o[7]));
         }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(kBarVFull + b));
-        mbar_arrive(bar(kBarStEmpty + sb));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(kBarVFull + b));
+          mbar_arrive(bar(kBarStEmpty + sb));
+        }
       }
     }
   } else {
     // ============================================================ softmax
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int hf = (warp - 6) >> 2;  // which 128-row half
+    const int quarter = warp & 3;    // TMEM lanes this warp may access
+    const int lrow = quarter * 32 + lane;
+    const int row = hf * 128 + lrow;
+    const uint32_t t_lane = tmem + hf * C::kHalfCols + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool valid = row < n_rows;
     const int tq = valid ? row / a.qpk : 0;
     const int hh = h * a.qpk + (valid ? row % a.qpk : 0);
     const int limit = valid ? ctx + tok0 + tq : kv_end - 1;
     const float sl2 = a.scale_log2;
-    // q row -> fp16, K-major SW128 [D/64][128 rows][128 B]
+    // q row -> fp16, K-major SW128 [D/64][128 rows][128 B] of this half
     {
       const uint16_t *src = a.q + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
-      const uint32_t q_addr = smem_base + C::kQOff;
-#pragma unroll
+      const uint32_t q_addr = smem_base + C::kQOff + hf * C::kQHalf;
+#pragma unroll 4
       for (int c16 = 0; c16 < D / 8; ++c16) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (valid) v = *reinterpret_cast<const uint4 *>(src + c16 * 8);
@@ -300,7 +327,7 @@ __global__ void __launch_bounds__(320, 1)
                                    pack_half2(bf16_lo(v.y), bf16_hi(v.y)),
                                    pack_half2(bf16_lo(v.z), bf16_hi(v.z)),
                                    pack_half2(bf16_lo(v.w), bf16_hi(v.w)));
-        sts128(q_addr + tc::sw128_chunk(row, c16, 128), f);
+        sts128(q_addr + tc::sw128_chunk(lrow, c16, 128), f);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -308,109 +335,116 @@ __global__ void __launch_bounds__(320, 1)
     }
     float m_used = -INFINITY;  // max the accumulator is scaled to (log2 units)
     float l = 0.0f;
+    if (hf < halves) {
 #pragma unroll 1
-    for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait(bar(kBarSFull + b), (j >> 1) & 1)) { ok = false; break; }
-      tc::fence_after();
-      uint32_t sr[64];
-      tc::ld32(t_lane + b * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tc::ld32(t_lane + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tc::wait_ld();
-      const int key0 = j * C::kTile;
-      const bool need_mask = key0 + C::kTile - 1 > limit;
-      // tile max of the scaled scores (scale > 0 typical; a negative scale
-      // flips max and min)
-      float mx = -INFINITY;
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float v = key0 + c > limit ? -INFINITY : __uint_as_float(sr[c]) * sl2;
-          mx = fmaxf(mx, v);
-          sr[c] = __float_as_uint(v);
-        }
-      } else {
-        float hi = -INFINITY, lo = INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          hi = fmaxf(hi, __uint_as_float(sr[c]));
-          lo = fminf(lo, __uint_as_float(sr[c]));
-        }
-        mx = sl2 >= 0.0f ? hi * sl2 : lo * sl2;
-      }
-      const float m_new = fmaxf(m_used, mx);
-      const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
-      if (__any_sync(0xffffffffu, rescale && j > 0)) {
-        // O holds tiles < j: wait for the PV of tile j - 1, then scale it in TMEM
-        if (!mbar_wait(bar(kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+      for (int j = 0; j < nt; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait(bar(kBarSFull + 2 * hf + b), (j >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        const float f = rescale ? fast_exp2(m_used - m_new) : 1.0f;
+        uint32_t sr[64];
+        tc::ld32(t_lane + b * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tc::ld32(t_lane + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tc::wait_ld();
+        const int key0 = j * C::kTile;
+        const bool need_mask = key0 + C::kTile - 1 > limit;
+        // tile max of the scaled scores (a negative scale flips max and min)
+        float mx;
+        if (need_mask) {
+          mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float v = key0 + c > limit ? -INFINITY : __uint_as_float(sr[c]) * sl2;
+            mx = fmaxf(mx, v);
+            sr[c] = __float_as_uint(v);
+          }
+        } else if (sl2 >= 0.0f) {
+          float hi = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) hi = fmaxf(hi, __uint_as_float(sr[c]));
+          mx = hi * sl2;
+        } else {
+          float lo = INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) lo = fminf(lo, __uint_as_float(sr[c]));
+          mx = lo * sl2;
+        }
+        const float m_new = fmaxf(m_used, mx);
+        const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
+        if (__any_sync(0xffffffffu, rescale && j > 0)) {
+          // O holds tiles < j: wait for the PV of tile j - 1, then scale it in TMEM
+          if (!mbar_wait(bar(kBarPvDone + 2 * hf + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          const float f = rescale ? fast_exp2(m_used - m_new) : 1.0f;
+#pragma unroll 1
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t orr[32];
+            tc::ld32(t_lane + C::kOCol + cb * 32, orr);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
+            tc::st32(t_lane + C::kOCol + cb * 32, orr);
+          }
+          tc::wait_st();
+        }
+        if (rescale) {
+          l *= fast_exp2(m_used - m_new);  // 0 on the first tile (m_used = -inf)
+          m_used = m_new;
+        }
+        // P = 2^(s * scale - m_used) <= 2^8, fp16, into the S buffer's TMEM columns
+        uint32_t pw[32];
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
+            const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
+            l += p0 + p1;
+            pw[c >> 1] = pack_half2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_used));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_used));
+            l += p0 + p1;
+            pw[c >> 1] = pack_half2(p0, p1);
+          }
+        }
+        tc::st32(t_lane + b * 64, pw);
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPFull + 2 * hf + b));
+      }
+      // ---- epilogue: O / l -> bf16, lse
+      if (ok && mbar_wait(bar(kBarPvDone + 2 * hf + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1)) {
+        tc::fence_after();
+        const float inv = 1.0f / l;
+        uint16_t *dst = a.out + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t orr[32];
           tc::ld32(t_lane + C::kOCol + cb * 32, orr);
           tc::wait_ld();
+          if (valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
-          tc::st32(t_lane + C::kOCol + cb * 32, orr);
-        }
-        tc::wait_st();
-      }
-      if (rescale) {
-        l *= fast_exp2(m_used - m_new);  // 0 on the first tile (m_used = -inf)
-        m_used = m_new;
-      }
-      // P = 2^(s * scale - m_used) <= 2^8, fp16, into the S buffer's TMEM columns
-      uint32_t pw[32];
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
-          const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
-          l += p0 + p1;
-          pw[c >> 1] = pack_half2(p0, p1);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_used));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_used));
-          l += p0 + p1;
-          pw[c >> 1] = pack_half2(p0, p1);
-        }
-      }
-      tc::st32(t_lane + b * 64, pw);
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + b));
-    }
-    // ---- epilogue: O / l -> bf16, lse
-    if (ok && mbar_wait(bar(kBarPvDone + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1)) {
-      tc::fence_after();
-      const float inv = 1.0f / l;
-      uint16_t *dst = a.out + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
-#pragma unroll 1
-      for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t orr[32];
-        tc::ld32(t_lane + C::kOCol + cb * 32, orr);
-        tc::wait_ld();
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            w.x = pack_bf162(__uint_as_float(orr[i]) * inv, __uint_as_float(orr[i + 1]) * inv);
-            w.y = pack_bf162(__uint_as_float(orr[i + 2]) * inv, __uint_as_float(orr[i + 3]) * inv);
-            w.z = pack_bf162(__uint_as_float(orr[i + 4]) * inv, __uint_as_float(orr[i + 5]) * inv);
-            w.w = pack_bf162(__uint_as_float(orr[i + 6]) * inv, __uint_as_float(orr[i + 7]) * inv);
-            *reinterpret_cast<uint4 *>(dst + cb * 32 + i) = w;
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w;
+              w.x = pack_bf162(__uint_as_float(orr[i]) * inv, __uint_as_float(orr[i + 1]) * inv);
+              w.y = pack_bf162(__uint_as_float(orr[i + 2]) * inv, __uint_as_float(orr[i + 3]) * inv);
+              w.z = pack_bf162(__uint_as_float(orr[i + 4]) * inv, __uint_as_float(orr[i + 5]) * inv);
+              w.w = pack_bf162(__uint_as_float(orr[i + 6]) * inv, __uint_as_float(orr[i + 7]) * inv);
+              *reinterpret_cast<uint4 *>(dst + cb * 32 + i) = w;
+            }
           }
         }
+        if (valid && a.lse)
+          a.lse[static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh] = (m_used + log2f(l)) * kLn2;
+      } else {
+        ok = false;
       }
-      if (valid && a.lse)
-        a.lse[static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh] = (m_used + log2f(l)) * kLn2;
-    } else {
-      ok = false;
     }
   }
   if (!ok && lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
@@ -437,11 +471,14 @@ static cudaError_t launch_prefill_tc_t(const AttnArgs &a, const CUtensorMap &tk,
     configured_device = dev;
   }
   dim3 grid(static_cast<unsigned>(a.n_qblocks), static_cast<unsigned>(a.hk), 1);
-  prefill_tc_kernel<D, BS><<<grid, 320, C::kSmem, stream>>>(a, tk, tv);
+  prefill_tc_kernel<D, BS><<<grid, C::kWarps * 32, C::kSmem, stream>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
 bool prefill_tc_supported(int d) { return d == 64 || d == 128; }
+
+// rows of one q-block of the tcgen05 prefill kernel
+int prefill_tc_rows() { return 256; }
 
 cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                               int d, int bs, cudaStream_t stream) {
