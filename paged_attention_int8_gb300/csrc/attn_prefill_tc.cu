@@ -74,7 +74,7 @@ enum : int {
   kBarVEmpty = 12,   // [2] commit after both halves' PV -> V dequant
   kBarSFull = 14,    // [2][2] commit after QK -> softmax of the half
   kBarPFull = 18,    // [2][2] softmax (P in TMEM) -> MMA (4 warps)
-  kBarPvDone = 22,   // [2][2] commit after PV -> MMA (S/P reuse), softmax (O ready)
+  kBarPvDone = 22,   // [2][2] commit after PV -> softmax (O ready for a rescale / the epilogue)
   kBarQFull = 26,    // softmax (q written) -> MMA (8 warps)
   kNumBars = 27
 };
@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(448, 1)
     // ============================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = tc::idesc_f16(128, 64);
+      constexpr uint32_t id_qk_neg = id_qk | (1u << 14);  // negate B: K_lo is stored as -lo
       constexpr uint32_t id_pv = tc::idesc_f16(128, D);
       auto issue_pv = [&](int i) -> bool {
         const int b = i & 1;
@@ -184,11 +185,10 @@ __global__ void __launch_bounds__(448, 1)
         if (!mbar_wait(bar(kBarKFull + b), (j >> 1) & 1)) { ok = false; break; }
         const uint32_t k_addr = smem_base + C::kKOff + b * C::kKSlot;
         for (int hf = 0; hf < halves; ++hf) {
-          // S/P buffer b of this half is free once the PV of tile j - 2 read its P
-          if (j >= 2 && !mbar_wait(bar(kBarPvDone + 2 * hf + b), ((j - 2) >> 1) & 1)) {
-            ok = false;
-            break;
-          }
+          // S/P buffer b of this half was last read (as P) by the PV of tile
+          // j - 2, issued earlier by this thread: tcgen05.mma operations from
+          // one thread execute in issue order, so no wait is needed; the
+          // softmax finished with S(j - 2) before that PV was issued.
           tc::fence_after();
           const uint32_t q_addr = smem_base + C::kQOff + hf * C::kQHalf;
 #pragma unroll
@@ -198,11 +198,11 @@ __global__ void __launch_bounds__(448, 1)
               const uint32_t qa = q_addr + (ks >> 2) * (128 * 128) + (ks & 3) * 32;
               const uint32_t ka = k_addr + part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
               tc::mma_f16(tmem + hf * C::kHalfCols + b * 64, tc::desc_sw128(qa),
-                          tc::desc_sw128(ka), id_qk, (part > 0 || ks > 0) ? 1u : 0u);
+                          tc::desc_sw128(ka), part ? id_qk_neg : id_qk,
+                          (part > 0 || ks > 0) ? 1u : 0u);
             }
           tc::commit(bar(kBarSFull + 2 * hf + b));
         }
-        if (!ok) break;
         tc::commit(bar(kBarKEmpty + b));
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
@@ -239,7 +239,8 @@ __global__ void __launch_bounds__(448, 1)
           for (int i = 0; i < 4; ++i) {
             uint32_t lo, hi;
             codes4_to_half2(cw[i], lo, hi);
-            // hi = fp16(code * s); code * (-s) + hi = -(code * s - hi), one rounding
+            // hi = fp16(code * s); lw = code * (-s) + hi = -lo (one rounding, exact);
+            // the QK MMA of the lo part negates B, so it adds q . lo
             hw[2 * i] = hmul2_u32(lo, s2);
             hw[2 * i + 1] = hmul2_u32(hi, s2);
             asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lw[2 * i]) : "r"(lo), "r"(ns2), "r"(hw[2 * i]));
@@ -247,8 +248,6 @@ __global__ void __launch_bounds__(448, 1)
                 : "=r"(lw[2 * i + 1])
                 : "r"(hi), "r"(ns2), "r"(hw[2 * i + 1]));
           }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) lw[i] ^= 0x80008000u;  // lo = -(hi - code * s), exact
           const int c16 = c / 8;
           sts128(kdst + tc::sw128_chunk(r, c16, 64), make_uint4(hw[0], hw[1], hw[2], hw[3]));
           sts128(kdst + tc::sw128_chunk(r, c16 + 1, 64), make_uint4(hw[4], hw[5], hw[6], hw[7]));
@@ -350,23 +349,29 @@ __global__ void __launch_bounds__(448, 1)
         // tile max of the scaled scores (a negative scale flips max and min)
         float mx;
         if (need_mask) {
-          mx = -INFINITY;
+          float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const float v = key0 + c > limit ? -INFINITY : __uint_as_float(sr[c]) * sl2;
-            mx = fmaxf(mx, v);
+            e[c & 3] = fmaxf(e[c & 3], v);
             sr[c] = __float_as_uint(v);
           }
-        } else if (sl2 >= 0.0f) {
-          float hi = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) hi = fmaxf(hi, __uint_as_float(sr[c]));
-          mx = hi * sl2;
+          mx = fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]));
         } else {
-          float lo = INFINITY;
+          // eight independent chains, then a tree: short dependency paths
+          float e[8];
+          const bool up = sl2 >= 0.0f;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) lo = fminf(lo, __uint_as_float(sr[c]));
-          mx = lo * sl2;
+          for (int k = 0; k < 8; ++k) e[k] = __uint_as_float(sr[k]);
+#pragma unroll
+          for (int c = 8; c < 64; ++c)
+            e[c & 7] = up ? fmaxf(e[c & 7], __uint_as_float(sr[c]))
+                          : fminf(e[c & 7], __uint_as_float(sr[c]));
+#pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) e[k] = up ? fmaxf(e[k], e[k + w]) : fminf(e[k], e[k + w]);
+          mx = e[0] * sl2;
         }
         const float m_new = fmaxf(m_used, mx);
         const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
@@ -395,23 +400,17 @@ __global__ void __launch_bounds__(448, 1)
         }
         // P = 2^(s * scale - m_used) <= 2^8, fp16, into the S buffer's TMEM columns
         uint32_t pw[32];
-        if (need_mask) {
+        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // masked scores are already scaled (and -inf where hidden)
+        const float mul = need_mask ? 1.0f : sl2;
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
-            const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
-            l += p0 + p1;
-            pw[c >> 1] = pack_half2(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sl2, -m_used));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -m_used));
-            l += p0 + p1;
-            pw[c >> 1] = pack_half2(p0, p1);
-          }
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), mul, -m_used));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), mul, -m_used));
+          ls[(c >> 1) & 3] += p0 + p1;
+          pw[c >> 1] = pack_half2(p0, p1);
         }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tc::st32(t_lane + b * 64, pw);
         tc::wait_st();
         tc::fence_before();
