@@ -16,23 +16,35 @@
 // (one rounding); P is fp16; the accumulators are fp32 in TMEM.
 //
 // The 256 rows are two 128-row halves (the MMA's M) that share every
-// converted K/V tile, so the int8 -> fp16 work per FLOP is halved.
-// Warp roles (448 threads):
-//   warp 0      TMA producer: int8 K/V pages + fp16 scales -> 3-stage ring
-//   warp 1      MMA issuer (one thread: QK of tile j for both halves, then PV
-//               of tile j - 1) and owner of the TMEM allocation
-//   warps 2-3   K dequant: ring stage -> fp16 K_hi/K_lo (2-slot K ring, a
+// converted K/V tile, so the int8 -> fp16 work per FLOP is halved.  Both MMA
+// A operands live in TMEM (q for QK, P for PV): shared memory then carries
+// only the K/V tiles (B operands), not a re-read of q for every MMA.
+// Warp roles (448 threads; warp w runs on SM sub-partition w % 4, and the
+// MMA warp shares its sub-partition only with the producer and two softmax
+// warps, so the ALU-heavy dequant warps never delay MMA issue):
+//   warp 5      TMA producer: int8 K/V pages + fp16 scales -> 3-stage ring
+//   warp 1      MMA issuer and owner of the TMEM allocation.  The converged
+//               warp issues through one elected lane, per tile j,
+//               PV(j-1, half 0), QK(j, half 0), PV(j-1, half 1), QK(j, half 1):
+//               while one half's softmax runs, the tensor core works on the
+//               other half
+//   warps 0, 2  K dequant: ring stage -> fp16 K_hi/K_lo (2-slot K ring, a
 //               slot freed when both halves' QK MMAs complete)
-//   warps 4-5   V dequant: ring stage -> fp16 V' (2-slot V ring, freed when
+//   warps 3, 4  V dequant: ring stage -> fp16 V' (2-slot V ring, freed when
 //               both halves' PV MMAs complete); both in the canonical
 //               128-byte-swizzle K-major layout
 //   warps 6-9   softmax of half 0, warps 10-13 of half 1: one q row per
-//               thread (its TMEM lane); load q; per tile read S from TMEM,
-//               online softmax, write P (fp16) back into the same TMEM columns
-//               as the PV MMA's A operand; rescale O in TMEM only when a row
-//               max rises by more than 2^8 (exact: the final division uses the
-//               same max); the epilogue reads O
-// TMEM (512 columns): per half, two 64-column S/P buffers + O (D columns).
+//               thread (its TMEM lane); write q (fp16) into TMEM; per tile read
+//               S from TMEM, online softmax, write P (fp16) back into the same
+//               TMEM columns as the PV MMA's A operand; rescale O in TMEM only
+//               when a row max rises by more than 2^8 (exact: the final
+//               division uses the same max); the epilogue reads O
+// TMEM (512 columns): per half, the S/P buffer (64 columns), q (D/2
+// columns: two fp16 per column) and O (D columns).  A half's next QK is
+// issued after its PV of the previous tile, and tcgen05 MMAs from one thread
+// execute in issue order, so the single S/P buffer is never overwritten
+// early; the commit of QK(j) also implies PV(j-1) is done, so the softmax may
+// rescale O as soon as S(j) is ready.
 #include "attn_common.cuh"
 #include "tcgen05.cuh"
 
@@ -49,22 +61,21 @@ struct TcCfg {
   static constexpr int kKBytes = kTile * D * 2;  // one of K_hi, K_lo: [D/64][64 keys][128 B]
   static constexpr int kKSlot = 2 * kKBytes;     // K ring slot: hi then lo
   static constexpr int kVBytes = D * kTile * 2;  // V' ring slot: [D rows][64 keys]
-  static constexpr int kQHalf = 128 * D * 2;     // one half's q: [D/64][128 rows][128 B]
   static constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
   static constexpr int kKOff = align1k(kSt * L::kBytes);
   static constexpr int kVOff = kKOff + 2 * kKSlot;
-  static constexpr int kQOff = kVOff + 2 * kVBytes;
-  static constexpr int kBarOff = kQOff + kHalves * kQHalf;
+  static constexpr int kBarOff = kVOff + 2 * kVBytes;
   static constexpr int kSmem = kBarOff + 256 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kHalfCols = 256;  // per half: S/P at +0, +64; O at +128
+  static constexpr uint32_t kHalfCols = 256;  // per half: S/P at +0, q at +64, O at +128
+  static constexpr uint32_t kQCol = 64;
   static constexpr uint32_t kOCol = 128;
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
   static_assert(D == 64 || D == 128, "tcgen05 prefill handles D = 64, 128");
   static_assert(kSmem <= 232448, "shared memory");
 };
 
-// barrier indices (8 bytes each, from kBarOff); [half][b] = base + 2 half + b
+// barrier indices (8 bytes each, from kBarOff)
 enum : int {
   kBarStFull = 0,    // [3] producer -> dequant (tx bytes)
   kBarStEmpty = 3,   // [3] dequant -> producer (4 warps)
@@ -72,11 +83,11 @@ enum : int {
   kBarKEmpty = 8,    // [2] commit after both halves' QK -> K dequant
   kBarVFull = 10,    // [2] V dequant -> MMA (2 warps)
   kBarVEmpty = 12,   // [2] commit after both halves' PV -> V dequant
-  kBarSFull = 14,    // [2][2] commit after QK -> softmax of the half
-  kBarPFull = 18,    // [2][2] softmax (P in TMEM) -> MMA (4 warps)
-  kBarPvDone = 22,   // [2][2] commit after PV -> softmax (O ready for a rescale / the epilogue)
-  kBarQFull = 26,    // softmax (q written) -> MMA (8 warps)
-  kNumBars = 27
+  kBarSFull = 14,    // [half] commit after QK -> softmax of the half
+  kBarPFull = 16,    // [half] softmax (P in TMEM) -> MMA (4 warps)
+  kBarPvDone = 18,   // [half] commit after the last PV -> epilogue
+  kBarQFull = 20,    // softmax (q written to TMEM) -> MMA (8 warps)
+  kNumBars = 21
 };
 
 template <int D, int BS>
@@ -133,7 +144,7 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(bar(kBarVFull + s), 2);
       mbar_init(bar(kBarVEmpty + s), 1);
     }
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarPFull + s), 4);
       mbar_init(bar(kBarPvDone + s), 1);
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(448, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kBarOff + 8 * kNumBars);
   bool ok = true;
 
-  if (warp == 0) {
+  if (warp == 5) {
     // ============================================================ producer
     if (lane == 0) {
       prefetch_tensormap(&tmap_k);
@@ -158,63 +169,68 @@ __global__ void __launch_bounds__(448, 1)
                                  bar(kBarStEmpty), seq, h, 0, nt, kv_end, lane);
   } else if (warp == 1) {
     // ============================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_qk = tc::idesc_f16(128, 64);
-      constexpr uint32_t id_qk_neg = id_qk | (1u << 14);  // negate B: K_lo is stored as -lo
-      constexpr uint32_t id_pv = tc::idesc_f16(128, D);
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
-        if (!mbar_wait(bar(kBarVFull + b), (i >> 1) & 1)) return false;
-        const uint32_t v_addr = smem_base + C::kVOff + b * C::kVBytes;
-        for (int hf = 0; hf < halves; ++hf) {
-          if (!mbar_wait(bar(kBarPFull + 2 * hf + b), (i >> 1) & 1)) return false;
-          tc::fence_after();
-          const uint32_t base = tmem + hf * C::kHalfCols;
+    // The whole warp runs this loop (uniform values, no divergence); the
+    // elected lane issues every MMA and commit.
+    const uint32_t leader = tc::elect_one();
+    constexpr uint32_t id_qk = tc::idesc_f16(128, 64);
+    constexpr uint32_t id_qk_neg = id_qk | (1u << 14);  // negate B: K_lo is stored as -lo
+    constexpr uint32_t id_pv = tc::idesc_f16(128, D);
+    auto wait = [&](int i, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar(i), parity)); };
+    // O(half) += P(i, half) V'(i): A = P from the half's S/P columns
+    auto issue_pv = [&](int i, int hf) -> bool {
+      const int b = i & 1;
+      if (hf == 0 && !wait(kBarVFull + b, (i >> 1) & 1)) return false;
+      if (!wait(kBarPFull + hf, i & 1)) return false;
+      tc::fence_after();
+      const uint64_t v_desc = tc::desc_sw128(smem_base + C::kVOff + b * C::kVBytes);
+      const uint32_t base = tmem + hf * C::kHalfCols;
 #pragma unroll
-          for (int ks = 0; ks < C::kTile / 16; ++ks)
-            tc::mma_f16_ts(base + C::kOCol, base + b * 64 + ks * 8,
-                           tc::desc_sw128(v_addr + ks * 32), id_pv, (i > 0 || ks > 0) ? 1u : 0u);
-          tc::commit(bar(kBarPvDone + 2 * hf + b));
+      for (int ks = 0; ks < C::kTile / 16; ++ks)  // +32 bytes of K per step
+        tc::mma_f16_ts_by(leader, base + C::kOCol, base + ks * 8, v_desc + 2 * ks, id_pv,
+                          (i > 0 || ks > 0) ? 1u : 0u);
+      return true;
+    };
+    // S(half) = q K_hi(j)^T - q (-K_lo(j))^T: A = q from the half's TMEM columns
+    auto issue_qk = [&](int j, int hf) {
+      const uint64_t k_desc = tc::desc_sw128(smem_base + C::kKOff + (j & 1) * C::kKSlot);
+      const uint32_t base = tmem + hf * C::kHalfCols;
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
+          tc::mma_f16_ts_by(leader, base, base + C::kQCol + ks * 8, k_desc + (koff >> 4),
+                            part ? id_qk_neg : id_qk, (part > 0 || ks > 0) ? 1u : 0u);
         }
-        tc::commit(bar(kBarVEmpty + b));
-        return true;
-      };
-      ok = mbar_wait(bar(kBarQFull), 0);
-      for (int j = 0; ok && j < nt; ++j) {
-        const int b = j & 1;
-        if (!mbar_wait(bar(kBarKFull + b), (j >> 1) & 1)) { ok = false; break; }
-        const uint32_t k_addr = smem_base + C::kKOff + b * C::kKSlot;
-        for (int hf = 0; hf < halves; ++hf) {
-          // S/P buffer b of this half was last read (as P) by the PV of tile
-          // j - 2, issued earlier by this thread: tcgen05.mma operations from
-          // one thread execute in issue order, so no wait is needed; the
-          // softmax finished with S(j - 2) before that PV was issued.
-          tc::fence_after();
-          const uint32_t q_addr = smem_base + C::kQOff + hf * C::kQHalf;
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t qa = q_addr + (ks >> 2) * (128 * 128) + (ks & 3) * 32;
-              const uint32_t ka = k_addr + part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
-              tc::mma_f16(tmem + hf * C::kHalfCols + b * 64, tc::desc_sw128(qa),
-                          tc::desc_sw128(ka), part ? id_qk_neg : id_qk,
-                          (part > 0 || ks > 0) ? 1u : 0u);
-            }
-          tc::commit(bar(kBarSFull + 2 * hf + b));
-        }
-        tc::commit(bar(kBarKEmpty + b));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      tc::commit_by(leader, bar(kBarSFull + hf));
+    };
+    ok = wait(kBarQFull, 0);
+    tc::fence_after();
+    for (int j = 0; ok && j < nt; ++j) {
+      const int b = j & 1;
+      for (int hf = 0; hf < halves; ++hf) {
+        // the half's S/P buffer is free once PV(j - 1) is issued: MMAs from
+        // this warp execute in order
+        if (j >= 1 && !issue_pv(j - 1, hf)) { ok = false; break; }
+        if (hf == 0 && !wait(kBarKFull + b, (j >> 1) & 1)) { ok = false; break; }
+        tc::fence_after();
+        issue_qk(j, hf);
       }
-      if (ok && !issue_pv(nt - 1)) ok = false;
+      if (!ok) break;
+      tc::commit_by(leader, bar(kBarKEmpty + b));
+      if (j >= 1) tc::commit_by(leader, bar(kBarVEmpty + (b ^ 1)));
+    }
+    for (int hf = 0; ok && hf < halves; ++hf) {
+      if (!issue_pv(nt - 1, hf)) { ok = false; break; }
+      tc::commit_by(leader, bar(kBarPvDone + hf));
     }
     __syncwarp();
   } else if (warp < 6) {
     // ============================================================ dequant
-    // warps 2-3: K (hi and lo parts), thread = one key row, all D channels
-    // warps 4-5: V', thread = D / 64 channel rows, all 64 keys
-    const bool k_side = warp < 4;
-    const int t = threadIdx.x - (k_side ? 64 : 128);  // 0..63
+    // warps 0, 2: K (hi and lo parts), thread = one key row, all D channels
+    // warps 3, 4: V', thread = D / 64 channel rows, all 64 keys
+    const bool k_side = warp == 0 || warp == 2;
+    const int t = ((warp == 0 || warp == 3) ? 0 : 32) + lane;  // 0..63
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int sb = j % C::kSt, b = j & 1;
@@ -314,21 +330,25 @@ __global__ void __launch_bounds__(448, 1)
     const int hh = h * a.qpk + (valid ? row % a.qpk : 0);
     const int limit = valid ? ctx + tok0 + tq : kv_end - 1;
     const float sl2 = a.scale_log2;
-    // q row -> fp16, K-major SW128 [D/64][128 rows][128 B] of this half
+    // q row -> fp16 pairs in this lane's q columns (the QK MMA's A operand)
     {
       const uint16_t *src = a.q + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
-      const uint32_t q_addr = smem_base + C::kQOff + hf * C::kQHalf;
-#pragma unroll 4
-      for (int c16 = 0; c16 < D / 8; ++c16) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) v = *reinterpret_cast<const uint4 *>(src + c16 * 8);
-        const uint4 f = make_uint4(pack_half2(bf16_lo(v.x), bf16_hi(v.x)),
-                                   pack_half2(bf16_lo(v.y), bf16_hi(v.y)),
-                                   pack_half2(bf16_lo(v.z), bf16_hi(v.z)),
-                                   pack_half2(bf16_lo(v.w), bf16_hi(v.w)));
-        sts128(q_addr + tc::sw128_chunk(lrow, c16, 128), f);
+#pragma unroll 1
+      for (int cb = 0; cb < D / 64; ++cb) {
+        uint32_t qw[32];
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (valid) v = *reinterpret_cast<const uint4 *>(src + cb * 64 + c16 * 8);
+          qw[4 * c16 + 0] = pack_half2(bf16_lo(v.x), bf16_hi(v.x));
+          qw[4 * c16 + 1] = pack_half2(bf16_lo(v.y), bf16_hi(v.y));
+          qw[4 * c16 + 2] = pack_half2(bf16_lo(v.z), bf16_hi(v.z));
+          qw[4 * c16 + 3] = pack_half2(bf16_lo(v.w), bf16_hi(v.w));
+        }
+        tc::st32(t_lane + C::kQCol + cb * 32, qw);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::wait_st();
+      tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarQFull));
     }
@@ -337,12 +357,11 @@ __global__ void __launch_bounds__(448, 1)
     if (hf < halves) {
 #pragma unroll 1
       for (int j = 0; j < nt; ++j) {
-        const int b = j & 1;
-        if (!mbar_wait(bar(kBarSFull + 2 * hf + b), (j >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(bar(kBarSFull + hf), j & 1)) { ok = false; break; }
         tc::fence_after();
         uint32_t sr[64];
-        tc::ld32(t_lane + b * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tc::ld32(t_lane + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tc::ld32(t_lane, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tc::ld32(t_lane + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tc::wait_ld();
         const int key0 = j * C::kTile;
         const bool need_mask = key0 + C::kTile - 1 > limit;
@@ -376,12 +395,8 @@ __global__ void __launch_bounds__(448, 1)
         const float m_new = fmaxf(m_used, mx);
         const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
         if (__any_sync(0xffffffffu, rescale && j > 0)) {
-          // O holds tiles < j: wait for the PV of tile j - 1, then scale it in TMEM
-          if (!mbar_wait(bar(kBarPvDone + 2 * hf + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after();
+          // O holds tiles < j (PV(j - 1) completed before S(j) was
+          // committed): scale it in TMEM
           const float f = rescale ? fast_exp2(m_used - m_new) : 1.0f;
 #pragma unroll 1
           for (int cb = 0; cb < D / 32; ++cb) {
@@ -411,14 +426,14 @@ __global__ void __launch_bounds__(448, 1)
           pw[c >> 1] = pack_half2(p0, p1);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        tc::st32(t_lane + b * 64, pw);
+        tc::st32(t_lane, pw);
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull + 2 * hf + b));
+        if (lane == 0) mbar_arrive(bar(kBarPFull + hf));
       }
       // ---- epilogue: O / l -> bf16, lse
-      if (ok && mbar_wait(bar(kBarPvDone + 2 * hf + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1)) {
+      if (ok && mbar_wait(bar(kBarPvDone + hf), 0)) {
         tc::fence_after();
         const float inv = 1.0f / l;
         uint16_t *dst = a.out + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;

@@ -77,6 +77,36 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// One lane of a converged warp (1 there, 0 elsewhere): the issuing lane of
+// the *_by forms below, which the whole warp executes.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}"
+               : "=r"(r));
+  return r;
+}
+
+// mma_f16_ts issued by the lane whose `leader` is non-zero.
+__device__ __forceinline__ void mma_f16_ts_by(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
+                                              uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, l;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 l, %5, 0;\n\t"
+      "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+
+// commit issued by the lane whose `leader` is non-zero.
+__device__ __forceinline__ void commit_by(uint32_t leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred l;\n\tsetp.ne.b32 l, %1, 0;\n\t"
+      "@l tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar),
+      "r"(leader)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every MMA issued so far by this thread completes.
 __device__ __forceinline__ void commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
