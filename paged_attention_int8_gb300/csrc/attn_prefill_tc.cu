@@ -19,18 +19,19 @@
 // converted K/V tile, so the int8 -> fp16 work per FLOP is halved.  Both MMA
 // A operands live in TMEM (q for QK, P for PV): shared memory then carries
 // only the K/V tiles (B operands), not a re-read of q for every MMA.
-// Warp roles (448 threads; warp w runs on SM sub-partition w % 4, and the
+// Warp roles (512 threads; warp w runs on SM sub-partition w % 4, and the
 // MMA warp shares its sub-partition only with the producer and two softmax
-// warps, so the ALU-heavy dequant warps never delay MMA issue):
-//   warp 5      TMA producer: int8 K/V pages + fp16 scales -> 3-stage ring
+// warps, so the ALU-heavy dequant warps never delay MMA issue; the others
+// each hold two dequant and two softmax warps):
+//   warp 5      TMA producer: int8 K/V pages + fp16 scales -> 4-stage ring
 //   warp 1      MMA issuer and owner of the TMEM allocation.  The converged
 //               warp issues through one elected lane, per tile j,
 //               PV(j-1, half 0), QK(j, half 0), PV(j-1, half 1), QK(j, half 1):
 //               while one half's softmax runs, the tensor core works on the
 //               other half
-//   warps 0, 2  K dequant: ring stage -> fp16 K_hi/K_lo (2-slot K ring, a
-//               slot freed when both halves' QK MMAs complete)
-//   warps 3, 4  V dequant: ring stage -> fp16 V' (2-slot V ring, freed when
+//   warps 0, 2, 3, 14  K dequant: ring stage -> fp16 K_hi/K_lo (2-slot K
+//               ring, a slot freed when both halves' QK MMAs complete)
+//   warps 4, 15 V dequant: ring stage -> fp16 V' (2-slot V ring, freed when
 //               both halves' PV MMAs complete); both in the canonical
 //               128-byte-swizzle K-major layout
 //   warps 6-9   softmax of half 0, warps 10-13 of half 1: one q row per
@@ -55,8 +56,8 @@ struct TcCfg {
   static constexpr int kTile = 64;
   static constexpr int kHalves = 2;
   static constexpr int kRows = 128 * kHalves;
-  static constexpr int kSt = 3;  // int8 staging stages (TMA)
-  static constexpr int kWarps = 14;
+  static constexpr int kSt = 4;  // int8 staging stages (TMA)
+  static constexpr int kWarps = 16;
   using L = StageLayout<D, BS, kTile>;
   static constexpr int kKBytes = kTile * D * 2;  // one of K_hi, K_lo: [D/64][64 keys][128 B]
   static constexpr int kKSlot = 2 * kKBytes;     // K ring slot: hi then lo
@@ -73,25 +74,26 @@ struct TcCfg {
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
   static_assert(D == 64 || D == 128, "tcgen05 prefill handles D = 64, 128");
   static_assert(kSmem <= 232448, "shared memory");
+  static_assert(kSt <= 4, "staging barriers");
 };
 
 // barrier indices (8 bytes each, from kBarOff)
 enum : int {
-  kBarStFull = 0,    // [3] producer -> dequant (tx bytes)
-  kBarStEmpty = 3,   // [3] dequant -> producer (4 warps)
-  kBarKFull = 6,     // [2] K dequant -> MMA (2 warps)
-  kBarKEmpty = 8,    // [2] commit after both halves' QK -> K dequant
-  kBarVFull = 10,    // [2] V dequant -> MMA (2 warps)
-  kBarVEmpty = 12,   // [2] commit after both halves' PV -> V dequant
-  kBarSFull = 14,    // [half] commit after QK -> softmax of the half
-  kBarPFull = 16,    // [half] softmax (P in TMEM) -> MMA (4 warps)
-  kBarPvDone = 18,   // [half] commit after the last PV -> epilogue
-  kBarQFull = 20,    // softmax (q written to TMEM) -> MMA (8 warps)
-  kNumBars = 21
+  kBarStFull = 0,    // [4] producer -> dequant (tx bytes)
+  kBarStEmpty = 4,   // [4] dequant -> producer (6 warps)
+  kBarKFull = 8,     // [2] K dequant -> MMA (4 warps)
+  kBarKEmpty = 10,   // [2] commit after both halves' QK -> K dequant
+  kBarVFull = 12,    // [2] V dequant -> MMA (2 warps)
+  kBarVEmpty = 14,   // [2] commit after both halves' PV -> V dequant
+  kBarSFull = 16,    // [half] commit after QK -> softmax of the half
+  kBarPFull = 18,    // [half] softmax (P in TMEM) -> MMA (4 warps)
+  kBarPvDone = 20,   // [half] commit after the last PV -> epilogue
+  kBarQFull = 22,    // softmax (q written to TMEM) -> MMA (8 warps)
+  kNumBars = 23
 };
 
 template <int D, int BS>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(512, 1)
     prefill_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
   using C = TcCfg<D, BS>;
@@ -136,10 +138,10 @@ __global__ void __launch_bounds__(448, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kSt; ++s) {
       mbar_init(bar(kBarStFull + s), 1);
-      mbar_init(bar(kBarStEmpty + s), 4);
+      mbar_init(bar(kBarStEmpty + s), 6);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarKFull + s), 2);
+      mbar_init(bar(kBarKFull + s), 4);
       mbar_init(bar(kBarKEmpty + s), 1);
       mbar_init(bar(kBarVFull + s), 2);
       mbar_init(bar(kBarVEmpty + s), 1);
@@ -225,12 +227,13 @@ __global__ void __launch_bounds__(448, 1)
       tc::commit_by(leader, bar(kBarPvDone + hf));
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp >= 14) {
     // ============================================================ dequant
-    // warps 0, 2: K (hi and lo parts), thread = one key row, all D channels
-    // warps 3, 4: V', thread = D / 64 channel rows, all 64 keys
-    const bool k_side = warp == 0 || warp == 2;
-    const int t = ((warp == 0 || warp == 3) ? 0 : 32) + lane;  // 0..63
+    // warps 0, 2, 3, 14: K (hi and lo parts), thread = one key row, D/2 channels
+    // warps 4, 15: V', thread = D / 64 channel rows, all 64 keys
+    const bool k_side = warp != 4 && warp != 15;
+    const int t = (k_side ? (warp == 14 ? 3 : warp == 0 ? 0 : warp - 1) : (warp == 4 ? 0 : 1)) * 32 +
+                  lane;  // K: 0..127, V: 0..63
 #pragma unroll 1
     for (int j = 0; j < nt; ++j) {
       const int sb = j % C::kSt, b = j & 1;
@@ -241,10 +244,11 @@ __global__ void __launch_bounds__(448, 1)
       if (k_side) {
         if (j >= 2 && !mbar_wait(bar(kBarKEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
         const uint32_t kdst = smem_base + C::kKOff + b * C::kKSlot;
-        const int r = t;
+        const int r = t & 63;
+        const int c0 = (t >> 6) * (D / 2);
         const bool dead = tail && key0 + r >= kv_end;  // stale bytes: write zeros
 #pragma unroll 2
-        for (int c = 0; c < D; c += 16) {
+        for (int c = c0; c < c0 + D / 2; c += 16) {
           const uint4 codes = lds128(st + L::k_off(r, c));
           const uint32_t sbits = lds16(st + L::ks_off(r, c / 32));
           const uint32_t s2 = dead ? 0u : (sbits | (sbits << 16));
@@ -377,20 +381,23 @@ __global__ void __launch_bounds__(448, 1)
           }
           mx = fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]));
         } else {
-          // eight independent chains, then a tree: short dependency paths
-          float e[8];
-          const bool up = sl2 >= 0.0f;
+          // four independent chains of three-input max (min for a negative
+          // scale), then combine
+          float e[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) e[k] = __uint_as_float(sr[k]);
+          for (int k = 0; k < 4; ++k) e[k] = __uint_as_float(sr[k]);
+          if (sl2 >= 0.0f) {
 #pragma unroll
-          for (int c = 8; c < 64; ++c)
-            e[c & 7] = up ? fmaxf(e[c & 7], __uint_as_float(sr[c]))
-                          : fminf(e[c & 7], __uint_as_float(sr[c]));
+            for (int c = 4; c < 64; c += 2)
+              e[(c >> 1) & 3] = fmax3(e[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            mx = fmax3(e[0], e[1], fmaxf(e[2], e[3]));
+          } else {
 #pragma unroll
-          for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) e[k] = up ? fmaxf(e[k], e[k + w]) : fminf(e[k], e[k + w]);
-          mx = e[0] * sl2;
+            for (int c = 4; c < 64; c += 2)
+              e[(c >> 1) & 3] = fmin3(e[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            mx = fmin3(e[0], e[1], fminf(e[2], e[3]));
+          }
+          mx *= sl2;
         }
         const float m_new = fmaxf(m_used, mx);
         const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
@@ -415,17 +422,25 @@ __global__ void __launch_bounds__(448, 1)
         }
         // P = 2^(s * scale - m_used) <= 2^8, fp16, into the S buffer's TMEM columns
         uint32_t pw[32];
-        float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        // masked scores are already scaled (and -inf where hidden)
+        // masked scores are already scaled (and -inf where hidden); pairs of
+        // columns go through the packed fp32 FMA and add
         const float mul = need_mask ? 1.0f : sl2;
+        const uint64_t mul2 = f32x2_pack(mul, mul), neg_m2 = f32x2_pack(-m_used, -m_used);
+        uint64_t ls2[4] = {0, 0, 0, 0};  // +0.0f pairs
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), mul, -m_used));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), mul, -m_used));
-          ls[(c >> 1) & 3] += p0 + p1;
+          float t0, t1;
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2,
+                                 neg_m2),
+                       t0, t1);
+          const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+          ls2[(c >> 1) & 3] = f32x2_add(ls2[(c >> 1) & 3], f32x2_pack(p0, p1));
           pw[c >> 1] = pack_half2(p0, p1);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        float ls[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f32x2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tc::st32(t_lane, pw);
         tc::wait_st();
         tc::fence_before();
