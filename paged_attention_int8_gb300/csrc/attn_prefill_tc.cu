@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp < 6 || warp >= 14) {
     // ============================================================ dequant
     // warps 0, 2, 3, 14: K (hi and lo parts), thread = one key row, D/2 channels
-    // warps 4, 15: V', thread = D / 64 channel rows, all 64 keys
+    // warps 4, 15: V', thread = D / 64 channel rows of one scale group, all 64 keys
     const bool k_side = warp != 4 && warp != 15;
     const int t = (k_side ? (warp == 14 ? 3 : warp == 0 ? 0 : warp - 1) : (warp == 4 ? 0 : 1)) * 32 +
                   lane;  // K: 0..127, V: 0..63
@@ -285,22 +285,33 @@ __global__ void __launch_bounds__(512, 1)
       } else {
         if (j >= 2 && !mbar_wait(bar(kBarVEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
         const uint32_t vrow = smem_base + C::kVOff + b * C::kVBytes;
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          const int ch = t + 64 * cc;
+        // D / 64 channel rows per thread, all in one scale group (for D = 128:
+        // lanes 0-15 take channels 32w + lane and 32w + lane + 16), so the
+        // per-key scales are loaded once for both rows
+        constexpr int R = D / 64;
+        int ch[R];
+        if constexpr (R == 2) {
+          ch[0] = (t >> 4) * 32 + (t & 15);
+          ch[1] = ch[0] + 16;
+        } else {
+          ch[0] = t;
+        }
+        const int g = ch[0] / 32;
 #pragma unroll 2
-          for (int key = 0; key < C::kTile; key += 16) {  // 16 keys: one 16-byte load
-            const uint4 codes = lds128(st + L::v_off(ch, key));
-            const uint4 s01 = lds128(st + L::vs_off(key, ch / 32));
-            const uint4 s23 = lds128(st + L::vs_off(key + 8, ch / 32));
-            uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
-            if (tail) {
+        for (int key = 0; key < C::kTile; key += 16) {  // 16 keys: one 16-byte load
+          const uint4 s01 = lds128(st + L::vs_off(key, g));
+          const uint4 s23 = lds128(st + L::vs_off(key + 8, g));
+          uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
+          if (tail) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if (key0 + key + 2 * i >= kv_end) sc[i] &= 0xffff0000u;
-                if (key0 + key + 2 * i + 1 >= kv_end) sc[i] &= 0x0000ffffu;
-              }
+            for (int i = 0; i < 8; ++i) {
+              if (key0 + key + 2 * i >= kv_end) sc[i] &= 0xffff0000u;
+              if (key0 + key + 2 * i + 1 >= kv_end) sc[i] &= 0x0000ffffu;
             }
+          }
+#pragma unroll
+          for (int rr = 0; rr < R; ++rr) {
+            const uint4 codes = lds128(st + L::v_off(ch[rr], key));
             uint32_t o[8];
             const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
@@ -310,8 +321,9 @@ __global__ void __launch_bounds__(512, 1)
               o[2 * i] = hmul2_u32(lo, sc[2 * i]);
               o[2 * i + 1] = hmul2_u32(hi, sc[2 * i + 1]);
             }
-            sts128(vrow + tc::sw128_chunk(ch, key / 8, D), make_uint4(o[0], o[1], o[2], o[3]));
-            sts128(vrow + tc::sw128_chunk(ch, key / 8 + 1, D), make_uint4(o[4], o[5], o[6], o[7]));
+            sts128(vrow + tc::sw128_chunk(ch[rr], key / 8, D), make_uint4(o[0], o[1], o[2], o[3]));
+            sts128(vrow + tc::sw128_chunk(ch[rr], key / 8 + 1, D),
+                   make_uint4(o[4], o[5], o[6], o[7]));
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -16,6 +16,7 @@ namespace paq8 {
 // A device-side wait gives up after this long and reports PA_DEV_TIMEOUT.
 // Normal waits last microseconds; the limit only bounds a broken pipeline.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kSuspendHintNs = 1000000u;  // 1 ms
 
 __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t bits) {
   if (status) atomicOr(status, bits);
@@ -52,14 +53,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One test of the phase; a thread whose phase is not yet complete may be
+// suspended (not spinning, so it takes no issue slots) for up to
+// kSuspendHintNs or until the phase completes.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
