@@ -10,7 +10,9 @@ before timing; inputs live in HBM when the timed region starts.
 
 Default workload: the decode batch (64 sequences, one query token each, KV
 lengths uniform in [512, 8192], 32 q / 8 kv heads, D = 128, block size 16).
-Its KV cache (~0.6 GB) is larger than L2, so no flush is needed between steps.
+Its KV cache (~0.6 GB) is larger than L2, so no flush is needed between steps;
+a workload whose KV bytes fit in twice the L2 gets a 512 MiB buffer write
+between timed steps, outside the per-step CUDA events that time it.
 Metric: algorithmic HBM bytes of a step / step time (GB/s); prefill-only
 workloads report attention TFLOP/s instead.
 
@@ -41,6 +43,8 @@ from paged_attention_int8_gb300 import _lib, build as pkg_build, inputs  # noqa:
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129e6
+FLUSH_BYTES = 512 << 20  # written between timed steps when the working set fits in L2
 
 
 # ----------------------------------------------------------------------------- work accounting
@@ -82,14 +86,26 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def kernel_sources_sha256() -> str:
+    """One hash over every kernel source file (any change invalidates a
+    recorded ncu figure)."""
+    d = os.path.join(ROOT, "paged_attention_int8_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()
+
+
 def recorded_traffic(workload: str):
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, if that summary was taken on the current kernel source."""
+    """Per-call DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum over
+    the kernels of one paged_attention call) from the committed ncu summary
+    profiles/attention_<workload>.md, if it was taken on the current kernel
+    sources; else None."""
     path = os.path.join(ROOT, "profiles", f"attention_{workload}.md")
-    src = os.path.join(ROOT, "paged_attention_int8_gb300", "csrc", "attention.cu")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
         return None
     rec_sha, traffic = None, None
@@ -98,7 +114,17 @@ def recorded_traffic(workload: str):
             rec_sha = line.split(":", 1)[1].strip()
         if line.startswith("traffic_bytes_per_launch:"):
             traffic = float(line.split(":", 1)[1].strip())
-    return traffic if rec_sha == sha else None
+    return traffic if rec_sha == kernel_sources_sha256() else None
+
+
+def attention_launches(spec: inputs.Spec, max_query_len: int, num_splits: int) -> int:
+    """Kernels one paged_attention call launches (the dispatch rule of the
+    library): the decode kernel when a kv head stacks at most 8 q heads, a
+    prefill kernel when some sequence has several query tokens (or the heads
+    do not fit the decode kernel), the segment reduce when splitting."""
+    use_decode = spec.hq // spec.hk <= 8
+    use_prefill = (not use_decode) or max_query_len > 1
+    return int(use_decode) + int(use_prefill) + int(num_splits > 1)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -190,7 +216,7 @@ class Runner:
                               dtype=torch.uint8, device=device)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty((w.num_tokens, s.hq), dtype=torch.float32, device=device)
-        self.launches_per_step = 2 + (1 if self.ns_eff > 1 else 0)
+        self.launches_per_step = 1 + attention_launches(s, w.max_query_len, self.ns_eff)
 
     def step(self, ev=None):
         w = self.w
@@ -360,6 +386,12 @@ def main():
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    # a working set that fits in L2 would be served from it on the next step:
+    # write a buffer larger than L2 between timed steps, outside the timing
+    flush = work["kv_bytes"] <= 2 * L2_BYTES
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if flush else None
+    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if flush else None
     clocks = ClockSampler(device.index)
     clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -370,7 +402,12 @@ def main():
     t_wall0 = time.time()
     e0.record()
     for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(i & 0xFF)
+            steps_ev[i][0].record()
         r.step(ev[i])
+        if flush:
+            steps_ev[i][1].record()
     e1.record()
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -379,7 +416,10 @@ def main():
         dist.barrier()
     clk = clocks.stop(t_wall0, t_wall1)
     r.check()
-    ms_total = e0.elapsed_time(e1)
+    if flush:
+        ms_total = sum(a.elapsed_time(b) for a, b in steps_ev)
+    else:
+        ms_total = e0.elapsed_time(e1)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     if world > 1:
         import torch.distributed as dist
@@ -406,7 +446,8 @@ def main():
         peak, runit = tc_peak, "TFLOP/s"
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
-                "kernel": "paged_attention call (attention_kernel + reduce_kernel)",
+                "kernel": "paged_attention call (%d kernel launches)"
+                          % attention_launches(spec, w.max_query_len, r.ns_eff),
                 "launch_ms": round(attn_ms, 5), "peak_source": peak_src,
                 "algorithmic_per_launch": work["attn_bytes"] if bound == "hbm" else work["flops"]}
 
@@ -429,8 +470,9 @@ def main():
                        "num_tokens": w.num_tokens, "q_heads": spec.hq, "kv_heads": spec.hk,
                        "head_dim": spec.d, "block_size": spec.bs, "max_seq_len": w.max_seq_len,
                        "sum_kv_len": int(w.seq_lens.sum()), "num_splits": r.ns_eff,
-                       "l2": "inputs larger than L2 (no flush)"
-                       if work["kv_bytes"] > 2 * 129e6 else "L2 not flushed",
+                       "l2": ("L2 flushed between steps (%d MiB written, untimed)"
+                              % (FLUSH_BYTES >> 20)) if flush
+                       else "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": r.launches_per_step * args.steps, "clocks": clk,

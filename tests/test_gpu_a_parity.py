@@ -193,6 +193,40 @@ def test_kv_store_adversarial_values(cuda_device):
     H.assert_cache_equal(g, H.OracleState(empty))
 
 
+def _store_only_workload(key, value, slots, num_blocks, bs):
+    hk, d = key.shape[1], key.shape[2]
+    spec = inputs.Spec("store_only", 0, hq=hk, hk=hk, d=d, bs=bs)
+    return inputs.Workload(spec=spec, q_lens=torch.zeros(0, dtype=torch.int32),
+                           seq_lens=torch.zeros(0, dtype=torch.int32),
+                           cu_seqlens_q=torch.zeros(1, dtype=torch.int32),
+                           block_table=torch.zeros((0, 1), dtype=torch.int32),
+                           num_blocks=num_blocks, prefix_key=key, prefix_value=value,
+                           prefix_slots=slots, new_key=key[:0], new_value=value[:0],
+                           new_slots=slots[:0], q=torch.zeros((0, hk, d), dtype=torch.bfloat16))
+
+
+def test_kv_store_near_ties_bit_exact(cuda_device):
+    # values whose quotient x / s lies at or within a few fp32 ulps of a
+    # rounding tie k + 1/2, for scales that are not powers of two: the codes
+    # must still equal those of the IEEE quotient (the oracle's rule)
+    rng = np.random.default_rng(11)
+    n, hk, d, bs = 512, 2, 128, 16
+    amax = rng.uniform(0.05, 80.0, size=(n, hk, d // 32)).astype(np.float32)
+    amax = torch.from_numpy(amax).to(torch.bfloat16).float().numpy()  # representable
+    s = np.maximum(amax / np.float32(127.0), np.float32(1e-8)).astype(np.float32)
+    k = rng.integers(-126, 126, size=(n, hk, d)).astype(np.float64)
+    eps = rng.choice([0.0, 2.0 ** -20, -(2.0 ** -20), 2.0 ** -13, -(2.0 ** -13), 2.0 ** -9],
+                     size=(n, hk, d))
+    x = (k + 0.5 + eps) * np.repeat(s, 32, axis=2).astype(np.float64)
+    x[:, :, ::32] = amax  # the group max
+    key = torch.from_numpy(x).to(torch.bfloat16)
+    value = torch.from_numpy(-x).to(torch.bfloat16)
+    slots = torch.from_numpy(rng.permutation(n)[:n].astype(np.int64))
+    w = _store_only_workload(key, value, slots, n // bs, bs)
+    g = H.GpuState(w, cuda_device)
+    H.assert_cache_equal(g, H.OracleState(w))
+
+
 # ------------------------------------------------------------------ device checks
 
 def test_kv_store_flags_out_of_range_slot(cuda_device):
