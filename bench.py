@@ -237,6 +237,35 @@ class Runner:
         assert _lib.check_status(self.ws) == 0
 
 
+def kv_store_measure(r: Runner, reps: int = 20):
+    """kv_store alone on the workload's prefix rows (the cache population
+    batch; storing the same rows again is idempotent): algorithmic bytes
+    (bf16 K/V read, codes + scales written, slots read) per CUDA-event time."""
+    w = r.w
+    s = w.spec
+    n = int(w.prefix_slots.shape[0])
+    if n == 0:
+        return None
+    G = s.d // 32
+    k, v, sl = (w.prefix_key.to(r.device), w.prefix_value.to(r.device),
+                w.prefix_slots.to(r.device))
+    nbytes = n * s.hk * (4 * s.d + 2 * (s.d + 2 * G)) + 8 * n
+    for _ in range(3):
+        _lib.kv_store(k, v, sl, r.kc, r.ks, r.vc, r.vs, status=r.status)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        _lib.kv_store(k, v, sl, r.kc, r.ks, r.vc, r.vs, status=r.status)
+        b.record()
+    torch.cuda.synchronize()
+    assert _lib.check_status(r.status) == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    del k, v, sl
+    return {"tokens": n, "bytes": nbytes, "ms": round(ms, 5),
+            "achieved_gbs": round(nbytes / (ms * 1e-3) * 1e-9, 2)}
+
+
 def e2e_measure(r: Runner, steps: int, warmup: int):
     """Same step through the public API with the step's inputs copied from
     pinned host memory and the outputs read back, all inside the timed region."""
@@ -451,6 +480,13 @@ def main():
                 "launch_ms": round(attn_ms, 5), "peak_source": peak_src,
                 "algorithmic_per_launch": work["attn_bytes"] if bound == "hbm" else work["flops"]}
 
+    store = None
+    if rank == 0:
+        store = kv_store_measure(r)
+        if store is not None:
+            store["peak"] = hbm_peak
+            store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w)
@@ -474,7 +510,7 @@ def main():
                               % (FLUSH_BYTES >> 20)) if flush
                        else "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "kv_store": store, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": r.launches_per_step * args.steps, "clocks": clk,
             "step_bytes": work["step_bytes"], "step_flops": work["flops"],
         }
