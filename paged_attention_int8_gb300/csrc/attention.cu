@@ -146,6 +146,8 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   a.cu_seqlens_q = L.cu;
   a.seq_lens = L.seq_lens;
   a.block_table = L.block_table;
+  a.k_cache = static_cast<const int8_t *>(L.k_cache);
+  a.v_cache = static_cast<const int8_t *>(L.v_cache);
   a.k_scale = static_cast<const uint16_t *>(L.k_scale);
   a.v_scale = static_cast<const uint16_t *>(L.v_scale);
   a.out = static_cast<uint16_t *>(L.out);

@@ -18,6 +18,8 @@ struct AttnArgs {
   const int32_t *cu_seqlens_q;  // [S+1]
   const int32_t *seq_lens;      // [S]
   const int32_t *block_table;   // [S, bt_stride]
+  const int8_t *k_cache;        // [nb, Hk, bs, D] int8
+  const int8_t *v_cache;        // [nb, Hk, D, bs] int8
   const uint16_t *k_scale;      // [nb, Hk, bs, G] fp16
   const uint16_t *v_scale;      // [nb, Hk, G, bs] fp16
   uint16_t *out;                // [T, Hq, D] bf16
@@ -36,12 +38,14 @@ struct AttnArgs {
 };
 
 // Layout of one pipeline stage of TILE keys (a whole number of pages):
-//   K codes  [TILE][D]    token-major pages, 2-D TMA with 128-byte swizzle
-//                         (64-byte for D = 64); D = 256 rows are two boxes
-//   V codes  [pages][D][BS] channel-major pages, one TMA box per page
-//                         (32-byte swizzle for BS = 32)
-//   K scales [TILE][G]    fp16, one bulk copy per page
-//   V scales [pages][G][BS] fp16, one bulk copy per page
+//   K codes  [TILE][D]    token-major pages in the 128-byte swizzle pattern
+//                         (64-byte for D = 64); D = 256 rows are two halves
+//   V codes  [pages][D][BS] channel-major pages (32-byte swizzle for BS = 32)
+//   K scales [TILE][G]    fp16
+//   V scales [pages][G][BS] fp16
+// Filled either by the TMA unit (produce_tiles: a 2-D box per page for the
+// codes, a bulk copy per page for each scale array) or by 16-byte cp.async
+// chunks written at the same swizzled places (produce_tiles_lsu).
 template <int D, int BS, int TILE>
 struct StageLayout {
   static constexpr int kD = D;
@@ -185,6 +189,93 @@ __device__ __forceinline__ void produce_tiles(const AttnArgs &a, const CUtensorM
       }
     }
     __syncwarp();
+  }
+}
+
+// 16-byte LSU copy global -> shared (L2 only), completion tracked per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// The mbarrier receives one arrival from this thread once all its earlier
+// cp.async copies have landed (counted against the expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Producer warp with LSU copies: the same tiles and stage layout as
+// produce_tiles, but every lane copies 16-byte chunks of the tile's pages
+// (K and V codes and both scale arrays) with cp.async, writing each chunk
+// at its swizzled place, and arrives on the stage's full barrier (which
+// expects 32 arrivals) when its copies land.  A page costs 2 * BS * (D +
+// D/16) / 16 chunks spread over the 32 lanes, instead of four TMA requests:
+// the TMA unit's per-request cost, not bandwidth, limited small pages.
+template <class L, int BS, int NST = kStages>
+__device__ __forceinline__ void produce_tiles_lsu(const AttnArgs &a, uint32_t smem_base,
+                                                  uint32_t bar_full, uint32_t bar_empty, int seq,
+                                                  int h, int tile_lo, int n_iter, int kv_end,
+                                                  int lane) {
+  constexpr int D = L::kD;
+  constexpr int kKChunks = BS * D / 16;        // K (or V) code chunks of a page
+  constexpr int kSChunks = BS * L::G * 2 / 16;  // K (or V) scale chunks of a page
+  constexpr int kRowChunks = D / 16;           // chunks of one K row
+  constexpr int kVRowChunks = BS / 16;         // chunks of one V channel row
+  static_assert(kSChunks >= 1 && kKChunks % 32 == 0, "page pieces are whole chunks");
+  const int n_pages = (kv_end + BS - 1) / BS;
+  const int32_t *bt_row = a.block_table + static_cast<int64_t>(seq) * a.bt_stride;
+  int page_base = -(1 << 30);
+  int my_blk = -1;
+  for (int it = 0; it < n_iter; ++it) {
+    const int stage = it % NST;
+    if (it >= NST) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / NST) - 1) & 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
+        return;
+      }
+    }
+    const int lp0 = (tile_lo + it) * L::kPages;
+    if (lp0 - page_base >= 32) {
+      page_base = lp0;
+      const int lp = page_base + lane;
+      my_blk = -1;
+      if (lp < n_pages) {
+        const int b = lp < a.bt_stride ? bt_row[lp] : -1;
+        if (b >= 0 && b < a.num_blocks) my_blk = b;
+        else flag_status(a.status, PA_DEV_BAD_BLOCK);
+      }
+    }
+    const uint32_t st = smem_base + stage * L::kBytes;
+#pragma unroll
+    for (int p = 0; p < L::kPages; ++p) {
+      const int blk = __shfl_sync(0xffffffffu, my_blk, lp0 + p - page_base);
+      if (blk < 0) continue;  // past the sequence (or a bad entry): the consumers mask it
+      const int64_t page = static_cast<int64_t>(blk) * a.hk + h;
+      const int8_t *ksrc = a.k_cache + page * (BS * D);
+      const int8_t *vsrc = a.v_cache + page * (BS * D);
+#pragma unroll 4
+      for (int c = lane; c < kKChunks; c += 32) {
+        const int r = c / kRowChunks, b = (c % kRowChunks) * 16;
+        cp_async16(st + L::k_off(p * BS + r, b), ksrc + c * 16);
+      }
+#pragma unroll 4
+      for (int c = lane; c < kKChunks; c += 32) {
+        const int ch = c / kVRowChunks, kk = (c % kVRowChunks) * 16;
+        cp_async16(st + L::v_off(ch, p * BS + kk), vsrc + c * 16);
+      }
+      const uint8_t *kss = reinterpret_cast<const uint8_t *>(a.k_scale + page * BS * L::G);
+      const uint8_t *vss = reinterpret_cast<const uint8_t *>(a.v_scale + page * BS * L::G);
+#pragma unroll
+      for (int c = lane; c < 2 * kSChunks; c += 32) {
+        if (c < kSChunks)
+          cp_async16(st + L::kKsOff + p * (BS * L::G * 2) + c * 16, kss + c * 16);
+        else
+          cp_async16(st + L::kVsOff + p * (BS * L::G * 2) + (c - kSChunks) * 16,
+                     vss + (c - kSChunks) * 16);
+      }
+    }
+    cp_async_arrive(bar_full + 8 * stage);
   }
 }
 

@@ -18,7 +18,10 @@
 //
 // CTA = 4 consumer warps, each taking one 16-key block of every 64-key tile
 // (D = 256: 32-key tiles, two warps per tile, pairs alternate tiles), with
-// private softmax states merged at the end, plus one TMA producer warp.
+// private softmax states merged at the end, plus one producer warp whose 32
+// lanes copy each tile's pages with 16-byte cp.async (a small page would
+// otherwise cost four TMA requests, and the per-request cost, not bandwidth,
+// limited the stream).
 // Grid: (num_seqs * num_splits, num_kv_heads); sequence and segment come
 // straight from blockIdx.x.
 #include "attn_common.cuh"
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
   const uint32_t bar_empty = bar_full + kStages * 8;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
       mbar_init(bar_empty + 8 * s, kWpt);  // every warp of the tile group reads it
     }
     fence_barrier_init();
@@ -127,12 +130,8 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
-    }
-    produce_tiles<L, BS>(a, &tmap_k, &tmap_v, smem_base, bar_full, bar_empty, seq, h, tile_lo,
-                         n_iter, kv_end, lane);
+    produce_tiles_lsu<L, BS>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter, kv_end,
+                             lane);
     return;
   }
 

@@ -8,7 +8,7 @@
 //
 // CTA = one q-block x one kv head (x one segment for split single-token
 // rows), 5 warps: warp 4 stages each 64-key tile's pages through a 4-deep
-// mbarrier ring (TMA for codes, bulk copies for scales); warps 0-3 take the
+// mbarrier ring (16-byte cp.async copies from all 32 lanes); warps 0-3 take the
 // rows in groups of 16 (R groups; the 4/R warps sharing a group alternate
 // tiles with private softmax states, merged at the end).  QK^T runs on the
 // exact integer codes (fp16) per 32-channel group, scaled by the group's K
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   const uint32_t bar_empty = bar_full + kStages * 8;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
       mbar_init(bar_empty + 8 * s, R);  // a tile is consumed by the R warps of one kv group
     }
     fence_barrier_init();
@@ -107,12 +107,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
-    }
-    produce_tiles<L, BS>(a, &tmap_k, &tmap_v, smem_base, bar_full, bar_empty, seq, h, tile_lo,
-                         n_iter, kv_end, lane);
+    produce_tiles_lsu<L, BS>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter, kv_end,
+                             lane);
     return;
   }
 
