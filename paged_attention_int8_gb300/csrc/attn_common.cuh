@@ -216,10 +216,29 @@ __device__ __forceinline__ void produce_tiles_lsu(const AttnArgs &a, uint32_t sm
                                                   int lane) {
   constexpr int D = L::kD;
   constexpr int kKChunks = BS * D / 16;        // K (or V) code chunks of a page
+  constexpr int kPer = kKChunks / 32;          // ... per lane
   constexpr int kSChunks = BS * L::G * 2 / 16;  // K (or V) scale chunks of a page
+  constexpr int kSPer = (2 * kSChunks + 31) / 32;
   constexpr int kRowChunks = D / 16;           // chunks of one K row
   constexpr int kVRowChunks = BS / 16;         // chunks of one V channel row
   static_assert(kSChunks >= 1 && kKChunks % 32 == 0, "page pieces are whole chunks");
+  // Stage offsets of this lane's chunks within page 0; page p adds p times the
+  // page's share of each array (the swizzle pattern repeats every page).
+  uint32_t koff[kPer], voff[kPer], soff[kSPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = lane + 32 * i;
+    koff[i] = L::k_off(c / kRowChunks, (c % kRowChunks) * 16);
+    voff[i] = L::v_off(c / kVRowChunks, (c % kVRowChunks) * 16);
+  }
+#pragma unroll
+  for (int i = 0; i < kSPer; ++i) {
+    const int c = lane + 32 * i;
+    soff[i] = c < kSChunks ? L::kKsOff + c * 16 : L::kVsOff + (c - kSChunks) * 16;
+  }
+  constexpr uint32_t kKPage = BS * L::kRowBytes;  // K bytes of a page within one row block
+  constexpr uint32_t kVPage = D * BS;
+  constexpr uint32_t kSPage = BS * L::G * 2;
   const int n_pages = (kv_end + BS - 1) / BS;
   const int32_t *bt_row = a.block_table + static_cast<int64_t>(seq) * a.bt_stride;
   int page_base = -(1 << 30);
@@ -252,27 +271,20 @@ __device__ __forceinline__ void produce_tiles_lsu(const AttnArgs &a, uint32_t sm
       const int blk = __shfl_sync(0xffffffffu, my_blk, lp0 + p - page_base);
       if (blk < 0) continue;  // past the sequence (or a bad entry): the consumers mask it
       const int64_t page = static_cast<int64_t>(blk) * a.hk + h;
-      const int8_t *ksrc = a.k_cache + page * (BS * D);
-      const int8_t *vsrc = a.v_cache + page * (BS * D);
-#pragma unroll 4
-      for (int c = lane; c < kKChunks; c += 32) {
-        const int r = c / kRowChunks, b = (c % kRowChunks) * 16;
-        cp_async16(st + L::k_off(p * BS + r, b), ksrc + c * 16);
-      }
-#pragma unroll 4
-      for (int c = lane; c < kKChunks; c += 32) {
-        const int ch = c / kVRowChunks, kk = (c % kVRowChunks) * 16;
-        cp_async16(st + L::v_off(ch, p * BS + kk), vsrc + c * 16);
-      }
+      const int8_t *ksrc = a.k_cache + page * (BS * D) + lane * 16;
+      const int8_t *vsrc = a.v_cache + page * (BS * D) + lane * 16;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) cp_async16(st + p * kKPage + koff[i], ksrc + i * 512);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) cp_async16(st + p * kVPage + voff[i], vsrc + i * 512);
       const uint8_t *kss = reinterpret_cast<const uint8_t *>(a.k_scale + page * BS * L::G);
       const uint8_t *vss = reinterpret_cast<const uint8_t *>(a.v_scale + page * BS * L::G);
 #pragma unroll
-      for (int c = lane; c < 2 * kSChunks; c += 32) {
-        if (c < kSChunks)
-          cp_async16(st + L::kKsOff + p * (BS * L::G * 2) + c * 16, kss + c * 16);
-        else
-          cp_async16(st + L::kVsOff + p * (BS * L::G * 2) + (c - kSChunks) * 16,
-                     vss + (c - kSChunks) * 16);
+      for (int i = 0; i < kSPer; ++i) {
+        const int c = lane + 32 * i;
+        if (c < 2 * kSChunks)
+          cp_async16(st + p * kSPage + soff[i],
+                     c < kSChunks ? kss + c * 16 : vss + (c - kSChunks) * 16);
       }
     }
     cp_async_arrive(bar_full + 8 * stage);

@@ -22,8 +22,8 @@
 // lanes copy each tile's pages with 16-byte cp.async (a small page would
 // otherwise cost four TMA requests, and the per-request cost, not bandwidth,
 // limited the stream).
-// Grid: (num_seqs * num_splits, num_kv_heads); sequence and segment come
-// straight from blockIdx.x.
+// Grid: num_splits * num_seqs * num_kv_heads CTAs, segment-major (then
+// sequence, then kv head).
 #include "attn_common.cuh"
 
 namespace paq8 {
@@ -83,9 +83,13 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int seq = blockIdx.x / a.num_splits;
-  const int sigma = blockIdx.x % a.num_splits;
+  // segment-major order: every sequence's first segment (and all kv heads)
+  // launches before any second segment, so the partial last segments of the
+  // longest sequences, not full ones, are what the final wave holds
+  const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.hk));
+  const int rest = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.hk));
+  const int seq = rest % a.num_seqs;
+  const int sigma = rest / a.num_seqs;
 
   const int q_start = a.cu_seqlens_q[seq];
   const int q_len = a.cu_seqlens_q[seq + 1] - q_start;
@@ -363,7 +367,7 @@ cudaError_t launch_decode_t(const AttnArgs &a, const CUtensorMap &tk, const CUte
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  dim3 grid(static_cast<unsigned>(a.num_seqs) * a.num_splits, a.hk);
+  dim3 grid(static_cast<unsigned>(a.num_seqs) * a.num_splits * a.hk, 1);
   decode_kernel<D, BS><<<grid, kThreads, kSmem, stream>>>(a, tk, tv);
   return cudaGetLastError();
 }
