@@ -64,10 +64,12 @@ struct DecodeCfg {
   static constexpr int kKg = kConsumerWarps / kWpt;  // tile groups (alternate tiles)
   static constexpr int kCm = D / 16;       // 16-channel blocks of the output
   static constexpr int G = D / 32;
+  static constexpr int kSt = D == 256 ? 4 : 3;          // ring stages
+  static constexpr int kMinBlocks = D == 256 ? 2 : 4;   // CTAs per SM
 };
 
 template <int D, int BS>
-__global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
+__global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
     decode_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
   using Cfg = DecodeCfg<D>;
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
   constexpr int kTile = Cfg::kTile;
   constexpr int kWpt = Cfg::kWpt;
   constexpr int kKg = Cfg::kKg;
+  constexpr int kStages = Cfg::kSt;
   static_assert(kStages % kKg == 0, "a stage always feeds the same tile group");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -134,8 +137,8 @@ __global__ void __launch_bounds__(kThreads, D == 256 ? 2 : 3)
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    produce_tiles_lsu<L, BS>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter, kv_end,
-                             lane);
+    produce_tiles_lsu<L, BS, kStages>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter,
+                                      kv_end, lane);
     return;
   }
 
@@ -357,7 +360,7 @@ template <int D, int BS>
 cudaError_t launch_decode_t(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                             cudaStream_t stream) {
   using L = StageLayout<D, BS, DecodeCfg<D>::kTile>;
-  constexpr int kSmem = kStages * L::kBytes + 2 * kStages * 8 + 1024;
+  constexpr int kSmem = DecodeCfg<D>::kSt * L::kBytes + 2 * DecodeCfg<D>::kSt * 8 + 1024;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
