@@ -92,8 +92,8 @@ pa_status pa_kv_store(const void *key, int64_t key_token_stride,
  * Split-KV segments chosen when pa_paged_attention gets num_splits == 0, for
  * these host-side hints (no device access).  Result in [1, 16].
  * Passage: "triton_turboquant_unified_attention.py" launcher (16 segments by
- * default, capped by the KV length); this library targets ~2048 keys per
- * segment.
+ * default, capped by the KV length); this library targets ~1024 keys per
+ * segment and at most ~8192 (sequence, kv head, segment) units in all.
  */
 int32_t pa_auto_num_splits(int32_t num_seqs, int32_t num_kv_heads,
                            int32_t max_query_len, int32_t max_seq_len);

@@ -131,12 +131,16 @@ static bool encode_map(CUtensorMap *map, const void *base, int64_t rows, int row
 
 int32_t auto_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_query_len,
                         int32_t max_seq_len) {
-  (void)num_seqs;
-  (void)num_kv_heads;
   (void)max_query_len;
-  // ~2048 keys per segment (measured best on the decode batch), at most 16
-  // segments (the pages' default count)
-  int32_t ns = (max_seq_len + 2047) / 2048;
+  // ~1024 keys per segment (measured best on the decode batch with four
+  // decode CTAs per SM), at most 16 segments (the pages' default count), and
+  // no more than ~8192 CTAs in all: past that, more segments only add
+  // partials to merge (measured on the mixed batch)
+  int32_t ns = (max_seq_len + 1023) / 1024;
+  const int64_t units = static_cast<int64_t>(num_seqs > 0 ? num_seqs : 1) *
+                        (num_kv_heads > 0 ? num_kv_heads : 1);
+  const int64_t cap = (8192 + units - 1) / units;
+  if (ns > cap) ns = static_cast<int32_t>(cap);
   return ns < 1 ? 1 : (ns > kMaxSplits ? kMaxSplits : ns);
 }
 

@@ -59,7 +59,8 @@ def test_auto_splits_range(lib):
         ns = lib.pa_auto_num_splits(64, 8, 1, L)
         assert 1 <= ns <= 16
     assert lib.pa_auto_num_splits(8, 8, 1, 131072) == 16
-    assert lib.pa_auto_num_splits(64, 8, 1, 8025) == 4
+    assert lib.pa_auto_num_splits(64, 8, 1, 8025) == 8
+    assert lib.pa_auto_num_splits(132, 8, 1024, 16384) == 8   # capped by ~8192 units
     assert lib.pa_auto_num_splits(2, 2, 1, 100) == 1
 
 
