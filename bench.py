@@ -382,6 +382,8 @@ def main():
     ap.add_argument("--num-splits", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kv-store", action="store_true",
+                    help="skip the separate kv_store throughput measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -481,7 +483,7 @@ def main():
                 "algorithmic_per_launch": work["attn_bytes"] if bound == "hbm" else work["flops"]}
 
     store = None
-    if rank == 0:
+    if rank == 0 and not args.no_kv_store:
         store = kv_store_measure(r)
         if store is not None:
             store["peak"] = hbm_peak
