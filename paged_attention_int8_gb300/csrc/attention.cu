@@ -45,6 +45,9 @@ __global__ void __launch_bounds__(128) reduce_kernel(const float *__restrict__ p
                                                      int32_t seg_keys, uint16_t *__restrict__ out,
                                                      float *__restrict__ lse) {
   constexpr int V = D / 32;  // channels per lane
+  // launched as a programmatic dependent of the decode / prefill kernel:
+  // wait for that grid's partials before reading anything
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (gw >= static_cast<int64_t>(num_seqs) * hq) return;
@@ -222,12 +225,27 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   const int64_t warps = static_cast<int64_t>(L.num_seqs) * L.hq;
   const unsigned blocks = static_cast<unsigned>((warps + 3) / 4);
   const int seg_keys = a.seg_tiles * seg_tile;
+  // programmatic dependent launch: the reduce's blocks are scheduled while
+  // the previous kernel drains, and wait for it inside (griddepcontrol.wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
 #define PAQ8_REDUCE_CASE(DD)                                                                     \
-  case DD:                                                                                       \
-    reduce_kernel<DD><<<blocks, 128, 0, stream>>>(a.part_acc, a.part_ml, L.cu, L.seq_lens,       \
-                                                  L.num_seqs, L.num_tokens, L.hq, L.num_splits, \
-                                                  seg_keys, a.out, L.lse);                       \
-    break;
+  case DD: {                                                                                     \
+    cudaError_t e = cudaLaunchKernelEx(&cfg, reduce_kernel<DD>,                                  \
+                                       static_cast<const float *>(a.part_acc),                   \
+                                       static_cast<const float *>(a.part_ml), L.cu, L.seq_lens,  \
+                                       L.num_seqs, L.num_tokens, L.hq, L.num_splits, seg_keys,   \
+                                       a.out, L.lse);                                            \
+    if (e != cudaSuccess) return e;                                                              \
+    break;                                                                                       \
+  }
   switch (L.d) {
     PAQ8_REDUCE_CASE(64)
     PAQ8_REDUCE_CASE(128)

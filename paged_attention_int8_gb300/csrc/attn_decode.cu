@@ -84,6 +84,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   float *smem_f = reinterpret_cast<float *>(smem_raw + (smem_base - smem_u32(smem_raw)));
 
+  // a dependent launched with programmatic serialization (the segment
+  // reduce) may be scheduled once every CTA of this grid has started; it
+  // still waits for this grid to finish before reading what it wrote
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // segment-major order: every sequence's first segment (and all kv heads)

@@ -273,3 +273,23 @@ def test_attention_flags_bad_block_table_and_bad_lengths(cuda_device):
     ref_out, ref_lse = o.attention(rows=rows)
     out, lse = g.attention()
     H.compare(out, lse, ref_out, ref_lse, rows)
+
+
+def test_workspace_reused_across_calls(cuda_device):
+    # one workspace for calls of different shapes and split counts: the
+    # decode kernel's segment counters must be back at zero after each call
+    ws = torch.zeros(_lib.workspace_size(16, 32, 128, 16), dtype=torch.uint8, device=cuda_device)
+    for name, ns in (("decode", 16), ("long_split", 4), ("decode", 2), ("long_split", 16)):
+        w = inputs.make_workload(SMALL[name])
+        g = H.GpuState(w, cuda_device)
+        o = H.OracleState(w)
+        rows = H.owned_rows(w)
+        ref_out, ref_lse = o.attention(rows=rows)
+        for _ in range(2):
+            out = torch.full_like(g.q, float("nan"))
+            lse = torch.full((w.num_tokens, w.spec.hq), float("nan"), device=cuda_device)
+            _lib.paged_attention(g.q, g.kc, g.ks, g.vc, g.vs, g.cu, g.seq_lens, g.block_table,
+                                 w.max_query_len, w.max_seq_len, w.softmax_scale,
+                                 num_splits=ns, out=out, lse=lse, workspace=ws)
+            assert _lib.check_status(ws) == 0
+            H.compare(out, lse, ref_out, ref_lse, rows, label=f"{name} splits={ns} reused")
