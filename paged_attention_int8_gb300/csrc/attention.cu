@@ -14,6 +14,8 @@
 //                      log-sum-exp (the pages' reduce_segments step).
 // A batch that holds only decode rows (max_query_len == 1) launches no
 // prefill kernel; both kernels exit at once for rows that are not theirs.
+#include <mutex>
+
 #include "attn_common.cuh"
 #include "launch.h"
 
@@ -147,6 +149,37 @@ int32_t auto_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_quer
   return ns < 1 ? 1 : (ns > kMaxSplits ? kMaxSplits : ns);
 }
 
+// A high-priority side stream per device (and fork / join events) on which
+// the tcgen05 prefill kernel runs beside the decode kernel of a mixed batch:
+// one is bound by the tensor cores, the other by HBM.  Created once; calls
+// from several host threads share it (correct, but their prefill kernels
+// then queue behind one another).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+static std::mutex g_side_mu;
+static SideStream g_side[64];
+
+static cudaError_t side_stream(SideStream **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream &ss = g_side[dev];
+  if (!ss.s) {
+    int lo = 0, hi = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, hi)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
 cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   AttnArgs a{};
   a.q = static_cast<const uint16_t *>(L.q);
@@ -193,19 +226,32 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     a.n_qblocks = 0;
     a.skip_single = 0;
     a.multi_token_ok = use_prefill ? 1 : 0;
-    cudaError_t e = launch_decode(a, tk, tv, L.d, L.bs, stream);
-    if (e != cudaSuccess) return e;
   }
   // tcgen05 prefill for multi-token sequences when the decode kernel takes the
   // single-token ones; the mma.sync kernel otherwise (D = 256, Hq/Hk > 8)
   const bool use_tc = use_decode && prefill_tc_supported(L.d);
-  if (use_prefill && use_tc) {
+  if (use_decode && use_prefill && use_tc) {
+    // mixed batch: the prefill kernel on the side stream, forked from and
+    // joined back to the caller's stream around the decode kernel
+    SideStream *ss = nullptr;
+    cudaError_t e = side_stream(&ss);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
     AttnArgs p = a;
     p.block_q = prefill_tc_rows() / a.qpk;
     p.n_qblocks = L.num_tokens / p.block_q + L.num_seqs;
     p.skip_single = 1;
-    cudaError_t e = launch_prefill_tc(p, tk, tv, L.d, L.bs, stream);
+    if ((e = launch_prefill_tc(p, tk, tv, L.d, L.bs, ss->s)) != cudaSuccess) return e;
+    if ((e = launch_decode(a, tk, tv, L.d, L.bs, stream)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(stream, ss->join, 0)) != cudaSuccess) return e;
+  } else if (use_decode) {
+    cudaError_t e = launch_decode(a, tk, tv, L.d, L.bs, stream);
     if (e != cudaSuccess) return e;
+  }
+  if (use_prefill && use_tc) {
+    // launched above with the decode kernel
   } else if (use_prefill) {
     AttnArgs p = a;
     p.block_q = L.max_query_len <= 1 ? 1 : (64 / a.qpk > 0 ? 64 / a.qpk : 1);
