@@ -78,6 +78,10 @@ size_t pa_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim
   return bytes;
 }
 
+// Set around the allocation-free entry's call: it must not create the side
+// stream (a driver resource) that mixed batches otherwise use.
+static thread_local bool t_no_side_stream = false;
+
 pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_scale,
                              const void *v_cache, const void *v_scale,
                              const int32_t *cu_seqlens_q, const int32_t *seq_lens,
@@ -148,6 +152,7 @@ pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_s
   L.out = out;
   L.lse = lse;
   L.workspace = static_cast<uint8_t *>(workspace);
+  L.side_stream_ok = !t_no_side_stream;
   cudaError_t e = paq8::launch_paged_attention(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
@@ -249,11 +254,13 @@ extern "C" pa_status pa_paged_attention_noalloc(
   // start at zero; the split partials are always written before they are read.
   cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return cuda_fail(e);
+  t_no_side_stream = true;
   st = pa_paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
                           block_table, block_table_stride, num_seqs, num_tokens, num_q_heads,
                           num_kv_heads, head_dim, num_blocks, block_size, max_query_len,
                           max_seq_len, softmax_scale, num_splits, out, lse, scratch,
                           kNoAllocScratchBytes, 0, stream);
+  t_no_side_stream = false;
   if (st != PA_OK) return st;
   if (status) {
     e = cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);

@@ -230,7 +230,8 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   // tcgen05 prefill for multi-token sequences when the decode kernel takes the
   // single-token ones; the mma.sync kernel otherwise (D = 256, Hq/Hk > 8)
   const bool use_tc = use_decode && prefill_tc_supported(L.d);
-  if (use_decode && use_prefill && use_tc) {
+  const bool fork = L.side_stream_ok && use_decode && use_prefill && use_tc;
+  if (fork) {
     // mixed batch: the prefill kernel on the side stream, forked from and
     // joined back to the caller's stream around the decode kernel
     SideStream *ss = nullptr;
@@ -251,7 +252,14 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if (use_prefill && use_tc) {
-    // launched above with the decode kernel
+    if (!fork) {
+      AttnArgs p = a;
+      p.block_q = prefill_tc_rows() / a.qpk;
+      p.n_qblocks = L.num_tokens / p.block_q + L.num_seqs;
+      p.skip_single = 1;
+      cudaError_t e = launch_prefill_tc(p, tk, tv, L.d, L.bs, stream);
+      if (e != cudaSuccess) return e;
+    }
   } else if (use_prefill) {
     AttnArgs p = a;
     p.block_q = L.max_query_len <= 1 ? 1 : (64 / a.qpk > 0 ? 64 / a.qpk : 1);

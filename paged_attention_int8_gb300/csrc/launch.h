@@ -25,6 +25,7 @@ struct AttnLaunch {
   void *out;
   float *lse;
   uint8_t *workspace;
+  bool side_stream_ok = true;  // a mixed batch may run prefill on the side stream
 };
 
 cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream);
