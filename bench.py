@@ -127,6 +127,25 @@ def attention_launches(spec: inputs.Spec, max_query_len: int, num_splits: int) -
     return int(use_decode) + int(use_prefill) + int(num_splits > 1)
 
 
+# ----------------------------------------------------------------------------- replicas
+
+def replica_spec(spec: inputs.Spec, rank: int) -> inputs.Spec:
+    """Rank r runs the same workload shape with its own seed (independent
+    replicas: the path has no exchange step)."""
+    return spec.replace(seed=spec.seed + 1000 * rank) if rank else spec
+
+
+def reduce_over_ranks(ms_total: float, units: float, device) -> tuple:
+    """(slowest rank's time, units all ranks processed): the whole-job
+    throughput is the second over the first."""
+    import torch.distributed as dist
+    t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -408,7 +427,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    w = inputs.make_workload(spec.replace(seed=spec.seed + 1000 * rank) if rank else spec)
+    w = inputs.make_workload(replica_spec(spec, rank))
     work = step_work(w)
     r = Runner(w, device, args.num_splits)
     for _ in range(args.warmup):
@@ -452,20 +471,19 @@ def main():
     else:
         ms_total = e0.elapsed_time(e1)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    units_local = work["flops"] if unit == "TFLOP/s" else work["step_bytes"]
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+        ms_total, units_per_step = reduce_over_ranks(ms_total, units_local, device)
+    else:
+        units_per_step = units_local
     ms_step = ms_total / args.steps
-    units_per_step = (work["flops"] if unit == "TFLOP/s" else work["step_bytes"]) * world
     scale = 1e-12 if unit == "TFLOP/s" else 1e-9
     value = units_per_step / (ms_step * 1e-3) * scale
 
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e_ms, h2d, d2h = e2e_measure(r, max(10, args.steps // 10), 5)
-        e2e = {"value": (units_per_step / world) / (e2e_ms * 1e-3) * scale, "unit": unit,
+        e2e = {"value": units_local / (e2e_ms * 1e-3) * scale, "unit": unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     hbm_peak, tc_peak, peak_src = load_peaks()
