@@ -37,9 +37,12 @@
 //   warps 6-9   softmax of half 0, warps 10-13 of half 1: one q row per
 //               thread (its TMEM lane); write q (fp16) into TMEM; per tile read
 //               S from TMEM, online softmax, write P (fp16) back into the same
-//               TMEM columns as the PV MMA's A operand; rescale O in TMEM only
-//               when a row max rises by more than 2^8 (exact: the final
-//               division uses the same max); the epilogue reads O
+//               TMEM columns as the PV MMA's A operand.  P is taken against
+//               the max O is currently scaled to; only when a tile's P
+//               sum would pass 2^15 (every P stays inside fp16) does the
+//               lane raise that max to the row max, rescale O in TMEM and
+//               redo the tile (exact: the final division uses the same
+//               max); the epilogue reads O
 // TMEM (512 columns): per half, the S/P buffer (64 columns), q (D/2
 // columns: two fp16 per column) and O (D columns).  A half's next QK is
 // issued after its PV of the previous tile, and tcgen05 MMAs from one thread
@@ -71,7 +74,7 @@ struct TcCfg {
   static constexpr uint32_t kHalfCols = 256;  // per half: S/P at +0, q at +64, O at +128
   static constexpr uint32_t kQCol = 64;
   static constexpr uint32_t kOCol = 128;
-  static constexpr float kRescaleThreshold = 8.0f;  // log2 units
+  static constexpr float kMaxTileSum = 32768.0f;  // bound on a tile's P sum (so on every P)
   static_assert(D == 64 || D == 128, "tcgen05 prefill handles D = 64, 128");
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(kSt <= 4, "staging barriers");
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(512, 1)
         const int r = t & 63;
         const int c0 = (t >> 6) * (D / 2);
         const bool dead = tail && key0 + r >= kv_end;  // stale bytes: write zeros
-#pragma unroll 2
+#pragma unroll
         for (int c = c0; c < c0 + D / 2; c += 16) {
           const uint4 codes = lds128(st + L::k_off(r, c));
           const uint32_t sbits = lds16(st + L::ks_off(r, c / 32));
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(512, 1)
           ch[0] = t;
         }
         const int g = ch[0] / 32;
-#pragma unroll 2
+#pragma unroll
         for (int key = 0; key < C::kTile; key += 16) {  // 16 keys: one 16-byte load
           const uint4 s01 = lds128(st + L::vs_off(key, g));
           const uint4 s23 = lds128(st + L::vs_off(key + 8, g));
@@ -375,84 +378,80 @@ __global__ void __launch_bounds__(512, 1)
       for (int j = 0; j < nt; ++j) {
         if (!mbar_wait(bar(kBarSFull + hf), j & 1)) { ok = false; break; }
         tc::fence_after();
-        uint32_t sr[64];
-        tc::ld32(t_lane, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tc::ld32(t_lane + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tc::wait_ld();
         const int key0 = j * C::kTile;
         const bool need_mask = key0 + C::kTile - 1 > limit;
-        // tile max of the scaled scores (a negative scale flips max and min)
-        float mx;
-        if (need_mask) {
-          float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        uint32_t sr[64];
+        // S from TMEM; masked columns -> -inf, the rest pre-scaled (only on
+        // tiles that cross this row's causal limit)
+        auto load_s = [&]() {
+          tc::ld32(t_lane, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          tc::ld32(t_lane + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tc::wait_ld();
+          if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float v = key0 + c > limit ? -INFINITY : __uint_as_float(sr[c]) * sl2;
-            e[c & 3] = fmaxf(e[c & 3], v);
-            sr[c] = __float_as_uint(v);
+            for (int c = 0; c < 64; ++c)
+              sr[c] = __float_as_uint(key0 + c > limit ? -INFINITY : __uint_as_float(sr[c]) * sl2);
           }
-          mx = fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]));
-        } else {
-          // four independent chains of three-input max (min for a negative
-          // scale), then combine
-          float e[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) e[k] = __uint_as_float(sr[k]);
-          if (sl2 >= 0.0f) {
-#pragma unroll
-            for (int c = 4; c < 64; c += 2)
-              e[(c >> 1) & 3] = fmax3(e[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            mx = fmax3(e[0], e[1], fmaxf(e[2], e[3]));
-          } else {
-#pragma unroll
-            for (int c = 4; c < 64; c += 2)
-              e[(c >> 1) & 3] = fmin3(e[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-            mx = fmin3(e[0], e[1], fminf(e[2], e[3]));
-          }
-          mx *= sl2;
-        }
-        const float m_new = fmaxf(m_used, mx);
-        const bool rescale = m_new > m_used + C::kRescaleThreshold;  // true on the first tile
-        if (__any_sync(0xffffffffu, rescale && j > 0)) {
-          // O holds tiles < j (PV(j - 1) completed before S(j) was
-          // committed): scale it in TMEM
-          const float f = rescale ? fast_exp2(m_used - m_new) : 1.0f;
-#pragma unroll 1
-          for (int cb = 0; cb < D / 32; ++cb) {
-            uint32_t orr[32];
-            tc::ld32(t_lane + C::kOCol + cb * 32, orr);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
-            tc::st32(t_lane + C::kOCol + cb * 32, orr);
-          }
-          tc::wait_st();
-        }
-        if (rescale) {
-          l *= fast_exp2(m_used - m_new);  // 0 on the first tile (m_used = -inf)
-          m_used = m_new;
-        }
-        // P = 2^(s * scale - m_used) <= 2^8, fp16, into the S buffer's TMEM columns
-        uint32_t pw[32];
-        // masked scores are already scaled (and -inf where hidden); pairs of
-        // columns go through the packed fp32 FMA and add
+        };
+        load_s();
         const float mul = need_mask ? 1.0f : sl2;
-        const uint64_t mul2 = f32x2_pack(mul, mul), neg_m2 = f32x2_pack(-m_used, -m_used);
-        uint64_t ls2[4] = {0, 0, 0, 0};  // +0.0f pairs
+        // P = 2^(s * scale - m_used) as fp16 pairs and their fp32 sum; pairs
+        // of columns go through the packed fp32 FMA and add
+        uint32_t pw[32];
+        float ts;
+        auto exp_tile = [&]() {
+          const uint64_t mul2 = f32x2_pack(mul, mul), neg_m2 = f32x2_pack(-m_used, -m_used);
+          uint64_t ls2[4] = {0, 0, 0, 0};  // +0.0f pairs
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float t0, t1;
-          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2,
-                                 neg_m2),
-                       t0, t1);
-          const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-          ls2[(c >> 1) & 3] = f32x2_add(ls2[(c >> 1) & 3], f32x2_pack(p0, p1));
-          pw[c >> 1] = pack_half2(p0, p1);
+          for (int c = 0; c < 64; c += 2) {
+            float t0, t1;
+            f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), mul2,
+                                   neg_m2),
+                         t0, t1);
+            const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+            ls2[(c >> 1) & 3] = f32x2_add(ls2[(c >> 1) & 3], f32x2_pack(p0, p1));
+            pw[c >> 1] = pack_half2(p0, p1);
+          }
+          float ls[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) f32x2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
+          ts = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        };
+        // The max the accumulator is scaled to moves only when this tile's
+        // P would exceed C::kMaxTileSum (2^15, inside fp16): no row max is
+        // taken on the common path.  The first tile (m_used = -inf) gives an
+        // infinite or NaN sum and always takes the slow path.
+        exp_tile();
+        const bool grow = !(ts <= C::kMaxTileSum);
+        if (__any_sync(0xffffffffu, grow)) {
+          float f = 1.0f;  // factor for what O and l hold
+          load_s();        // S is still in TMEM (P not yet written)
+          if (grow) {
+            float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < 64; ++c) e[c & 3] = fmaxf(e[c & 3], __uint_as_float(sr[c]) * mul);
+            const float m_new = fmaxf(m_used, fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])));
+            f = fast_exp2(m_used - m_new);  // 0 on the first tile
+            l *= f;
+            m_used = m_new;
+          }
+          exp_tile();
+          if (j > 0) {
+            // O holds tiles < j (PV(j - 1) completed before S(j) was
+            // committed): scale it in TMEM
+#pragma unroll 1
+            for (int cb = 0; cb < D / 32; ++cb) {
+              uint32_t orr[32];
+              tc::ld32(t_lane + C::kOCol + cb * 32, orr);
+              tc::wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
+              tc::st32(t_lane + C::kOCol + cb * 32, orr);
+            }
+            tc::wait_st();
+          }
         }
-        float ls[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) f32x2_unpack(ls2[k], ls[2 * k], ls[2 * k + 1]);
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        l += ts;
         tc::st32(t_lane, pw);
         tc::wait_st();
         tc::fence_before();
