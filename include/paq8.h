@@ -73,7 +73,7 @@ typedef enum {
  *   key, value        bf16 [num_tokens][num_kv_heads][head_dim]; the head and
  *                     channel dims contiguous, token stride given in elements
  *                     (a multiple of 8, so each row is 16-byte aligned).
- *   slot_mapping      int64 [num_tokens].
+ *   slot_mapping      int64 [num_tokens], 8-byte aligned.
  *   k_cache .. v_scale the HND caches (written).
  *   status            device uint32 status word (may be NULL: no reporting).
  * Slots >= num_blocks * block_size are skipped and flagged PA_DEV_BAD_SLOT.

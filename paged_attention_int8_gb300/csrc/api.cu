@@ -52,6 +52,8 @@ pa_status pa_kv_store(const void *key, int64_t key_token_stride, const void *val
     return fail(PA_ERR_INVALID_ARG, "key/value rows must be 16-byte aligned");
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) || !aligned16(v_scale))
     return fail(PA_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)
+    return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
   if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size >= (int64_t{1} << 31))
     return fail(PA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * block_size must be < 2^31");
   cudaError_t e = paq8::launch_kv_store(

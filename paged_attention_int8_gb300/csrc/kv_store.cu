@@ -15,9 +15,9 @@
 // the byte stores into the channel-major V pages (and the V scale stores)
 // coalesce across lanes whenever consecutive tokens fill consecutive slots
 // of a page (prefill chunks, cache population).  The quotient x / s is
-// formed as x * (1/s) and rounded there unless it lies within 2^-12 of a
+// formed as x * (1/s) and rounded there unless it lies within 2^-15 of a
 // rounding tie, where the IEEE quotient decides (the two differ by less than
-// 2.3e-5 for |x / s| <= 127.00001).
+// 2.27e-5 for |x / s| <= 127.00002).
 // Memory bound: per (token, kv head) it reads 4*D bytes and writes
 // 2*(D + D/16) bytes.
 #include "common.cuh"
@@ -37,40 +37,46 @@ __device__ __forceinline__ int32_t code_exact(float x, float s) {
   return static_cast<int32_t>(r);
 }
 
-// Codes of 32 values (4-byte words, little-endian) for scale s and its
-// correctly rounded reciprocal rs.
-__device__ __forceinline__ void quantize32(const float (&x)[32], float s, float rs,
-                                           uint32_t (&w)[8]) {
-  uint32_t near = 0u;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float q = x[i] * rs;
-    const float a = fabsf(q);
-    const float fl = floorf(a);
-    const float f = a - fl;
-    // |frac - 1/2| < 2^-12, or a non-finite quotient: let the IEEE divide decide
-    if (!(fabsf(f - 0.5f) >= 0x1p-12f)) near |= 1u << i;
-    const float m = fminf(fl + (f >= 0.5f ? 1.0f : 0.0f), 127.0f);
-    const int32_t c = static_cast<int32_t>(copysignf(m, q));
-    if ((i & 3) == 0) w[i >> 2] = 0u;
-    w[i >> 2] |= (static_cast<uint32_t>(c) & 0xffu) << (8 * (i & 3));
-  }
-  if (near) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((near >> i) & 1u) {
-        const uint32_t c = static_cast<uint32_t>(code_exact(x[i], s)) & 0xffu;
-        const int sh = 8 * (i & 3);
-        w[i >> 2] = (w[i >> 2] & ~(0xffu << sh)) | (c << sh);
-      }
-    }
-  }
+// Four codes (each in [-127, 127]) -> one little-endian word.
+__device__ __forceinline__ uint32_t pack4(int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+  const uint32_t lo = __byte_perm(static_cast<uint32_t>(c0), static_cast<uint32_t>(c1), 0x0040);
+  const uint32_t hi = __byte_perm(static_cast<uint32_t>(c2), static_cast<uint32_t>(c3), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
 }
 
-__device__ __forceinline__ void load32(const uint16_t *p, float (&x)[32]) {
+// copies into shared memory that complete asynchronously (per thread)
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kStoreWarps = 8;
+constexpr int kStoreStages = 3;
+constexpr int kStoreStageBytes = 32 * 64 + 32 * 8;  // 32 rows of 32 bf16, then 32 slots
+constexpr int kStoreSmem = kStoreWarps * kStoreStages * kStoreStageBytes;
+
+// 16-byte chunk j of lane `lane`'s 64-byte row within a stage: rotated by
+// lane / 2 so that the 8 lanes of each quarter-warp read 8 distinct bank
+// groups
+__device__ __forceinline__ uint32_t row_chunk(int lane, int j) {
+  return static_cast<uint32_t>(lane * 64 + ((j + (lane >> 1)) & 3) * 16);
+}
+
+// this lane's 32 bf16 values of a stage -> fp32
+__device__ __forceinline__ void load32(uint32_t stage, int lane, float (&x)[32]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(p + 8 * j);
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(stage + row_chunk(lane, j)));
     x[8 * j + 0] = bf16_lo(v.x); x[8 * j + 1] = bf16_hi(v.x);
     x[8 * j + 2] = bf16_lo(v.y); x[8 * j + 3] = bf16_hi(v.y);
     x[8 * j + 4] = bf16_lo(v.z); x[8 * j + 5] = bf16_hi(v.z);
@@ -78,64 +84,169 @@ __device__ __forceinline__ void load32(const uint16_t *p, float (&x)[32]) {
   }
 }
 
-constexpr int kStoreWarps = 8;
-
-// grid: (ceil(num_tokens / 32), ceil(2 * hk * D/32 / kStoreWarps)); block: 32 x
-// kStoreWarps.  Warp (blockIdx.y * kStoreWarps + w) takes one (kv head, group)
-// of K (even) or of V (odd) for 32 consecutive tokens.
-template <int D>
+// grid: (token-block slots, ceil(2 * hk * D/32 / kStoreWarps)); block: 32 x
+// kStoreWarps; dynamic shared memory kStoreSmem.  Warp (blockIdx.y *
+// kStoreWarps + w) takes one (kv head, group) of K (even) or of V (odd) and
+// walks the blocks of 32 consecutive tokens blockIdx.x, blockIdx.x +
+// gridDim.x, ...  Each lane copies its own row slice and slot two token
+// blocks ahead into the warp's 3-stage ring (cp.async) and reads back only
+// what it copied, so loads stay in flight without holding registers and no
+// barrier is needed.
+template <int D, int BS>
 __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
     const uint16_t *__restrict__ key, int64_t key_stride, const uint16_t *__restrict__ value,
     int64_t value_stride, const int64_t *__restrict__ slot_mapping, int32_t num_tokens,
     int32_t hk, int8_t *__restrict__ k_cache, uint16_t *__restrict__ k_scale,
     int8_t *__restrict__ v_cache, uint16_t *__restrict__ v_scale, int64_t num_slots,
-    int32_t block_size, uint32_t *status) {
+    uint32_t *status) {
   constexpr int G = D / 32;
+  constexpr int block_size = BS;
+  extern __shared__ __align__(16) uint8_t store_smem[];
   const int lane = threadIdx.x & 31;
-  const int combo = blockIdx.y * kStoreWarps + (threadIdx.x >> 5);
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * 32 + lane;
-  if (combo >= 2 * hk * G || n >= num_tokens) return;
+  const int warp = threadIdx.x >> 5;
+  const int combo = blockIdx.y * kStoreWarps + warp;
+  if (combo >= 2 * hk * G) return;
   const bool is_v = combo & 1;
   const int h = (combo >> 1) / G, g = (combo >> 1) % G;
-  const int64_t slot = slot_mapping[n];
-  if (slot < 0) return;
-  if (slot >= num_slots) {
-    if (combo == 0) flag_status(status, PA_DEV_BAD_SLOT);
-    return;
-  }
-  float x[32];
-  uint32_t w[8];
-  const int64_t blk = slot / block_size;
-  const int64_t off = slot % block_size;
-  const int64_t page = blk * hk + h;
-  if (!is_v) {
-    // K: token-major page row, 32 codes of group g; scale [page][bs][G]
-    load32(key + n * key_stride + h * D + g * 32, x);
-  } else {
-    load32(value + n * value_stride + h * D + g * 32, x);
-  }
-  float amax = 0.0f;
+  const uint16_t *src = (is_v ? value : key) + h * D + g * 32;
+  const int64_t stride = is_v ? value_stride : key_stride;
+  const int n_tblocks = (num_tokens + 31) / 32;
+  const uint32_t ring = smem_u32(store_smem) + warp * (kStoreStages * kStoreStageBytes);
+  // copies of token block tb into a stage (one commit group per call, empty
+  // past the end)
+  auto issue = [&](int tb, int stage) {
+    const int64_t n = static_cast<int64_t>(tb) * 32 + lane;
+    if (tb < n_tblocks && n < num_tokens) {
+      const uint32_t dst = ring + stage * kStoreStageBytes;
+      const uint16_t *row = src + n * stride;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float sc = group_scale(amax);
-  quantize32(x, sc, __frcp_rn(sc), w);
-  const uint16_t sbits = __half_as_ushort(__float2half_rn(sc));
-  if (!is_v) {
-    const int64_t row = page * block_size + off;
-    uint4 *kdst = reinterpret_cast<uint4 *>(k_cache + row * D + g * 32);
-    kdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    kdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    k_scale[row * G + g] = sbits;
-  } else {
-    // V: channel-major page, channel c of this token at (page * D + c) * bs + off;
-    // scale [page][G][bs]
-    int8_t *vdst = v_cache + (page * D + g * 32) * block_size + off;
+      for (int j = 0; j < 4; ++j) cp_async_16(dst + row_chunk(lane, j), row + 8 * j);
+      cp_async_8(dst + 32 * 64 + lane * 8, slot_mapping + n);
+    }
+    cp_async_commit();
+  };
+  int tb = blockIdx.x;
+  issue(tb, 0);
+  issue(tb + gridDim.x, 1);
+#pragma unroll 1
+  for (int i = 0; tb < n_tblocks; ++i, tb += gridDim.x) {
+    const int stage = i % kStoreStages;
+    issue(tb + 2 * gridDim.x, (i + 2) % kStoreStages);
+    cp_async_wait<2>();  // this lane's copies of `stage` have landed
+    const int64_t n = static_cast<int64_t>(tb) * 32 + lane;
+    if (n >= num_tokens) continue;
+    const uint32_t sbase = ring + stage * kStoreStageBytes;
+    int64_t slot;
+    asm volatile("ld.shared.s64 %0, [%1];" : "=l"(slot) : "r"(sbase + 32 * 64 + lane * 8));
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (combo == 0) flag_status(status, PA_DEV_BAD_SLOT);
+      continue;
+    }
+    float x[32];
+    uint32_t w[8];
+    load32(sbase, lane, x);
+    const int64_t blk = slot / block_size;
+    const int64_t off = slot % block_size;
+    const int64_t page = blk * hk + h;
+    float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      vdst[static_cast<int64_t>(i) * block_size] =
-          static_cast<int8_t>((w[i >> 2] >> (8 * (i & 3))) & 0xffu);
-    v_scale[(page * G + g) * block_size + off] = sbits;
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(x[k]));
+    const float sc = group_scale(amax);
+    const float rs = __frcp_rn(sc);
+    // Codes: q = x * rs rounded to the nearest integer (ties to even).  q
+    // and the IEEE quotient x / s differ by under 2.27e-5 (|q| <= 127.00002:
+    // two roundings of at most 2^-24 relative each in q, one in x / s), so
+    // where q lies 2^-15 or more from a rounding tie both round alike, and
+    // nearest-even there is also half away from zero; no clamp is needed.
+    // A value closer to a tie is redone: exactly from q when the scale is a
+    // power of two (then 1/s and x * rs are exact, and exact ties are common),
+    // otherwise from the IEEE quotient.  x is reloaded from the ring, whose
+    // stage is refilled two token blocks later.
+    constexpr float kFar = 0.5f - 0x1p-15f;  // |q - rint(q)| below this: not near a tie
+    bool far = true;  // every q of the group is far from a tie (false on NaN)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      int32_t c[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float q = x[4 * k + u] * rs;
+        const float r = rintf(q);
+        far = far && fabsf(q - r) < kFar;
+        c[u] = __float2int_rn(r);
+      }
+      w[k] = pack4(c[0], c[1], c[2], c[3]);
+    }
+    if (!far) {
+      const bool pow2 = (__float_as_uint(sc) & 0x7fffffu) == 0u && sc < INFINITY;
+      load32(sbase, lane, x);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        int32_t c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float q = x[4 * k + u] * rs;
+          const float r = rintf(q);
+          if (fabsf(q - r) < kFar)
+            c[u] = __float2int_rn(r);
+          else if (pow2 && fabsf(q) < INFINITY)
+            c[u] = static_cast<int32_t>(roundf(q));
+          else
+            c[u] = code_exact(x[4 * k + u], sc);
+        }
+        w[k] = pack4(c[0], c[1], c[2], c[3]);
+      }
+    }
+    const uint16_t sbits = __half_as_ushort(__float2half_rn(sc));
+    if (!is_v) {
+      // K: token-major page row, 32 codes of group g; scale [page][bs][G]
+      const int64_t row = page * block_size + off;
+      uint4 *kdst = reinterpret_cast<uint4 *>(k_cache + row * D + g * 32);
+      kdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      kdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      k_scale[row * G + g] = sbits;
+    } else {
+      // V: channel-major page, channel c of this token at (page * D + c) * bs + off;
+      // scale [page][G][bs]
+      int8_t *vdst = v_cache + (page * D + g * 32) * block_size + off;
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        vdst[static_cast<int64_t>(k) * block_size] =
+            static_cast<int8_t>((w[k >> 2] >> (8 * (k & 3))) & 0xffu);
+      v_scale[(page * G + g) * block_size + off] = sbits;
+    }
   }
+  cp_async_wait<0>();
+}
+
+// token-block slots of the grid
+template <int D, int BS>
+static cudaError_t store_grid_x(int n_tblocks, unsigned grid_y, unsigned *grid_x) {
+  static int cached_device = -1;
+  static unsigned resident = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (cached_device != dev) {
+    e = cudaFuncSetAttribute(kv_store_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStoreSmem);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_store_kernel<D, BS>,
+                                                      32 * kStoreWarps, kStoreSmem);
+    if (e != cudaSuccess) return e;
+    resident = static_cast<unsigned>(sms > 0 ? sms : 1) * static_cast<unsigned>(per_sm > 0 ? per_sm : 1);
+    cached_device = dev;
+  }
+  // up to 16 waves: one block per token block (every block starts at once
+  // with its own loads); beyond that, one resident set of blocks that walks
+  // the token blocks with its loads two steps ahead
+  const unsigned want = (resident + grid_y - 1) / grid_y;
+  const unsigned n = static_cast<unsigned>(n_tblocks);
+  *grid_x = n <= 16 * want ? n : want;
+  return cudaSuccess;
 }
 
 cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint16_t *value,
@@ -146,23 +257,26 @@ cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint1
                             cudaStream_t stream) {
   const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
   const dim3 block(32 * kStoreWarps);
-  const dim3 grid(static_cast<unsigned>((num_tokens + 31) / 32),
-                  static_cast<unsigned>((2 * hk * (d / 32) + kStoreWarps - 1) / kStoreWarps));
-  switch (d) {
-#define PAQ8_STORE_CASE(DD)                                                                   \
-  case DD:                                                                                    \
-    kv_store_kernel<DD><<<grid, block, 0, stream>>>(                                          \
+  const int n_tblocks = (num_tokens + 31) / 32;
+  const unsigned grid_y = static_cast<unsigned>((2 * hk * (d / 32) + kStoreWarps - 1) / kStoreWarps);
+  unsigned grid_x = 0;
+#define PAQ8_STORE_CASE(DD, BB)                                                               \
+  if (d == DD && block_size == BB) {                                                          \
+    if (cudaError_t e = store_grid_x<DD, BB>(n_tblocks, grid_y, &grid_x); e != cudaSuccess)  \
+      return e;                                                                               \
+    kv_store_kernel<DD, BB><<<dim3(grid_x, grid_y), block, kStoreSmem, stream>>>(              \
         key, key_stride, value, value_stride, slot_mapping, num_tokens, hk, k_cache, k_scale, \
-        v_cache, v_scale, num_slots, block_size, status);                                     \
-    break;
-    PAQ8_STORE_CASE(64)
-    PAQ8_STORE_CASE(128)
-    PAQ8_STORE_CASE(256)
-#undef PAQ8_STORE_CASE
-    default:
-      return cudaErrorInvalidValue;
+        v_cache, v_scale, num_slots, status);                                                 \
+    return cudaGetLastError();                                                                \
   }
-  return cudaGetLastError();
+  PAQ8_STORE_CASE(64, 16)
+  PAQ8_STORE_CASE(64, 32)
+  PAQ8_STORE_CASE(128, 16)
+  PAQ8_STORE_CASE(128, 32)
+  PAQ8_STORE_CASE(256, 16)
+  PAQ8_STORE_CASE(256, 32)
+#undef PAQ8_STORE_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace paq8

@@ -83,6 +83,7 @@ def _store_args(**kw):
     (dict(key=24), _lib.Status.INVALID_ARG),
     (dict(kc=8), _lib.Status.INVALID_ARG),
     (dict(nb=0), _lib.Status.INVALID_ARG),
+    (dict(slots=20), _lib.Status.INVALID_ARG),   # slot_mapping not 8-byte aligned
 ])
 def test_kv_store_rejects_bad_arguments(lib, kw, expect):
     assert lib.pa_kv_store(*_store_args(**kw)) == expect

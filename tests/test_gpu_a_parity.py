@@ -227,6 +227,51 @@ def test_kv_store_near_ties_bit_exact(cuda_device):
     H.assert_cache_equal(g, H.OracleState(w))
 
 
+def _near_tie_groups(rng, count):
+    """Groups of 32 bf16 values (as fp32), group max first, whose quotients
+    x / s (s = fp32(amax / 127)) sit on a rounding tie k + 1/2 or close to
+    one: half the groups have a power-of-two scale (amax = 1.984375 * 2^e,
+    so s = 2^(e-6)) and exact ties x = (k + 1/2) s; the rest have other
+    scales and values searched among all bf16 numbers for |x / s - (k +
+    1/2)| < 2^-12 (fp32 quotient)."""
+    pos = (np.arange(0x0080, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    groups = []
+    while len(groups) < count:
+        if len(groups) % 2 == 0:
+            e = int(rng.integers(-6, 7))
+            amax = np.float32(1.984375 * 2.0 ** e)
+            s = np.float32(amax / np.float32(127.0))
+            k = rng.integers(-127, 127, size=31)
+            vals = ((k + 0.5) * np.float64(s)).astype(np.float32)
+        else:
+            amax = np.float32(torch.tensor(float(rng.uniform(0.05, 60.0))).to(torch.bfloat16).item())
+            s = np.float32(amax / np.float32(127.0))
+            cand = pos[pos < amax]
+            q = (cand / s).astype(np.float32)
+            near = np.abs(q - np.floor(q) - 0.5) < 2.0 ** -12
+            if near.sum() < 4:
+                continue
+            pick = rng.choice(cand[near], size=31)
+            vals = pick * rng.choice([-1.0, 1.0], size=31).astype(np.float32)
+        groups.append(np.concatenate([[amax], vals]).astype(np.float32))
+    return np.stack(groups)
+
+
+def test_kv_store_exact_and_near_ties_bit_exact(cuda_device):
+    rng = np.random.default_rng(12)
+    n, hk, d, bs = 128, 2, 128, 16
+    G = d // 32
+    gk = _near_tie_groups(rng, n * hk * G)
+    gv = _near_tie_groups(rng, n * hk * G)
+    key = torch.from_numpy(gk.reshape(n, hk, d)).to(torch.bfloat16)
+    value = torch.from_numpy(gv.reshape(n, hk, d)).to(torch.bfloat16)
+    assert torch.equal(key.float(), torch.from_numpy(gk.reshape(n, hk, d)))  # exact in bf16
+    slots = torch.from_numpy(rng.permutation(n).astype(np.int64))
+    w = _store_only_workload(key, value, slots, n // bs, bs)
+    g = H.GpuState(w, cuda_device)
+    H.assert_cache_equal(g, H.OracleState(w))
+
+
 # ------------------------------------------------------------------ device checks
 
 def test_kv_store_flags_out_of_range_slot(cuda_device):
