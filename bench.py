@@ -86,15 +86,20 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+# The sources of the kernels one paged_attention call launches (their host
+# dispatch included); a recorded ncu figure holds while these are unchanged.
+ATTENTION_SOURCES = ("attention.cu", "attn_decode.cu", "attn_prefill.cu", "attn_prefill_tc.cu",
+                     "attn_common.cuh", "common.cuh", "tcgen05.cuh", "launch.h")
+
+
 def kernel_sources_sha256() -> str:
-    """One hash over every kernel source file (any change invalidates a
-    recorded ncu figure)."""
+    """One hash over the attention kernels' source files (any change
+    invalidates a recorded ncu figure)."""
     d = os.path.join(ROOT, "paged_attention_int8_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(d, name), "rb").read())
+    for name in sorted(ATTENTION_SOURCES):
+        h.update(name.encode())
+        h.update(open(os.path.join(d, name), "rb").read())
     return h.hexdigest()
 
 
@@ -285,6 +290,62 @@ def kv_store_measure(r: Runner, reps: int = 20):
             "achieved_gbs": round(nbytes / (ms * 1e-3) * 1e-9, 2)}
 
 
+def merge_measure(r: Runner, reps: int = 20):
+    """merge_attn_states on the step's output (all T * Hq rows) and a second
+    state of the same shape, as when a cached prefix and the new keys are
+    attended in two passes: algorithmic bytes (two bf16 outputs and two LSEs
+    read, the merged output and LSE written) per CUDA-event time."""
+    d = r.out.shape[-1]
+    rows = r.out.numel() // d
+    out_b = r.out.clone()
+    lse_b = r.lse.clone().nan_to_num_(0.0) - 0.5
+    lse_a = r.lse.clone().nan_to_num_(0.0)
+    merged = torch.empty_like(r.out)
+    lse_m = torch.empty_like(r.lse)
+    nbytes = rows * (3 * d * 2 + 3 * 4)
+
+    def call():
+        _lib.merge_attn_states(r.out, lse_a, out_b, lse_b, out=merged, lse=lse_m)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        # the calls replayed from a CUDA graph: device time, no host launch cost
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(reps):
+                call()
+        graph.replay()
+        torch.cuda.synchronize()
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        timing = f"CUDA graph of {reps} calls, replayed"
+        del graph
+    except RuntimeError:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            call()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        timing = "CUDA events around each call"
+    del out_b, lse_b, lse_a, merged, lse_m
+    return {"rows": rows, "bytes": nbytes, "ms": round(ms, 5),
+            "achieved_gbs": round(nbytes / (ms * 1e-3) * 1e-9, 2), "timing": timing,
+            "l2": "inputs larger than L2" if rows * (4 * d + 8) > L2_BYTES else "inputs fit in L2"}
+
+
 def e2e_measure(r: Runner, steps: int, warmup: int):
     """Same step through the public API with the step's inputs copied from
     pinned host memory and the outputs read back, all inside the timed region."""
@@ -402,7 +463,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kv-store", action="store_true",
-                    help="skip the separate kv_store throughput measurement")
+                    help="skip the separate kv_store and merge_attn_states throughput measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -507,6 +568,12 @@ def main():
             store["peak"] = hbm_peak
             store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
 
+    merge = None
+    if rank == 0 and not args.no_kv_store:
+        merge = merge_measure(r)
+        merge["peak"] = hbm_peak
+        merge["frac"] = round(merge["achieved_gbs"] / hbm_peak, 4)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w)
@@ -530,7 +597,8 @@ def main():
                               % (FLUSH_BYTES >> 20)) if flush
                        else "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roofline, "kv_store": store, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "kv_store": store, "merge_attn_states": merge,
+            "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": r.launches_per_step * args.steps, "clocks": clk,
             "step_bytes": work["step_bytes"], "step_flops": work["flops"],
         }

@@ -158,6 +158,36 @@ pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_s
                              uint32_t flags, void *stream);
 
 /*
+ * merge_attn_states -- the attention of queries over the union of two
+ * disjoint key sets, from their attention over each set (e.g. a cached
+ * prefix attended in one pass and the new keys in another, or two calls'
+ * split-KV results).
+ * Passage: "shared/attention_kit.py", `_merge_lse_(out, lse, other,
+ * other_lse)`: log-sum-exp weights of the two partial results (the page
+ * keeps base-2 LSEs; here, as for pa_paged_attention, they are natural-log).
+ *
+ *   out_a, out_b  bf16 [num_rows][head_dim], 16-byte aligned: the
+ *                 normalized attention output of each part (a row = one
+ *                 query token and q head, e.g. pa_paged_attention's out
+ *                 viewed as [num_tokens * num_q_heads][head_dim]).
+ *   lse_a, lse_b  fp32 [num_rows], 4-byte aligned: natural-log LSE of each
+ *                 part; -inf marks a part with no key for that row.  +inf
+ *                 and NaN are not supported.
+ *   out           bf16 [num_rows][head_dim] (written); may be out_a or out_b.
+ *   lse           fp32 [num_rows] merged LSE (written), or NULL; may be
+ *                 lse_a or lse_b.
+ * Per row: M = max(lse_a, lse_b), e_x = exp(lse_x - M),
+ *   out = (e_a * out_a + e_b * out_b) / (e_a + e_b)   (fp32, rounded to bf16)
+ *   lse = M + ln(e_a + e_b).
+ * A row whose two LSEs are both -inf gets out = 0 and lse = -inf.
+ * Supported head_dim: 64, 128, 256.  num_rows == 0 is a no-op.
+ * Returns PA_OK or an error; asynchronous on `stream`.
+ */
+pa_status pa_merge_attn_states(const void *out_a, const float *lse_a, const void *out_b,
+                               const float *lse_b, void *out, float *lse, int64_t num_rows,
+                               int32_t head_dim, void *stream);
+
+/*
  * Synchronizes `stream`, reads the device status word at `status` (a kv_store
  * status word, or the start of an attention workspace), clears it, and maps
  * it to PA_OK / PA_ERR_TIMEOUT (bit 0x8 set) / PA_ERR_DEVICE_CHECK (other

@@ -18,6 +18,8 @@ Each function cites the page passage it follows:
 * ``attention_partial`` / ``merge_partials`` -- the split-KV segments of
   "triton_turboquant_unified_attention.py" (3D kernel) and the log-sum-exp
   merge ``_merge_lse_`` of "shared/attention_kit.py", in natural-log form.
+* ``merge_states`` -- ``_merge_lse_`` of "shared/attention_kit.py" on two
+  normalized (out, lse) results, row by row, in natural-log form.
 
 Parity status of each function (what pins it) is listed in the design notes.
 """
@@ -81,6 +83,8 @@ def _load():
         lib.or_attention_partial.restype = ctypes.c_int
         lib.or_merge_partials.argtypes = [i32, P, P, P, i32, P, P]
         lib.or_merge_partials.restype = None
+        lib.or_merge_states.argtypes = [i64, i32, P, P, P, P, P, P]
+        lib.or_merge_states.restype = None
         _lib = lib
         return lib
 
@@ -244,3 +248,21 @@ def merge_partials(m, l, acc):
     lse = np.empty(1, np.float64)
     _load().or_merge_partials(n, _ptr(m), _ptr(l), _ptr(acc), d, _ptr(out), _ptr(lse))
     return out, float(lse[0])
+
+
+def merge_states(out_a, lse_a, out_b, lse_b):
+    """Row-wise merge of two normalized attention results over disjoint key
+    sets: out_a, out_b [rows, D], lse_a, lse_b [rows] (natural log; -inf =
+    no key) -> (out [rows, D], lse [rows]), fp64."""
+    out_a = _c(np.asarray(out_a, np.float64), np.float64)
+    out_b = _c(np.asarray(out_b, np.float64), np.float64)
+    lse_a = _c(np.asarray(lse_a, np.float64), np.float64)
+    lse_b = _c(np.asarray(lse_b, np.float64), np.float64)
+    rows, d = out_a.shape
+    if out_b.shape != (rows, d) or lse_a.shape != (rows,) or lse_b.shape != (rows,):
+        raise ValueError("merge_states: shape mismatch")
+    out = np.empty((rows, d), np.float64)
+    lse = np.empty(rows, np.float64)
+    _load().or_merge_states(rows, d, _ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b),
+                            _ptr(out), _ptr(lse))
+    return out, lse

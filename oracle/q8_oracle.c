@@ -397,6 +397,35 @@ void or_merge_partials(int32_t n, const double *m, const double *l,
     *lse = M + log(L);
 }
 
+/*
+ * Merge of two normalized attention results over disjoint key sets, row by
+ * row ("shared/attention_kit.py" `_merge_lse_(out, lse, other, other_lse)`,
+ * natural-log LSE):
+ *   M = max(lse_a, lse_b);  e_x = exp(lse_x - M);
+ *   out = (e_a out_a + e_b out_b) / (e_a + e_b);  lse = M + ln(e_a + e_b).
+ * Rows with both LSEs -inf (no key on either side) get out = 0, lse = -inf.
+ * out_a, out_b, out [rows, d]; lse_a, lse_b, lse [rows]; fp64 throughout.
+ */
+void or_merge_states(int64_t rows, int32_t d, const double *out_a, const double *lse_a,
+                     const double *out_b, const double *lse_b, double *out, double *lse)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double a = lse_a[r], b = lse_b[r];
+        const double M = a > b ? a : b;
+        double *o = out + r * d;
+        if (M == -INFINITY) {
+            for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
+        const double ea = exp(a - M), eb = exp(b - M);
+        const double sum = ea + eb;
+        for (int32_t c = 0; c < d; ++c)
+            o[c] = (ea * out_a[r * d + c] + eb * out_b[r * d + c]) / sum;
+        lse[r] = M + log(sum);
+    }
+}
+
 typedef struct {
     const or_problem *p;
     const int64_t *rows;     /* row r = token * hq + head */

@@ -4,14 +4,16 @@ The compute lives in a C-ABI CUDA library (``libpaq8.so``, built for sm_103a);
 this package is its thin ctypes binding.  ``kv_store`` quantizes K/V rows to
 the q8 format (int8 codes, one fp16 scale per token, kv head and 32 channels)
 and scatters them into a block-paged cache; ``paged_attention`` runs unified
-causal prefill + decode over that cache and returns bf16 output and fp32 LSE.
+causal prefill + decode over that cache and returns bf16 output and fp32 LSE;
+``merge_attn_states`` merges two such results over disjoint key sets by their
+LSEs.
 
 Importing the package does not load the CUDA library; the first call does, and
 fails loudly if it has not been built.
 """
 from __future__ import annotations
 
-__all__ = ["kv_store", "paged_attention", "workspace_size", "check_status",
+__all__ = ["kv_store", "paged_attention", "merge_attn_states", "workspace_size", "check_status",
            "auto_num_splits", "Status", "PagedAttentionError", "library_path"]
 
 

@@ -68,6 +68,8 @@ def load():
                                            i32, i32, i32, i32, ctypes.c_float, i32, P, P, P,
                                            ctypes.c_size_t, ctypes.c_uint32, P]
         lib.pa_paged_attention.restype = ctypes.c_int
+        lib.pa_merge_attn_states.argtypes = [P, P, P, P, P, P, i64, i32, P]
+        lib.pa_merge_attn_states.restype = ctypes.c_int
         lib.pa_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
         lib.pa_check_status.restype = ctypes.c_int
         lib.pa_status_string.argtypes = [ctypes.c_int]
@@ -216,6 +218,39 @@ def paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
                                 float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 0, _stream(stream))
+    _raise_if(st)
+    return (out, lse) if return_lse else out
+
+
+def merge_attn_states(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None,
+                      return_lse: bool = True):
+    """Attention over the union of two disjoint key sets from the attention
+    over each: out_a, out_b bf16 [..., D] (e.g. [T, Hq, D]) with their
+    natural-log LSEs lse_a, lse_b fp32 [...] (-inf = no key).  ``out`` may be
+    out_a or out_b and ``lse`` lse_a or lse_b (in place).  Returns (out, lse)
+    or out alone when ``return_lse`` is False."""
+    _check_cuda(out_a, lse_a, out_b, lse_b, out, lse)
+    for name, t in (("out_a", out_a), ("out_b", out_b)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 tensor")
+    for name, t in (("lse_a", lse_a), ("lse_b", lse_b)):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous fp32 tensor")
+    d = out_a.shape[-1]
+    rows = out_a.numel() // d if d else 0
+    if out_b.shape != out_a.shape or lse_a.numel() != rows or lse_b.numel() != rows:
+        raise ValueError("merge_attn_states: shape mismatch")
+    if out is None:
+        out = torch.empty_like(out_a)
+    elif out.shape != out_a.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like out_a")
+    if lse is None and return_lse:
+        lse = torch.empty_like(lse_a)
+    elif lse is not None and (lse.numel() != rows or lse.dtype != torch.float32
+                              or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 tensor with one value per row")
+    st = load().pa_merge_attn_states(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b),
+                                     _ptr(out), _ptr(lse), rows, d, _stream(stream))
     _raise_if(st)
     return (out, lse) if return_lse else out
 

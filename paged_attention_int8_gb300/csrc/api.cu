@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "merge.h"
 
 
 namespace {
@@ -156,6 +157,25 @@ pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_s
   L.workspace = static_cast<uint8_t *>(workspace);
   L.side_stream_ok = !t_no_side_stream;
   cudaError_t e = paq8::launch_paged_attention(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_merge_attn_states(const void *out_a, const float *lse_a, const void *out_b,
+                               const float *lse_b, void *out, float *lse, int64_t num_rows,
+                               int32_t head_dim, void *stream) {
+  if (num_rows < 0) return fail(PA_ERR_INVALID_ARG, "num_rows < 0");
+  if (num_rows == 0) return PA_OK;
+  if (!out_a || !lse_a || !out_b || !lse_b || !out) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!supported_dim(head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (!aligned16(out_a) || !aligned16(out_b) || !aligned16(out))
+    return fail(PA_ERR_INVALID_ARG, "out_a, out_b and out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse_a) | reinterpret_cast<uintptr_t>(lse_b) |
+       reinterpret_cast<uintptr_t>(lse)) & 3u)
+    return fail(PA_ERR_INVALID_ARG, "lse arrays must be 4-byte aligned");
+  if (num_rows > (int64_t{1} << 40)) return fail(PA_ERR_INVALID_ARG, "num_rows too large");
+  cudaError_t e = paq8::launch_merge_states(
+      static_cast<const uint16_t *>(out_a), lse_a, static_cast<const uint16_t *>(out_b), lse_b,
+      static_cast<uint16_t *>(out), lse, num_rows, head_dim, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

@@ -29,7 +29,8 @@ def _declared():
 def test_header_declares_the_boundary():
     names = _declared()
     for n in ("pa_kv_store", "pa_paged_attention", "pa_workspace_size", "pa_check_status",
-              "pa_status_string", "pa_auto_num_splits", "pa_last_error"):
+              "pa_status_string", "pa_auto_num_splits", "pa_last_error",
+              "pa_merge_attn_states"):
         assert n in names
 
 
@@ -134,3 +135,28 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load()
+
+
+def _merge_args(**kw):
+    a = dict(oa=16, la=16, ob=32, lb=32, out=48, lse=64, rows=10, d=128, stream=None)
+    a.update(kw)
+    v = lambda x: ctypes.c_void_p(x) if x is not None else None  # noqa: E731
+    return [v(a["oa"]), v(a["la"]), v(a["ob"]), v(a["lb"]), v(a["out"]), v(a["lse"]),
+            a["rows"], a["d"], v(a["stream"])]
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(oa=None), _lib.Status.INVALID_ARG),
+    (dict(out=None), _lib.Status.INVALID_ARG),
+    (dict(rows=-1), _lib.Status.INVALID_ARG),
+    (dict(d=96), _lib.Status.UNSUPPORTED),
+    (dict(ob=40), _lib.Status.INVALID_ARG),   # not 16-byte aligned
+    (dict(lse=66), _lib.Status.INVALID_ARG),  # not 4-byte aligned
+])
+def test_merge_attn_states_rejects_bad_arguments(lib, kw, expect):
+    assert lib.pa_merge_attn_states(*_merge_args(**kw)) == expect
+    assert lib.pa_last_error().decode()
+
+
+def test_merge_attn_states_zero_rows_is_a_no_op(lib):
+    assert lib.pa_merge_attn_states(*_merge_args(rows=0, oa=None)) == _lib.Status.OK

@@ -429,6 +429,49 @@ def test_split_segments_merged_by_lse_equal_one_joint_pass():
             assert abs(lse - full_lse[r]) < 1e-12
 
 
+def test_merge_states_of_two_key_ranges_equals_one_joint_pass():
+    # "shared/attention_kit.py" _merge_lse_: the attention over A and over B,
+    # each normalized with its LSE, merge into the attention over A u B
+    rng = np.random.default_rng(21)
+    p = _problem(rng, [1, 3], [257, 64], 4, 2, 64, 16)
+    scale = 0.125
+    full_out, full_lse = _run(p, scale)
+    args = (p["q"], p["kc"], p["ks"], p["vc"], p["vs"], p["cu"], p["sl"], p["bt"], scale)
+    for token, n in ((0, 257), (2, 63), (3, 64)):
+        for split in (1, 16, n // 2, n - 1):
+            for head in (0, 3):
+                a = oracle.attention_partial(*args, token=token, head=head, lo=0, hi=split)
+                b = oracle.attention_partial(*args, token=token, head=head, lo=split, hi=n)
+                out_a, lse_a = a[2] / a[1], a[0] + np.log(a[1])
+                out_b, lse_b = b[2] / b[1], b[0] + np.log(b[1])
+                out, lse = oracle.merge_states(out_a[None], [lse_a], out_b[None], [lse_b])
+                r = token * 4 + head
+                np.testing.assert_allclose(out[0], full_out[r], rtol=0, atol=1e-12)
+                assert abs(lse[0] - full_lse[r]) < 1e-12
+
+
+def test_merge_states_closed_forms():
+    rng = np.random.default_rng(22)
+    a = rng.standard_normal((5, 8))
+    b = rng.standard_normal((5, 8))
+    la = np.array([0.0, np.log(3.0), -np.inf, 2.0, -np.inf])
+    lb = np.array([0.0, 0.0, 1.5, -np.inf, -np.inf])
+    out, lse = oracle.merge_states(a, la, b, lb)
+    np.testing.assert_allclose(out[0], (a[0] + b[0]) / 2, rtol=0, atol=1e-15)   # equal weights
+    assert abs(lse[0] - np.log(2.0)) < 1e-15
+    np.testing.assert_allclose(out[1], 0.75 * a[1] + 0.25 * b[1], rtol=0, atol=1e-15)  # 3 : 1
+    assert abs(lse[1] - np.log(4.0)) < 1e-15
+    np.testing.assert_array_equal(out[2], b[2])        # an empty side contributes nothing
+    assert lse[2] == 1.5
+    np.testing.assert_array_equal(out[3], a[3])
+    assert lse[3] == 2.0
+    np.testing.assert_array_equal(out[4], np.zeros(8))  # no key on either side
+    assert lse[4] == -np.inf
+    out2, lse2 = oracle.merge_states(b, lb, a, la)      # symmetric in its two parts
+    np.testing.assert_allclose(out2, out, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(lse2, lse)
+
+
 def test_oracle_reports_bad_block_table():
     rng = np.random.default_rng(13)
     p = _problem(rng, [1], [40], 2, 1, 32, 16)
