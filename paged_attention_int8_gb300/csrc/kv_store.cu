@@ -18,8 +18,9 @@
 // formed as x * (1/s) and rounded there unless it lies within 2^-15 of a
 // rounding tie, where the IEEE quotient decides (the two differ by less than
 // 2.27e-5 for |x / s| <= 127.00002).
-// Memory bound: per (token, kv head) it reads 4*D bytes and writes
-// 2*(D + D/16) bytes.
+// Its roofline is HBM: per (token, kv head) it reads 4*D bytes and writes
+// 2*(D + D/16) bytes.  The V side is bound instead by memory-instruction
+// issue: each channel-major V page takes one byte per (token, channel).
 #include "common.cuh"
 #include "launch.h"
 
