@@ -55,7 +55,9 @@ def step_work(w: inputs.Workload) -> dict:
     attention: every visible (row, key) pair's K and V codes + fp16 scales
     once per kv head (sum_s L_s * Hk * 2 * (D + 2 * D/32)), plus q read, out and
     lse written, the block-table entries used and the metadata;
-    kv_store: N * Hk * (4D read + 2(D + D/16) written) + 8N slot bytes."""
+    kv_store: N * Hk * (4D read + 2(D + D/16) written) for the N rows with a
+    slot, + 8 slot bytes for every row (padding rows, slot < 0, are only
+    looked up)."""
     s = w.spec
     G = s.d // 32
     L = w.seq_lens.to(torch.int64)
@@ -65,8 +67,9 @@ def step_work(w: inputs.Workload) -> dict:
     pages = int(((L + s.bs - 1) // s.bs).sum()) * 4
     meta = (2 * S + 1) * 4
     attn_bytes = kv + q_out + pages + meta
-    n_new = int(w.new_slots.shape[0])
-    store_bytes = n_new * s.hk * (4 * s.d + 2 * (s.d + 2 * G)) + 8 * n_new
+    n_rows = int(w.new_slots.shape[0])
+    n_new = int((w.new_slots >= 0).sum())
+    store_bytes = n_new * s.hk * (4 * s.d + 2 * (s.d + 2 * G)) + 8 * n_rows
     # visible (row, key) pairs: token i of sequence s sees ctx + i + 1 keys
     ql = w.q_lens.to(torch.int64)
     ctx = L - ql
