@@ -20,6 +20,11 @@ Each function cites the page passage it follows:
   merge ``_merge_lse_`` of "shared/attention_kit.py", in natural-log form.
 * ``merge_states`` -- ``_merge_lse_`` of "shared/attention_kit.py" on two
   normalized (out, lse) results, row by row, in natural-log form.
+* ``paged_attention`` options: attention sinks (USE_SINKS of
+  "triton_turboquant_unified_attention.py"), a sliding window
+  (``window_size = (sliding_window - 1, 0)`` of "attention_impl.py") and a
+  non-causal mode for a cached prefix attended in a pass of its own (the
+  two-pass prefix of "shared/attention_kit.py", ``_attend_with_prefix``).
 
 Parity status of each function (what pins it) is listed in the design notes.
 """
@@ -77,6 +82,10 @@ def _load():
         lib.or_paged_attention.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
                                            P, P, i32, P, i32, f32, P, i64, P, P, i32]
         lib.or_paged_attention.restype = ctypes.c_int
+        lib.or_paged_attention_ex.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
+                                              P, P, i32, P, i32, f32, P, i32, i32, P, i64,
+                                              P, P, i32]
+        lib.or_paged_attention_ex.restype = ctypes.c_int
         lib.or_attention_partial.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
                                              P, P, i32, P, i32, f32, i32, i32, i64, i64,
                                              P, P, P]
@@ -199,9 +208,20 @@ def _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
 
 
 def paged_attention(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
-                    block_table, softmax_scale: float, rows=None, n_threads: int = 0):
+                    block_table, softmax_scale: float, rows=None, n_threads: int = 0,
+                    sinks=None, window: int = 0, causal: bool = True):
     """fp64 causal paged attention.  Returns (out [n, D] float64, lse [n] float64)
-    for the rows ``rows`` (row = token * Hq + q head), all T*Hq rows if None."""
+    for the rows ``rows`` (row = token * Hq + q head), all T*Hq rows if None.
+
+    Options (the defaults give plain causal attention): ``sinks`` -- per-q-head
+    sink logits [Hq] in the units of the scaled scores, added to the softmax
+    denominator only (the USE_SINKS rule of "triton_turboquant_unified_
+    attention.py"; the LSE then includes the sink); ``window`` -- sliding
+    window W > 0, the query at position p sees keys p - (W - 1) .. p
+    ("attention_impl.py", window_size = (sliding_window - 1, 0)), causal
+    only; ``causal=False`` -- every query sees all seq_len keys (a cached
+    prefix in a pass of its own).  A row with no key and no sink gets out = 0
+    and lse = -inf."""
     keep, args, T, hq, d = _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale,
                                       cu_seqlens_q, seq_lens, block_table)
     if rows is None:
@@ -213,8 +233,20 @@ def paged_attention(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, se
         rows_ptr = _ptr(rows_arr)
     out = np.empty((n, d), np.float64)
     lse = np.empty(n, np.float64)
-    err = _load().or_paged_attention(*args, ctypes.c_float(softmax_scale), rows_ptr, n,
-                                     _ptr(out), _ptr(lse), n_threads)
+    if sinks is None and window == 0 and causal:
+        err = _load().or_paged_attention(*args, ctypes.c_float(softmax_scale), rows_ptr, n,
+                                         _ptr(out), _ptr(lse), n_threads)
+    else:
+        sk = None if sinks is None else _c(np.asarray(sinks, np.float32), np.float32)
+        if sk is not None and sk.shape != (hq,):
+            raise ValueError("sinks must hold one logit per q head")
+        err = _load().or_paged_attention_ex(*args, ctypes.c_float(softmax_scale),
+                                            None if sk is None else _ptr(sk), int(window),
+                                            1 if causal else 0, rows_ptr, n, _ptr(out),
+                                            _ptr(lse), n_threads)
+        del sk
+        if err == 2:
+            raise ValueError("oracle: window must be >= 0 and needs causal attention")
     del keep
     if err:
         raise RuntimeError("oracle: invalid metadata (block table, seq_lens or cu_seqlens_q)")

@@ -276,6 +276,20 @@ typedef struct {
     const int32_t *block_table;     /* [S, bt_stride] */
     int32_t bt_stride;
     double softmax_scale;
+    /* Options (defaults: NULL, 0, 1 -- plain causal attention):
+     * sinks   [hq] per-q-head sink logit, in the units of the scaled scores,
+     *         added to the softmax denominator only ("triton_turboquant_
+     *         unified_attention.py", USE_SINKS: out = sum_i exp(s_i) v_i /
+     *         (exp(sink) + sum_i exp(s_i))); NULL = none.
+     * window  sliding window W > 0: the query at absolute position p sees
+     *         keys p - (W - 1) .. p ("attention_impl.py", window_size =
+     *         (sliding_window - 1, 0)); 0 = none.  Causal attention only.
+     * causal  1: query i of a sequence sees keys 0 .. seq_len - q_len + i;
+     *         0: every query sees keys 0 .. seq_len - 1 (a cached prefix
+     *         attended in a pass of its own), seq_len may be below q_len. */
+    const float *sinks;
+    int32_t window;
+    int32_t causal;
 } or_problem;
 
 /* HND row of key j of kv head h of sequence s, through the block table
@@ -341,7 +355,12 @@ static int or_partial(const or_problem *p, int32_t t, int32_t h, int64_t lo,
     int64_t ctx = (int64_t)p->seq_lens[s] - q_len;
     int64_t i = t - p->cu_seqlens_q[s];
     int64_t last = ctx + i;                     /* last visible key */
-    if (ctx < 0) return 1;
+    if (!p->causal) {
+        last = (int64_t)p->seq_lens[s] - 1;
+    } else {
+        if (ctx < 0) return 1;
+        if (p->window > 0 && lo < last - (p->window - 1)) lo = last - (p->window - 1);
+    }
     if (hi > last + 1) hi = last + 1;
     int32_t kvh = h / (p->hq / p->hk);
     const uint16_t *qrow = p->q + ((int64_t)t * p->hq + h) * p->d;
@@ -453,6 +472,23 @@ static void *or_worker(void *arg)
         int32_t t = (int32_t)(r / p->hq), h = (int32_t)(r % p->hq);
         double m, l;
         errors |= or_partial(p, t, h, 0, job->max_keys, scores, &m, &l, acc);
+        if (p->sinks) {
+            /* the sink logit joins the denominator with no value */
+            double sink = (double)p->sinks[h];
+            if (sink > m) {
+                double r = exp(m - sink);  /* 0 when the row has no key */
+                l *= r;
+                for (int32_t c = 0; c < p->d; ++c) acc[c] *= r;
+                m = sink;
+            }
+            if (m > -INFINITY) l += exp(sink - m);
+        }
+        if (l == 0.0) {
+            /* no key and no sink: out = 0, lse = -inf */
+            for (int32_t c = 0; c < p->d; ++c) job->out[k * p->d + c] = 0.0;
+            job->lse[k] = -INFINITY;
+            continue;
+        }
         /* one part: out = acc / l, lse = m + ln l */
         or_merge_partials(1, &m, &l, acc, p->d, job->out + k * p->d, job->lse + k);
     }
@@ -463,6 +499,9 @@ static void *or_worker(void *arg)
     free(acc);
     return NULL;
 }
+
+static int or_run_rows(const or_problem *pp, const int64_t *rows, int64_t n_rows,
+                       double *out, double *lse, int32_t n_threads);
 
 /*
  * Full attention for the listed rows (row = token * hq + q head; rows == NULL
@@ -481,7 +520,40 @@ int or_paged_attention(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
 {
     or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
                     num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
-                    bt_stride, (double)softmax_scale};
+                    bt_stride, (double)softmax_scale, NULL, 0, 1};
+    return or_run_rows(&p, rows, n_rows, out, lse, n_threads);
+}
+
+/*
+ * or_paged_attention with the options of or_problem: per-q-head sinks (or
+ * NULL), a sliding window (0 = none; causal only) and causal (1) or
+ * full-prefix (0) visibility.  A row that sees no key and has no sink gets
+ * out = 0 and lse = -inf; with a sink, lse = ln(exp(sink) + sum exp(s_i)).
+ * Returns 0, 1 on invalid metadata, 2 on an invalid option.
+ */
+int or_paged_attention_ex(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
+                          int32_t d, const int8_t *k_cache, const uint16_t *k_scale,
+                          const int8_t *v_cache, const uint16_t *v_scale,
+                          int64_t num_blocks, int32_t bs, const int32_t *cu_seqlens_q,
+                          const int32_t *seq_lens, int32_t S,
+                          const int32_t *block_table, int32_t bt_stride,
+                          float softmax_scale, const float *sinks, int32_t window,
+                          int32_t causal, const int64_t *rows, int64_t n_rows,
+                          double *out, double *lse, int32_t n_threads)
+{
+    if (window < 0 || (window > 0 && !causal)) return 2;
+    or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
+                    num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
+                    bt_stride, (double)softmax_scale, sinks, window, causal ? 1 : 0};
+    return or_run_rows(&p, rows, n_rows, out, lse, n_threads);
+}
+
+static int or_run_rows(const or_problem *pp, const int64_t *rows, int64_t n_rows,
+                       double *out, double *lse, int32_t n_threads)
+{
+    or_problem p = *pp;
+    int32_t T = p.T, hq = p.hq, S = p.S;
+    const int32_t *seq_lens = p.seq_lens;
     if (!rows) n_rows = (int64_t)T * hq;
     int64_t max_keys = 1;
     for (int32_t s = 0; s < S; ++s) if (seq_lens[s] > max_keys) max_keys = seq_lens[s];
@@ -514,7 +586,7 @@ int or_attention_partial(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
 {
     or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
                     num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
-                    bt_stride, (double)softmax_scale};
+                    bt_stride, (double)softmax_scale, NULL, 0, 1};
     int64_t n = hi > lo ? hi - lo : 1;
     double *scores = (double *)malloc(sizeof(double) * (size_t)n);
     int err = or_partial(&p, token, head, lo, hi, scores, m, l, acc);

@@ -305,6 +305,143 @@ def test_attention_matches_torch_sdpa_fp64_brute_force():
         np.testing.assert_allclose(lse[p["cu"][s]:p["cu"][s + 1]], ref_lse.numpy(), rtol=0, atol=1e-12)
 
 
+def _run_opt(p, scale, **kw):
+    return oracle.paged_attention(p["q"], p["kc"], p["ks"], p["vc"], p["vs"], p["cu"],
+                                  p["sl"], p["bt"], scale, n_threads=4, **kw)
+
+
+def _sdpa_masked(p, scale, mask_fn):
+    """Per-sequence fp64 SDPA with an explicit boolean mask mask_fn(L, ql) ->
+    [ql, L], and the logsumexp of the masked scores (rows with no visible key
+    give out 0 and -inf here, as the oracle defines them)."""
+    hq, hk, d = p["hq"], p["hk"], p["d"]
+    qf = torch.from_numpy(p["q"].view(np.int16)).view(torch.bfloat16).double()
+    outs, lses = [], []
+    for s in range(len(p["sl"])):
+        L, ql = int(p["sl"][s]), int(p["cu"][s + 1] - p["cu"][s])
+        Q = qf[p["cu"][s]:p["cu"][s + 1]].transpose(0, 1)                  # [hq, ql, d]
+        if L == 0:
+            outs.append(np.zeros((ql, hq, d)))
+            lses.append(np.full((ql, hq), -np.inf))
+            continue
+        K = torch.from_numpy(_gather(p, p["kc"], p["ks"], s, L))
+        V = torch.from_numpy(_gather(p, p["vc"], p["vs"], s, L))
+        K = K.repeat_interleave(hq // hk, dim=1).transpose(0, 1)
+        V = V.repeat_interleave(hq // hk, dim=1).transpose(0, 1)
+        mask = mask_fn(L, ql)
+        scores = ((Q @ K.transpose(1, 2)) * scale).masked_fill(~mask, float("-inf"))
+        lse = torch.logsumexp(scores, dim=-1)
+        out = torch.softmax(scores, dim=-1) @ V
+        outs.append(out.transpose(0, 1).numpy())
+        lses.append(lse.transpose(0, 1).numpy())
+    return np.concatenate(outs).reshape(-1, d), np.concatenate(lses).reshape(-1)
+
+
+@pytest.mark.parametrize("window", [1, 3, 16, 37])
+def test_sliding_window_matches_torch_brute_force(window):
+    # "attention_impl.py": window_size = (sliding_window - 1, 0) -- the query
+    # at absolute position p sees keys p - (W - 1) .. p
+    rng = np.random.default_rng(31)
+    p = _problem(rng, [4, 1, 9, 2], [60, 33, 9, 70], 6, 2, 64, 16)
+    scale = 0.125
+    out, lse = _run_opt(p, scale, window=window)
+
+    def band(L, ql):
+        pos = L - ql + torch.arange(ql)[:, None]
+        j = torch.arange(L)[None, :]
+        return (j <= pos) & (j >= pos - (window - 1))
+    ref, ref_lse = _sdpa_masked(p, scale, band)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_sliding_window_special_cases():
+    rng = np.random.default_rng(32)
+    p = _problem(rng, [3, 1], [40, 25], 4, 2, 64, 16)
+    scale = 0.2
+    full = _run(p, scale)
+    wide = _run_opt(p, scale, window=40)            # covers every visible key
+    np.testing.assert_array_equal(wide[0], full[0])
+    np.testing.assert_array_equal(wide[1], full[1])
+    one = _run_opt(p, scale, window=1)              # only the query's own position
+    qf = torch.from_numpy(p["q"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    for s, (t0, t1) in enumerate(((0, 3), (3, 4))):
+        L = int(p["sl"][s])
+        K = _gather(p, p["kc"], p["ks"], s, L)
+        V = _gather(p, p["vc"], p["vs"], s, L)
+        for t in range(t0, t1):
+            pos = L - (t1 - t0) + (t - t0)
+            for h in range(4):
+                r = t * 4 + h
+                np.testing.assert_allclose(one[0][r], V[pos, h // 2], rtol=0, atol=1e-15)
+                sc = np.float64(np.float32(scale)) * float(qf[t, h] @ K[pos, h // 2])
+                assert abs(one[1][r] - sc) < 1e-12
+
+
+def test_sinks_closed_form():
+    # "triton_turboquant_unified_attention.py", USE_SINKS: out = sum_i
+    # exp(s_i) v_i / (exp(sink) + sum_i exp(s_i)); so out_sink = out *
+    # sigmoid(lse - sink) and lse_sink = logaddexp(lse, sink)
+    rng = np.random.default_rng(33)
+    p = _problem(rng, [5, 1, 2], [50, 17, 2], 6, 3, 64, 16)
+    scale = 0.125
+    out, lse = _run(p, scale)
+    sinks = np.array([-np.inf, -3.0, 0.0, 2.5, 30.0, 1e4], np.float32)
+    so, sl = _run_opt(p, scale, sinks=sinks)
+    hq = 6
+    sk = np.tile(sinks.astype(np.float64), out.shape[0] // hq)
+    with np.errstate(over="ignore"):                 # a 1e4 sink: weight 0
+        w = 1.0 / (1.0 + np.exp(sk - lse))
+    np.testing.assert_allclose(so, out * w[:, None], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sl, np.logaddexp(lse, sk), rtol=1e-15, atol=1e-12)
+    head0 = np.arange(out.shape[0]) % hq == 0       # sink -inf: no change
+    np.testing.assert_array_equal(so[head0], out[head0])
+    np.testing.assert_array_equal(sl[head0], lse[head0])
+    with pytest.raises(ValueError):
+        _run_opt(p, scale, sinks=sinks[:3])
+
+
+def test_non_causal_matches_torch_brute_force():
+    # a cached prefix attended in a pass of its own: every query of a
+    # sequence sees all seq_len keys, seq_len may be below q_len, and a
+    # sequence with no key gives out 0 and lse -inf
+    rng = np.random.default_rng(34)
+    p = _problem(rng, [6, 1, 3], [4, 30, 1], 4, 2, 64, 16)
+    p["sl"][2] = 0
+    scale = 0.125
+    out, lse = _run_opt(p, scale, causal=False)
+    ref, ref_lse = _sdpa_masked(p, scale, lambda L, ql: torch.ones(ql, L, dtype=torch.bool))
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+    with pytest.raises(ValueError):
+        _run_opt(p, scale, causal=False, window=4)
+
+
+def test_prefix_pass_merged_with_new_keys_equals_one_causal_pass():
+    # "shared/attention_kit.py", _attend_with_prefix: the chunk's queries
+    # attend the cached prefix (all of it) and the new keys (causally) in two
+    # passes, merged by log-sum-exp; here the prefix is whole pages, so the
+    # new keys are the block table shifted by prefix / bs pages
+    rng = np.random.default_rng(35)
+    bs = 16
+    prefix = [32, 0, 48]
+    q_lens = [20, 7, 1]
+    p = _problem(rng, q_lens, [a + b for a, b in zip(prefix, q_lens)], 4, 2, 64, bs)
+    scale = 0.125
+    full_out, full_lse = _run(p, scale)
+    pre = dict(p, sl=np.array(prefix, np.int32))
+    out_a, lse_a = _run_opt(pre, scale, causal=False)
+    bt2 = np.full_like(p["bt"], -1)
+    for s, P in enumerate(prefix):
+        shifted = p["bt"][s, P // bs:]
+        bt2[s, :shifted.shape[0]] = shifted
+    new = dict(p, sl=np.array(q_lens, np.int32), bt=bt2)
+    out_b, lse_b = _run(new, scale)
+    out, lse = oracle.merge_states(out_a, lse_a, out_b, lse_b)
+    np.testing.assert_allclose(out, full_out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, full_lse, rtol=0, atol=1e-12)
+
+
 def test_one_visible_key_gives_that_value_and_its_score():
     # "attention_impl.py" single-token path: a one-key softmax is exactly 1.
     rng = np.random.default_rng(2)
