@@ -68,6 +68,10 @@ def load():
                                            i32, i32, i32, i32, ctypes.c_float, i32, P, P, P,
                                            ctypes.c_size_t, ctypes.c_uint32, P]
         lib.pa_paged_attention.restype = ctypes.c_int
+        lib.pa_paged_attention_noalloc.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                   i32, i32, i32, i32, i32, i32,
+                                                   ctypes.c_float, i32, P, P, P, P]
+        lib.pa_paged_attention_noalloc.restype = ctypes.c_int
         lib.pa_merge_attn_states.argtypes = [P, P, P, P, P, P, i64, i32, P]
         lib.pa_merge_attn_states.restype = ctypes.c_int
         lib.pa_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -179,8 +183,56 @@ def paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
     ``return_lse`` is False.  ``workspace``: optional uint8 CUDA tensor of at
     least ``workspace_size(S, Hq, D, num_splits)`` bytes whose first 4 bytes
     are zero (the device status word); allocated zeroed when omitted."""
+    _check_cuda(workspace)
+    T, hq, d, num_blocks, hk, bs, S, softmax_scale, out, lse = _attention_args(
+        q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
+        softmax_scale, out, lse, return_lse)
+    lib = load()
+    need = int(lib.pa_workspace_size(S, hq, d, num_splits))
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    st = lib.pa_paged_attention(_ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
+                                _ptr(v_scale), _ptr(cu_seqlens_q), _ptr(seq_lens),
+                                _ptr(block_table), block_table.stride(0), S, T, hq, hk, d,
+                                num_blocks, bs, int(max_query_len), int(max_seq_len),
+                                float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                0, _stream(stream))
+    _raise_if(st)
+    return (out, lse) if return_lse else out
+
+
+def paged_attention_noalloc(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
+                            block_table, max_query_len: int, max_seq_len: int,
+                            softmax_scale: float | None = None, num_splits: int = 0, out=None,
+                            lse=None, status=None, stream=None, return_lse: bool = True):
+    """paged_attention without a workspace (pa_paged_attention_noalloc): the
+    split partials live in the library's fixed 8 MiB device array, so calls
+    that overlap on the GPU race, and a split count whose partials do not fit
+    is rejected.  ``status``: optional int32 CUDA tensor that receives this
+    call's device status bits.  ``out`` / ``lse``, when omitted, are
+    allocated here by PyTorch (the library itself allocates nothing)."""
+    _check_cuda(status)
+    T, hq, d, num_blocks, hk, bs, S, softmax_scale, out, lse = _attention_args(
+        q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
+        softmax_scale, out, lse, return_lse)
+    if status is not None and (status.dtype != torch.int32 or status.numel() < 1):
+        raise TypeError("status must be an int32 tensor")
+    st = load().pa_paged_attention_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
+        _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(block_table), block_table.stride(0), S, T,
+        hq, hk, d, num_blocks, bs, int(max_query_len), int(max_seq_len), float(softmax_scale),
+        int(num_splits), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    _raise_if(st)
+    return (out, lse) if return_lse else out
+
+
+def _attention_args(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
+                    block_table, softmax_scale, out, lse, return_lse):
+    """Shared checks of the attention entry points; allocates out / lse when
+    omitted."""
     _check_cuda(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
-                out, lse, workspace)
+                out, lse)
     if q.dtype != torch.bfloat16 or not q.is_contiguous():
         raise TypeError("q must be a contiguous bf16 tensor")
     for name, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens", seq_lens),
@@ -207,19 +259,7 @@ def paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
-    lib = load()
-    need = int(lib.pa_workspace_size(S, hq, d, num_splits))
-    if workspace is None:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
-    st = lib.pa_paged_attention(_ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
-                                _ptr(v_scale), _ptr(cu_seqlens_q), _ptr(seq_lens),
-                                _ptr(block_table), block_table.stride(0), S, T, hq, hk, d,
-                                num_blocks, bs, int(max_query_len), int(max_seq_len),
-                                float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse),
-                                _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                0, _stream(stream))
-    _raise_if(st)
-    return (out, lse) if return_lse else out
+    return T, hq, d, num_blocks, hk, bs, S, softmax_scale, out, lse
 
 
 def merge_attn_states(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None,

@@ -160,3 +160,28 @@ def test_merge_attn_states_rejects_bad_arguments(lib, kw, expect):
 
 def test_merge_attn_states_zero_rows_is_a_no_op(lib):
     assert lib.pa_merge_attn_states(*_merge_args(rows=0, oa=None)) == _lib.Status.OK
+
+
+def test_bindings_mirror_the_boundary():
+    # every compute entry point of the header has a binding of the same name
+    import paged_attention_int8_gb300 as pkg
+    for name in ("kv_store", "paged_attention", "paged_attention_noalloc",
+                 "merge_attn_states", "workspace_size", "auto_num_splits", "check_status"):
+        assert name in pkg.__all__ and callable(getattr(pkg, name))
+
+
+def test_bindings_refuse_host_tensors():
+    import torch
+    q = torch.zeros((2, 4, 64), dtype=torch.bfloat16)
+    kc = torch.zeros((2, 2, 16, 64), dtype=torch.int8)
+    ks = torch.zeros((2, 2, 16, 2), dtype=torch.float16)
+    vc = torch.zeros((2, 2, 64, 16), dtype=torch.int8)
+    vs = torch.zeros((2, 2, 2, 16), dtype=torch.float16)
+    cu = torch.tensor([0, 1, 2], dtype=torch.int32)
+    sl = torch.tensor([5, 9], dtype=torch.int32)
+    bt = torch.zeros((2, 1), dtype=torch.int32)
+    for fn in (_lib.paged_attention, _lib.paged_attention_noalloc):
+        with pytest.raises(ValueError):
+            fn(q, kc, ks, vc, vs, cu, sl, bt, 1, 9)
+    with pytest.raises(ValueError):
+        _lib.merge_attn_states(q, sl.float(), q, sl.float())

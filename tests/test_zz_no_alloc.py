@@ -75,3 +75,22 @@ def test_noalloc_rejects_splits_beyond_its_scratch(cuda_device):
             ctypes.c_float(0.1), 16, p, p, None, None)
     assert st == _lib.Status.INVALID_ARG
     assert "static scratch" in lib.pa_last_error().decode()
+
+
+def test_noalloc_binding_matches_the_raw_call(cuda_device):
+    # the thin binding marshals the same arguments as the raw C call
+    w = inputs.make_workload(SPEC)
+    g = H.GpuState(w, cuda_device)
+    lib = _lib.load()
+    fn = _noalloc(lib)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    raw_out = torch.full_like(g.q, float("nan"))
+    raw_lse = torch.full((w.num_tokens, w.spec.hq), float("nan"), device=cuda_device)
+    assert _call(fn, g, w, 0, raw_out, raw_lse, status) == _lib.Status.OK
+    out, lse = _lib.paged_attention_noalloc(g.q, g.kc, g.ks, g.vc, g.vs, g.cu, g.seq_lens,
+                                            g.block_table, w.max_query_len, w.max_seq_len,
+                                            w.softmax_scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out, raw_out)
+    assert torch.equal(lse, raw_lse)
