@@ -272,6 +272,66 @@ def test_store_then_gather_is_independent_of_physical_placement():
         np.testing.assert_array_equal(a, b)
 
 
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 32), (256, 16)])
+def test_kv_store_places_each_tokens_quantized_row_at_its_slot(d, bs):
+    """What lands where: for every (token, kv head) with a slot, the codes and
+    fp16 scale bits read back at (slot // bs, head, slot % bs) -- token-major
+    K rows, channel-major V columns, read here with numpy indexing written from
+    the page layout -- equal the quantized source row of that token and head
+    (block = slot // block_size, offset = slot % block_size, as in
+    "attention_impl.py", `_store_kvcache_nhd`), and dequantize to within the
+    q8 round-trip bound of the bf16 source ("shared/attention_kit.py",
+    `quantize_q8`).  Heads get magnitudes 10^(h-1) and K / V different ones,
+    so a head or K/V exchange, or a transposed V page, breaks both checks."""
+    hk = 3
+    rng = np.random.default_rng(40 + d)
+    n_tok = 3 * bs + 5
+    num_blocks = n_tok // bs + 4
+    # distinct slots in shuffled blocks, ragged offsets, a few padding rows
+    slots = rng.permutation(num_blocks * bs)[:n_tok].astype(np.int64)
+    slots[rng.choice(n_tok, size=4, replace=False)] = -1
+    mag_k = 10.0 ** (np.arange(hk) - 1.0)
+    mag_v = 3.0 * 10.0 ** (1.0 - np.arange(hk))
+    k = torch.from_numpy(rng.standard_normal((n_tok, hk, d)) * mag_k[None, :, None])
+    v = torch.from_numpy(rng.standard_normal((n_tok, hk, d)) * mag_v[None, :, None])
+    kb, vb = _bf16_bits(k), _bf16_bits(v)
+    kc, ks, vc, vs = [t.numpy() for t in inputs.empty_cache(num_blocks, hk, bs, d)]
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    assert oracle.kv_store(kb, vb, slots, kc, ks, vc, vs) == 0
+    src = {"k": torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).double().numpy(),
+           "v": torch.from_numpy(vb.view(np.int16)).view(torch.bfloat16).double().numpy()}
+    checked = 0
+    for n in range(n_tok):
+        slot = int(slots[n])
+        if slot < 0:
+            continue
+        blk, off = slot // bs, slot % bs
+        for h in range(hk):
+            got = {"k": (kc[blk, h, off, :], ks[blk, h, off, :]),
+                   "v": (vc[blk, h, :, off], vs[blk, h, :, off])}
+            for name, bits in (("k", kb), ("v", vb)):
+                codes, scales = got[name]
+                want_c, want_s = oracle.q8_quantize_rows(bits[n, h][None, :])
+                np.testing.assert_array_equal(codes, want_c[0], err_msg=f"{name} n={n} h={h}")
+                np.testing.assert_array_equal(scales, want_s[0], err_msg=f"{name} n={n} h={h}")
+                s16 = np.repeat(scales.view(np.float16).astype(np.float64), 32)
+                x = src[name][n, h]
+                # |x - code * s16| <= s32/2 + 127 |s32 - s16| with |s32 - s16| <= 2^-11 s32
+                bound = s16 * (0.5 + 127 * 2.0 ** -11) * (1 + 2.0 ** -10)
+                assert np.all(np.abs(x - codes.astype(np.float64) * s16) <= bound), (name, n, h)
+                # each group's largest magnitude maps to +-127
+                assert np.all(np.abs(codes.reshape(-1, 32)).max(axis=1) == 127)
+            checked += 1
+    assert checked == (n_tok - 4) * hk
+    # every unwritten slot still holds the canary, in K and in V
+    written = np.zeros(num_blocks * bs, bool)
+    written[slots[slots >= 0]] = True
+    unw = np.nonzero(~written)[0]
+    assert np.all(kc[unw // bs, :, unw % bs, :] == -128)
+    assert np.all(vc.transpose(0, 3, 1, 2)[unw // bs, unw % bs] == -128)
+    assert np.all(vs.transpose(0, 3, 1, 2)[unw // bs, unw % bs] == 0xFFFF)
+
+
 # ----------------------------------------------------------------------------- attention
 
 def test_attention_matches_torch_sdpa_fp64_brute_force():
