@@ -20,6 +20,10 @@ Each function cites the page passage it follows:
   merge ``_merge_lse_`` of "shared/attention_kit.py", in natural-log form.
 * ``merge_states`` -- ``_merge_lse_`` of "shared/attention_kit.py" on two
   normalized (out, lse) results, row by row, in natural-log form.
+* ``norm_rope_rows`` / ``kv_store_norm_rope`` -- the weighted RMSNorm and the
+  rotation of "shared/kernels/qk_quant_triton.py" (``_rows``) applied to key
+  rows, quantized from fp32 in the q8 format and scattered as ``kv_store``
+  does.
 * ``paged_attention`` options: attention sinks (USE_SINKS of
   "triton_turboquant_unified_attention.py"), a sliding window
   (``window_size = (sliding_window - 1, 0)`` of "attention_impl.py") and a
@@ -94,6 +98,13 @@ def _load():
         lib.or_merge_partials.restype = None
         lib.or_merge_states.argtypes = [i64, i32, P, P, P, P, P, P]
         lib.or_merge_states.restype = None
+        lib.or_f32_to_bf16_rne.argtypes = [f32]
+        lib.or_f32_to_bf16_rne.restype = ctypes.c_uint16
+        lib.or_norm_rope_row.argtypes = [P, i32, P, f32, P, i32, i32, P]
+        lib.or_norm_rope_row.restype = None
+        lib.or_kv_store_norm_rope.argtypes = [P, P, P, P, i64, i32, i32, P, f32, P, i64, i32,
+                                              i32, P, P, P, P, i64, i32, i32]
+        lib.or_kv_store_norm_rope.restype = i64
         _lib = lib
         return lib
 
@@ -123,6 +134,11 @@ def _c(a, dtype) -> np.ndarray:
 def f32_to_f16_bits(x: float) -> int:
     """binary32 -> binary16 bits, round to nearest even (IEEE definition)."""
     return int(_load().or_f32_to_f16_rne(ctypes.c_float(x)))
+
+
+def f32_to_bf16_bits(x: float) -> int:
+    """binary32 -> bfloat16 bits, round to nearest even (IEEE definition)."""
+    return int(_load().or_f32_to_bf16_rne(ctypes.c_float(x)))
 
 
 def f16_bits_to_f32(h: int) -> float:
@@ -181,6 +197,77 @@ def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_sc
     return int(_load().or_kv_store(_ptr(key), _ptr(value), _ptr(slots), n, hk, d,
                                    _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
                                    _ptr(v_scale), num_blocks, bs, n_threads))
+
+
+# --------------------------------------------------------------------------- fused store
+
+def _rope_table(rope, rot):
+    rope = _c(np.asarray(rope, np.float32), np.float32)
+    if rope.ndim != 3 or rope.shape[1:] != (rot // 2, 2):
+        raise ValueError("rope must be fp32 [positions, rotary_dim / 2, 2] (cos, sin)")
+    return rope
+
+
+def norm_rope_rows(x_bits, norm_weight_bits=None, eps: float = 1e-6, rope_rows=None,
+                   interleaved: bool = False) -> np.ndarray:
+    """Key rows [n, D] (bf16 bits) -> the fp32 values the fused store
+    quantizes: weighted RMSNorm (norm_weight_bits bf16 bits [D], or None: no
+    norm) rounded to bf16, then the rotation of the pairs of rope_rows
+    (fp32 [n, rotary_dim / 2, 2]: cos, sin per pair, one row per token; None:
+    no rotation), split halves or interleaved pairs ("shared/kernels/
+    qk_quant_triton.py", `_rows`)."""
+    x = _c(x_bits, np.uint16)
+    n, d = x.shape
+    if d % 32 or d > 1024:
+        raise ValueError("D must be a multiple of 32, at most 1024")
+    w = None if norm_weight_bits is None else _c(norm_weight_bits, np.uint16)
+    if w is not None and w.shape != (d,):
+        raise ValueError("norm weight must hold D values")
+    rot = 0
+    if rope_rows is not None:
+        rope_rows = _c(np.asarray(rope_rows, np.float32), np.float32)
+        rot = 2 * rope_rows.shape[1]
+        if rope_rows.shape != (n, rot // 2, 2) or rot > d:
+            raise ValueError("rope rows must be [n, rotary_dim / 2, 2] with rotary_dim <= D")
+    out = np.empty((n, d), np.float32)
+    lib = _load()
+    for r in range(n):
+        lib.or_norm_rope_row(_ptr(x[r]), d, None if w is None else _ptr(w), ctypes.c_float(eps),
+                             None if rope_rows is None else _ptr(rope_rows[r]), rot,
+                             1 if interleaved else 0, _ptr(out[r]))
+    return out
+
+
+def kv_store_norm_rope(key_bits, value_bits, slot_mapping, positions, k_cache, k_scale,
+                       v_cache, v_scale, norm_weight_bits=None, eps: float = 1e-6, rope=None,
+                       interleaved: bool = False, n_threads: int = 0) -> int:
+    """kv_store with each key row normalized and rotated first (norm_rope_rows
+    with the rope row of the token's position; rope fp32 [max_position,
+    rotary_dim / 2, 2]) and quantized from the fp32 result; values stored
+    unchanged.  Returns the number of skipped rows (slot beyond the cache or
+    position outside the table)."""
+    key = _c(key_bits, np.uint16)
+    value = _c(value_bits, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    n, hk, d = key.shape
+    num_blocks, hk2, bs, d2 = k_cache.shape
+    if (hk2, d2) != (hk, d) or value.shape != key.shape or slots.shape != (n,):
+        raise ValueError("shape mismatch")
+    _check_cache(k_cache, k_scale, v_cache, v_scale)
+    pos = _c(np.zeros(n, np.int64) if positions is None else positions, np.int64)
+    w = None if norm_weight_bits is None else _c(norm_weight_bits, np.uint16)
+    rot, max_pos, table = 0, 0, None
+    if rope is not None:
+        table = _c(np.asarray(rope, np.float32), np.float32)
+        max_pos, rot = table.shape[0], 2 * table.shape[1]
+        table = _rope_table(table, rot)
+        if rot > d:
+            raise ValueError("rotary_dim must be at most D")
+    return int(_load().or_kv_store_norm_rope(
+        _ptr(key), _ptr(value), _ptr(slots), _ptr(pos), n, hk, d,
+        None if w is None else _ptr(w), ctypes.c_float(eps),
+        None if table is None else _ptr(table), max_pos, rot, 1 if interleaved else 0,
+        _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale), num_blocks, bs, n_threads))
 
 
 # --------------------------------------------------------------------------- attention

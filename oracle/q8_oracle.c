@@ -10,8 +10,10 @@
  *    (`quantize_q8`, `dequantize_q8_into`: int8 data, one FP16 scale per
  *    32 channels, scale = max|x|/127 clamped at 1e-8) and the two-set
  *    log-sum-exp merge `_merge_lse_`.
- *  - "shared/kernels/qk_quant_triton.py" (`_norm_rope_quant`): rounding half
- *    away from zero before the int8 cast.
+ *  - "shared/kernels/qk_quant_triton.py" (`_norm_rope_quant`, `_rows`):
+ *    rounding half away from zero before the int8 cast; the weighted RMSNorm
+ *    (fp32 statistics, output rounded to the activation dtype) and the fp32
+ *    rotation of channel pairs that the fused store applies to keys.
  *  - "attention_impl.py" (fastkernels-b200, `_store_kvcache_nhd`,
  *    `StoreKVCache`): scatter by slot, slot < 0 skipped,
  *    block = slot // block_size, offset = slot % block_size; the torch SDPA
@@ -123,6 +125,23 @@ uint16_t or_f32_to_f16_rne(float x)
     if (exp16 >= 31) return (uint16_t)(sign | 0x7c00u);
     uint16_t man = (uint16_t)((m * 2.0 - 1.0) * 1024.0);
     return (uint16_t)(sign | ((uint16_t)exp16 << 10) | man);
+}
+
+/*
+ * binary32 -> bfloat16 bits, round to nearest, ties to even.  bfloat16 keeps
+ * the top 16 bits of a binary32 (same exponent range): the result is the
+ * nearer of the two bfloat16 values that bracket x -- the truncation and the
+ * next value up in magnitude -- the even one on a tie.  NaN stays NaN.
+ */
+uint16_t or_f32_to_bf16_rne(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if (isnan(x)) return (uint16_t)((u >> 16) | 0x40u);   /* quiet NaN, sign kept */
+    uint32_t lower = u >> 16;                 /* truncation toward zero */
+    uint32_t rest = u & 0xffffu;              /* the dropped bits */
+    if (rest > 0x8000u || (rest == 0x8000u && (lower & 1u))) lower += 1u;  /* carries into the exponent */
+    return (uint16_t)lower;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -249,6 +268,166 @@ int64_t or_kv_store(const uint16_t *key, const uint16_t *value,
         jobs[i] = j;
     }
     for (int32_t i = 0; i < n_threads; ++i) pthread_create(&tids[i], NULL, or_store_worker, &jobs[i]);
+    int64_t bad = 0;
+    for (int32_t i = 0; i < n_threads; ++i) {
+        pthread_join(tids[i], NULL);
+        bad += jobs[i].bad;
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fused store: RMSNorm and rotation of the key rows, then q8                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One key row x [d] (bf16 bits) -> the fp32 values the fused store quantizes
+ * ("shared/kernels/qk_quant_triton.py", `_rows`, with the readings noted):
+ *  1. weighted RMSNorm when w != NULL (bf16 bits [d]):
+ *       lane sums: lane l (0..31) takes channels l, l + 32, l + 64, ... in
+ *       order, the first squared, each next one added by a fused
+ *       multiply-add (the page's lane sums for d = 128); the 32 lane sums are
+ *       then added pairwise, lane l with lane l ^ o for o = 16, 8, 4, 2, 1
+ *       (the page sums the lanes by a tree whose order it does not fix);
+ *       inv = 1 / sqrt(total / d + eps), the square root and the division
+ *       each rounded once in fp32 (the page uses an approximate hardware
+ *       rsqrt);
+ *       y_c = bf16((x_c * inv) * w_c), each product rounded to fp32, the
+ *       result rounded to the activation dtype;
+ *     otherwise y = x;
+ *  2. rotation when rope != NULL (fp32 [rot / 2][2]: cos, sin of pair p at
+ *     this token's position), for the rot / 2 pairs (lead, trail) =
+ *     (p, p + rot / 2), or (2p, 2p + 1) when interleaved:
+ *       out_lead  = fma(cos, y_lead, (-sin) * y_trail)
+ *       out_trail = fma(sin, y_lead, cos * y_trail)
+ *     in fp32, the plain product rounded first (the page's tl.fma with fp
+ *     fusion off); channels at and past rot keep y.  The rotated values stay
+ *     fp32: they are quantized without a rounding to bf16.
+ */
+void or_norm_rope_row(const uint16_t *x, int32_t d, const uint16_t *w, float eps,
+                      const float *rope, int32_t rot, int32_t interleaved, float *out)
+{
+    float y[1024];
+    for (int32_t c = 0; c < d; ++c) y[c] = or_bf16_to_f32(x[c]);
+    if (w) {
+        float lanes[32], next[32];
+        for (int32_t l = 0; l < 32; ++l) {
+            float acc = y[l] * y[l];
+            for (int32_t j = 1; j < d / 32; ++j) acc = fmaf(y[l + 32 * j], y[l + 32 * j], acc);
+            lanes[l] = acc;
+        }
+        for (int32_t o = 16; o > 0; o >>= 1) {
+            for (int32_t l = 0; l < 32; ++l) next[l] = lanes[l] + lanes[l ^ o];
+            for (int32_t l = 0; l < 32; ++l) lanes[l] = next[l];
+        }
+        float inv = 1.0f / sqrtf(lanes[0] / (float)d + eps);
+        for (int32_t c = 0; c < d; ++c) {
+            float t = y[c] * inv;
+            t = t * or_bf16_to_f32(w[c]);
+            y[c] = or_bf16_to_f32(or_f32_to_bf16_rne(t));
+        }
+    }
+    for (int32_t c = 0; c < d; ++c) out[c] = y[c];
+    if (rope) {
+        int32_t pairs = rot / 2;
+        for (int32_t p = 0; p < pairs; ++p) {
+            int32_t lead = interleaved ? 2 * p : p;
+            int32_t trail = interleaved ? 2 * p + 1 : p + pairs;
+            float cs = rope[2 * p], sn = rope[2 * p + 1];
+            float prod_lead = (-sn) * y[trail];
+            float prod_trail = cs * y[trail];
+            out[lead] = fmaf(cs, y[lead], prod_lead);
+            out[trail] = fmaf(sn, y[lead], prod_trail);
+        }
+    }
+}
+
+typedef struct {
+    const uint16_t *key, *value;
+    const int64_t *slot_mapping, *positions;
+    int64_t n0, n1;
+    int32_t hk, d;
+    const uint16_t *w;
+    float eps;
+    const float *rope;
+    int64_t max_pos;
+    int32_t rot, interleaved;
+    int8_t *k_cache, *v_cache;
+    uint16_t *k_scale, *v_scale;
+    int64_t num_blocks;
+    int32_t bs;
+    int64_t bad;
+} or_fused_job;
+
+static void *or_fused_worker(void *arg)
+{
+    or_fused_job *j = (or_fused_job *)arg;
+    int32_t groups = j->d / OR_GROUP;
+    float vals[1024];
+    for (int64_t n = j->n0; n < j->n1; ++n) {
+        int64_t slot = j->slot_mapping[n];
+        if (slot < 0) continue;
+        int64_t pos = j->rope ? j->positions[n] : 0;
+        if (slot >= j->num_blocks * j->bs || (j->rope && (pos < 0 || pos >= j->max_pos))) {
+            ++j->bad;
+            continue;
+        }
+        int64_t block = slot / j->bs, offset = slot % j->bs;
+        for (int32_t h = 0; h < j->hk; ++h) {
+            int64_t row = (block * j->hk + h) * j->bs + offset;
+            const uint16_t *ks = j->key + (n * j->hk + h) * (int64_t)j->d;
+            const uint16_t *vs = j->value + (n * j->hk + h) * (int64_t)j->d;
+            or_norm_rope_row(ks, j->d, j->w, j->eps,
+                             j->rope ? j->rope + pos * (int64_t)j->rot : NULL, j->rot,
+                             j->interleaved, vals);
+            for (int32_t g = 0; g < groups; ++g)
+                or_q8_quantize_group(vals + g * OR_GROUP, j->k_cache + row * j->d + g * OR_GROUP,
+                                     j->k_scale + row * groups + g);
+            int8_t vcodes[1024];
+            uint16_t vscales[32];
+            or_q8_quantize_rows(vs, 1, j->d, vcodes, vscales);
+            int64_t page = block * j->hk + h;
+            for (int32_t c = 0; c < j->d; ++c)
+                j->v_cache[(page * j->d + c) * j->bs + offset] = vcodes[c];
+            for (int32_t g = 0; g < groups; ++g)
+                j->v_scale[(page * groups + g) * j->bs + offset] = vscales[g];
+        }
+    }
+    return NULL;
+}
+
+/*
+ * kv_store with the key rows normalized and rotated first (or_norm_rope_row;
+ * norm_weight NULL skips the norm, rope NULL the rotation), then stored as
+ * or_kv_store stores them; values are stored unchanged.  positions [n_tokens]
+ * picks each token's row of rope (fp32 [max_pos][rot / 2][2]).  Tokens with a
+ * slot beyond the cache or a position outside [0, max_pos) are skipped and
+ * counted in the return value.
+ */
+int64_t or_kv_store_norm_rope(const uint16_t *key, const uint16_t *value,
+                              const int64_t *slot_mapping, const int64_t *positions,
+                              int64_t n_tokens, int32_t hk, int32_t d,
+                              const uint16_t *norm_weight, float eps, const float *rope,
+                              int64_t max_pos, int32_t rot, int32_t interleaved,
+                              int8_t *k_cache, uint16_t *k_scale, int8_t *v_cache,
+                              uint16_t *v_scale, int64_t num_blocks, int32_t bs,
+                              int32_t n_threads)
+{
+    if (n_threads <= 0) n_threads = (int32_t)sysconf(_SC_NPROCESSORS_ONLN);
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 512) n_threads = 512;
+    if (n_tokens < (int64_t)n_threads * 64) n_threads = 1;
+    or_fused_job jobs[512];
+    pthread_t tids[512];
+    for (int32_t i = 0; i < n_threads; ++i) {
+        or_fused_job j = {key, value, slot_mapping, positions, n_tokens * i / n_threads,
+                          n_tokens * (i + 1) / n_threads, hk, d, norm_weight, eps, rope,
+                          max_pos, rot, interleaved, k_cache, v_cache, k_scale, v_scale,
+                          num_blocks, bs, 0};
+        jobs[i] = j;
+    }
+    for (int32_t i = 0; i < n_threads; ++i)
+        pthread_create(&tids[i], NULL, or_fused_worker, &jobs[i]);
     int64_t bad = 0;
     for (int32_t i = 0; i < n_threads; ++i) {
         pthread_join(tids[i], NULL);

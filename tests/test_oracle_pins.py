@@ -675,3 +675,176 @@ def test_oracle_reports_bad_block_table():
     p["bt"][0, 1] = p["kc"].shape[0] + 5
     with pytest.raises(RuntimeError):
         _run(p, 0.1)
+
+
+# ----------------------------------------------------------------------------- fused norm + rotation store
+
+
+def test_bf16_conversion_matches_torch_round_to_nearest_even():
+    rng = np.random.default_rng(21)
+    vals = [rng.standard_normal(3000) * 10.0 ** rng.integers(-30, 30, 3000)]
+    # exact midpoints between neighbouring bf16 values (ties), normal and subnormal
+    hb = np.arange(0, 0x7f7f, 13, dtype=np.uint32)
+    lo = (hb << 16).view(np.float32).astype(np.float64)
+    hi = ((hb + 1) << 16).view(np.float32).astype(np.float64)
+    vals.append(((lo + hi) / 2).astype(np.float32))
+    vals.append(np.array([0.0, 1e-40, 3.4e38, 3.3961776e38, np.inf, 1.00390625, 1.01171875],
+                         np.float32))
+    x = np.concatenate([np.asarray(v, np.float32) for v in vals])
+    x = np.concatenate([x, -x])
+    got = np.array([oracle.f32_to_bf16_bits(float(v)) for v in x], np.uint16)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, want)
+    assert np.isnan(torch.tensor([oracle.f32_to_bf16_bits(float("nan"))], dtype=torch.int16)
+                    .view(torch.bfloat16).float().item())
+
+
+def _bf16_to_f64(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16) \
+        .double().numpy()
+
+
+def _rope_rows(rng, n, pairs, theta=None):
+    ang = rng.uniform(-np.pi, np.pi, (n, pairs)) if theta is None else theta
+    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+
+
+@pytest.mark.parametrize("d,scale", [(64, 3.0), (128, 3.0), (256, 3.0), (128, 1e-3)])
+def test_rms_norm_matches_the_closed_form_within_bf16_rounding(d, scale):
+    # y = x / sqrt(mean(x^2) + eps) * w: fp64 closed form against the oracle's
+    # fp32 statistics and bf16 output (relative 2^-8 from the output rounding,
+    # plus fp32 rounding of the statistics), with no systematic bias; at scale
+    # 1e-3 eps is as large as the mean square
+    rng = np.random.default_rng(22 + d)
+    x = _bf16_bits(torch.from_numpy(rng.standard_normal((40, d)) * scale))
+    w = _bf16_bits(torch.from_numpy(rng.uniform(0.2, 2.0, d)))
+    eps = 1e-6
+    got = oracle.norm_rope_rows(x, w, eps).astype(np.float64)
+    xf, wf = _bf16_to_f64(x), _bf16_to_f64(w)
+    want = xf / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + eps) * wf
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) * (1 + 1e-5) + 1e-30)
+    nz = want != 0
+    assert abs(np.mean((got[nz] - want[nz]) / want[nz])) <= 2.0 ** -12
+    # every value is a bf16 value (the norm output is rounded to the activation dtype)
+    np.testing.assert_array_equal(
+        _bf16_to_f64(_bf16_bits(torch.from_numpy(got))), got)
+
+
+def test_rms_norm_is_exactly_scale_invariant_for_powers_of_two():
+    # scaling a row by 2^k scales every fp32 step of the statistics exactly
+    # (with eps 0): the normalized row is bit-identical
+    rng = np.random.default_rng(23)
+    x = _bf16_bits(torch.from_numpy(rng.standard_normal((16, 128))))
+    w = _bf16_bits(torch.from_numpy(rng.uniform(0.5, 1.5, 128)))
+    base = oracle.norm_rope_rows(x, w, 0.0)
+    for k in (-6, 3, 9):
+        xs = _bf16_bits(torch.from_numpy(_bf16_to_f64(x) * 2.0 ** k))
+        np.testing.assert_array_equal(oracle.norm_rope_rows(xs, w, 0.0), base)
+
+
+def test_no_norm_no_rotation_passes_the_values_through():
+    rng = np.random.default_rng(24)
+    x = _bf16_bits(torch.from_numpy(rng.standard_normal((8, 64))))
+    np.testing.assert_array_equal(oracle.norm_rope_rows(x), _bf16_to_f64(x).astype(np.float32))
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_rotation_pairs_signs_and_identity(interleaved):
+    rng = np.random.default_rng(25)
+    n, d, rot = 6, 128, 96
+    x = _bf16_bits(torch.from_numpy(rng.standard_normal((n, d))))
+    y = _bf16_to_f64(x)
+    # cos 1, sin 0: the identity, exactly
+    ident = oracle.norm_rope_rows(x, rope_rows=_rope_rows(rng, n, rot // 2,
+                                                          np.zeros((n, rot // 2))),
+                                  interleaved=interleaved)
+    np.testing.assert_array_equal(ident, y.astype(np.float32))
+    # a quarter turn (cos 0, sin 1): lead <- -trail, trail <- lead, exactly;
+    # the pairs are (p, p + rot/2), or (2p, 2p + 1) when interleaved
+    quarter = np.stack([np.zeros((n, rot // 2)), np.ones((n, rot // 2))], -1).astype(np.float32)
+    got = oracle.norm_rope_rows(x, rope_rows=quarter, interleaved=interleaved)
+    p = np.arange(rot // 2)
+    lead, trail = (2 * p, 2 * p + 1) if interleaved else (p, p + rot // 2)
+    np.testing.assert_array_equal(got[:, lead], -y[:, trail])
+    np.testing.assert_array_equal(got[:, trail], y[:, lead])
+    np.testing.assert_array_equal(got[:, rot:], y[:, rot:])  # channels past rot unchanged
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_rotation_matches_complex_multiplication(interleaved):
+    # (y_lead + i y_trail) (cos + i sin) in fp64, within the fp32 rounding of
+    # the page's fma form; every pair keeps its length
+    rng = np.random.default_rng(26)
+    n, d, rot = 50, 128, 128
+    x = _bf16_bits(torch.from_numpy(rng.standard_normal((n, d)) * 4))
+    rows = _rope_rows(rng, n, rot // 2)
+    got = oracle.norm_rope_rows(x, rope_rows=rows, interleaved=interleaved).astype(np.float64)
+    y = _bf16_to_f64(x)
+    p = np.arange(rot // 2)
+    lead, trail = (2 * p, 2 * p + 1) if interleaved else (p, p + rot // 2)
+    z = (y[:, lead] + 1j * y[:, trail]) * (rows[..., 0].astype(np.float64)
+                                           + 1j * rows[..., 1].astype(np.float64))
+    bound = 2.0 ** -23 * (np.abs(y[:, lead]) + np.abs(y[:, trail])) * 2
+    assert np.all(np.abs(got[:, lead] - z.real) <= bound)
+    assert np.all(np.abs(got[:, trail] - z.imag) <= bound)
+
+
+def test_fused_store_without_norm_or_rotation_is_kv_store():
+    w = _small_store_problem(seed=5, hk=3, d=128, bs=32)
+    k, v, slots = w.all_key_value()
+    caches = []
+    for fused in (False, True):
+        kc, ks, vc, vs = [t.numpy() for t in inputs.empty_cache(w.num_blocks, 3, 32, 128)]
+        ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+        if fused:
+            assert oracle.kv_store_norm_rope(inputs.bf16_bits(k), inputs.bf16_bits(v),
+                                             slots.numpy(), None, kc, ks, vc, vs) == 0
+        else:
+            oracle.kv_store(inputs.bf16_bits(k), inputs.bf16_bits(v), slots.numpy(), kc, ks, vc, vs)
+        caches.append((kc, ks, vc, vs))
+    for a, b in zip(*caches):
+        np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_fused_store_quantizes_each_tokens_rotated_row_at_its_slot(interleaved):
+    # keys: normalized, rotated with the row of the token's own position, and
+    # quantized from fp32 by the group quantizer (pinned above); values exactly
+    # as kv_store stores them; a position outside the table skips the token
+    rng = np.random.default_rng(27)
+    hk, d, bs, n = 2, 128, 16, 40
+    num_blocks = 4
+    slots = rng.permutation(num_blocks * bs)[:n].astype(np.int64)
+    slots[3] = -1
+    positions = rng.integers(0, 300, n).astype(np.int64)
+    positions[7] = 300  # past the table: skipped and counted
+    table = _rope_rows(rng, 300, 32)  # rotary_dim 64 of 128
+    k = _bf16_bits(torch.from_numpy(rng.standard_normal((n, hk, d)) * 2))
+    v = _bf16_bits(torch.from_numpy(rng.standard_normal((n, hk, d))))
+    wt = _bf16_bits(torch.from_numpy(rng.uniform(0.5, 1.5, d)))
+    kc, ks, vc, vs = [t.numpy() for t in inputs.empty_cache(num_blocks, hk, bs, d)]
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    bad = oracle.kv_store_norm_rope(k, v, slots, positions, kc, ks, vc, vs, wt, 1e-5, table,
+                                    interleaved=interleaved)
+    assert bad == 1
+    vc_ref, vs_ref = [t.numpy() for t in inputs.empty_cache(num_blocks, hk, bs, d)][2:]
+    vs_ref = vs_ref.view(np.uint16)
+    kc_dummy, ks_dummy = [t.numpy() for t in inputs.empty_cache(num_blocks, hk, bs, d)][:2]
+    keep = positions < 300
+    oracle.kv_store(k[keep], v[keep], slots[keep], kc_dummy, ks_dummy.view(np.uint16), vc_ref,
+                    vs_ref)
+    np.testing.assert_array_equal(vc, vc_ref)
+    np.testing.assert_array_equal(vs, vs_ref)
+    for t in range(n):
+        if slots[t] < 0 or not keep[t]:
+            if slots[t] >= 0:
+                assert np.all(kc[slots[t] // bs, :, slots[t] % bs] == -128)
+            continue
+        rows = oracle.norm_rope_rows(k[t], wt, 1e-5, np.repeat(table[positions[t]][None], hk, 0),
+                                     interleaved=interleaved)
+        for h in range(hk):
+            for g in range(d // 32):
+                codes, sbits = oracle.q8_quantize_group(rows[h, 32 * g:32 * g + 32])
+                np.testing.assert_array_equal(kc[slots[t] // bs, h, slots[t] % bs,
+                                                 32 * g:32 * g + 32], codes)
+                assert ks[slots[t] // bs, h, slots[t] % bs, g] == sbits
