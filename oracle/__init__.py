@@ -20,6 +20,10 @@ Each function cites the page passage it follows:
   merge ``_merge_lse_`` of "shared/attention_kit.py", in natural-log form.
 * ``merge_states`` -- ``_merge_lse_`` of "shared/attention_kit.py" on two
   normalized (out, lse) results, row by row, in natural-log form.
+* ``kv_store_f8v4`` and the ``v_zero`` option of ``paged_attention`` -- the
+  alternative formats of "triton_turboquant_unified_attention.py" (FP8 keys
+  read as e4m3 values; 4-bit values dequantized as idx * scale + zero with
+  one fp16 scale and zero per token), stored by a plain quantizer.
 * ``norm_rope_rows`` / ``kv_store_norm_rope`` -- the weighted RMSNorm and the
   rotation of "shared/kernels/qk_quant_triton.py" (``_rows``) applied to key
   rows, quantized from fp32 in the q8 format and scattered as ``kv_store``
@@ -87,8 +91,8 @@ def _load():
                                            P, P, i32, P, i32, f32, P, i64, P, P, i32]
         lib.or_paged_attention.restype = ctypes.c_int
         lib.or_paged_attention_ex.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
-                                              P, P, i32, P, i32, f32, P, i32, i32, P, i64,
-                                              P, P, i32]
+                                              P, P, i32, P, i32, f32, P, i32, i32, i32, P, P,
+                                              i64, P, P, i32]
         lib.or_paged_attention_ex.restype = ctypes.c_int
         lib.or_attention_partial.argtypes = [P, i32, i32, i32, i32, P, P, P, P, i64, i32,
                                              P, P, i32, P, i32, f32, i32, i32, i64, i64,
@@ -98,6 +102,14 @@ def _load():
         lib.or_merge_partials.restype = None
         lib.or_merge_states.argtypes = [i64, i32, P, P, P, P, P, P]
         lib.or_merge_states.restype = None
+        lib.or_f32_to_e4m3.argtypes = [f32]
+        lib.or_f32_to_e4m3.restype = ctypes.c_uint8
+        lib.or_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        lib.or_e4m3_to_f32.restype = f32
+        lib.or_v4_quantize_row.argtypes = [P, i32, P, P, P]
+        lib.or_v4_quantize_row.restype = None
+        lib.or_kv_store_f8v4.argtypes = [P, P, P, i64, i32, i32, P, P, P, P, i64, i32]
+        lib.or_kv_store_f8v4.restype = i64
         lib.or_f32_to_bf16_rne.argtypes = [f32]
         lib.or_f32_to_bf16_rne.restype = ctypes.c_uint16
         lib.or_norm_rope_row.argtypes = [P, i32, P, f32, P, i32, i32, P]
@@ -199,6 +211,66 @@ def kv_store(key_bits, value_bits, slot_mapping, k_cache, k_scale, v_cache, v_sc
                                    _ptr(v_scale), num_blocks, bs, n_threads))
 
 
+# --------------------------------------------------------------------------- fp8 keys, 4-bit values
+
+def f32_to_e4m3_bits(x: float) -> int:
+    """binary32 -> fp8 e4m3 bits, round to nearest even, saturating at 448."""
+    return int(_load().or_f32_to_e4m3(ctypes.c_float(x)))
+
+
+def e4m3_bits_to_f32(b: int) -> float:
+    return float(_load().or_e4m3_to_f32(ctypes.c_uint8(b)))
+
+
+def v4_quantize_rows(x_bf16_bits: np.ndarray):
+    """Value rows [n, D] (bf16 bits) -> (nibbles uint8 [n, D/2] with channel c
+    in byte c/2, low nibble for even c; scale fp16 bits [n]; zero fp16 bits
+    [n]): idx = clamp(round_half_away((x - min) / s), 0, 15),
+    s = max((max - min) / 15, 1e-8)."""
+    x = _c(x_bf16_bits, np.uint16)
+    n, d = x.shape
+    nib = np.empty((n, d // 2), np.uint8)
+    sc = np.empty(n, np.uint16)
+    zr = np.empty(n, np.uint16)
+    lib = _load()
+    for r in range(n):
+        lib.or_v4_quantize_row(_ptr(x[r]), d, _ptr(nib[r]), _ptr(sc[r:r + 1]), _ptr(zr[r:r + 1]))
+    return nib, sc, zr
+
+
+def f8v4_cache_shapes(num_blocks: int, hk: int, bs: int, d: int):
+    """(k_cache uint8, v_cache uint8, v_scale fp16, v_zero fp16) shapes."""
+    return ((num_blocks, hk, bs, d), (num_blocks, hk, d, bs // 2), (num_blocks, hk, bs),
+            (num_blocks, hk, bs))
+
+
+def _check_f8v4(kc, vc, vs, vz):
+    nb, hk, bs, d = kc.shape
+    want = f8v4_cache_shapes(nb, hk, bs, d)
+    if (kc.shape, vc.shape, vs.shape, vz.shape) != want:
+        raise ValueError(f"fp8/4-bit cache shapes {kc.shape, vc.shape, vs.shape, vz.shape} != {want}")
+    for a, t in ((kc, np.uint8), (vc, np.uint8), (vs, np.uint16), (vz, np.uint16)):
+        if not (a.flags.c_contiguous and a.dtype == t):
+            raise TypeError("fp8/4-bit caches: contiguous uint8 codes, uint16 scale / zero bits")
+
+
+def kv_store_f8v4(key_bits, value_bits, slot_mapping, k_cache, v_cache, v_scale, v_zero) -> int:
+    """Store [N, Hk, D] bf16 rows in the alternative format: keys as fp8
+    e4m3, values as 4-bit codes with one fp16 scale and zero per (token,
+    head).  Returns the number of skipped out-of-range slots."""
+    key = _c(key_bits, np.uint16)
+    value = _c(value_bits, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    n, hk, d = key.shape
+    _check_f8v4(k_cache, v_cache, v_scale, v_zero)
+    num_blocks, hk2, bs, d2 = k_cache.shape
+    if (hk2, d2) != (hk, d) or value.shape != key.shape or slots.shape != (n,) or bs % 2:
+        raise ValueError("shape mismatch")
+    return int(_load().or_kv_store_f8v4(_ptr(key), _ptr(value), _ptr(slots), n, hk, d,
+                                        _ptr(k_cache), _ptr(v_cache), _ptr(v_scale),
+                                        _ptr(v_zero), num_blocks, bs))
+
+
 # --------------------------------------------------------------------------- fused store
 
 def _rope_table(rope, rot):
@@ -273,10 +345,16 @@ def kv_store_norm_rope(key_bits, value_bits, slot_mapping, positions, k_cache, k
 # --------------------------------------------------------------------------- attention
 
 def _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
-               block_table):
+               block_table, v_zero=None):
     q = _c(q_bits, np.uint16)
-    kc, vc = _c(k_cache, np.int8), _c(v_cache, np.int8)
-    ks, vs = _c(k_scale, np.uint16), _c(v_scale, np.uint16)
+    if v_zero is None:  # q8 caches
+        kc, vc = _c(k_cache, np.int8), _c(v_cache, np.int8)
+        ks, vs = _c(k_scale, np.uint16), _c(v_scale, np.uint16)
+        _check_cache(kc, ks, vc, vs)
+    else:               # fp8 keys, 4-bit values (k_scale unused)
+        kc, vc = _c(k_cache, np.uint8), _c(v_cache, np.uint8)
+        vs, ks = _c(v_scale, np.uint16), _c(v_zero, np.uint16)
+        _check_f8v4(kc, vc, vs, ks)
     cu = _c(cu_seqlens_q, np.int32)
     sl = _c(seq_lens, np.int32)
     bt = _c(block_table, np.int32)
@@ -284,7 +362,6 @@ def _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
     num_blocks, hk, bs, d2 = kc.shape
     if d2 != d or hq % hk:
         raise ValueError("shape mismatch")
-    _check_cache(kc, ks, vc, vs)
     S = sl.shape[0]
     if cu.shape != (S + 1,) or bt.ndim != 2 or bt.shape[0] != S:
         raise ValueError("metadata shape mismatch")
@@ -296,7 +373,7 @@ def _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_len
 
 def paged_attention(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens,
                     block_table, softmax_scale: float, rows=None, n_threads: int = 0,
-                    sinks=None, window: int = 0, causal: bool = True):
+                    sinks=None, window: int = 0, causal: bool = True, v_zero=None):
     """fp64 causal paged attention.  Returns (out [n, D] float64, lse [n] float64)
     for the rows ``rows`` (row = token * Hq + q head), all T*Hq rows if None.
 
@@ -308,9 +385,19 @@ def paged_attention(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, se
     ("attention_impl.py", window_size = (sliding_window - 1, 0)), causal
     only; ``causal=False`` -- every query sees all seq_len keys (a cached
     prefix in a pass of its own).  A row with no key and no sink gets out = 0
-    and lse = -inf."""
+    and lse = -inf.
+
+    ``v_zero`` (fp16 bits [num_blocks, Hk, bs]) selects the alternative cache
+    format of ``kv_store_f8v4``: k_cache holds e4m3 keys, v_cache 4-bit
+    values, v_scale / v_zero their per-key scale and zero; k_scale is
+    ignored (may be None)."""
     keep, args, T, hq, d = _attn_args(q_bits, k_cache, k_scale, v_cache, v_scale,
-                                      cu_seqlens_q, seq_lens, block_table)
+                                      cu_seqlens_q, seq_lens, block_table, v_zero)
+    if v_zero is not None:
+        # the C side reads the zero array from its own argument; k_scale's
+        # slot carries nothing for this format
+        zero_arr = keep[2]
+        args[6] = None
     if rows is None:
         n = T * hq
         rows_arr, rows_ptr = None, None
@@ -320,7 +407,7 @@ def paged_attention(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, se
         rows_ptr = _ptr(rows_arr)
     out = np.empty((n, d), np.float64)
     lse = np.empty(n, np.float64)
-    if sinks is None and window == 0 and causal:
+    if sinks is None and window == 0 and causal and v_zero is None:
         err = _load().or_paged_attention(*args, ctypes.c_float(softmax_scale), rows_ptr, n,
                                          _ptr(out), _ptr(lse), n_threads)
     else:
@@ -329,8 +416,9 @@ def paged_attention(q_bits, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, se
             raise ValueError("sinks must hold one logit per q head")
         err = _load().or_paged_attention_ex(*args, ctypes.c_float(softmax_scale),
                                             None if sk is None else _ptr(sk), int(window),
-                                            1 if causal else 0, rows_ptr, n, _ptr(out),
-                                            _ptr(lse), n_threads)
+                                            1 if causal else 0, 0 if v_zero is None else 1,
+                                            None if v_zero is None else _ptr(zero_arr),
+                                            rows_ptr, n, _ptr(out), _ptr(lse), n_threads)
         del sk
         if err == 2:
             raise ValueError("oracle: window must be >= 0 and needs causal attention")

@@ -21,7 +21,10 @@
  *    paged gather, GQA by repeat_interleave, causal mask k_pos <= q_pos with
  *    key_offset = k_len - q_len.
  *  - "triton_turboquant_unified_attention.py" (vLLM unified kernel): the
- *    seq_lens / query_start_loc meaning, the causal limit
+ *    K and V load sites of its alternative formats (FP8 keys read as e4m3
+ *    values; 4-bit values dequantized as idx * scale + zero with one fp16
+ *    scale and zero per token); the seq_lens / query_start_loc meaning, the
+ *    causal limit
  *    seq_offset <= context_len + query_pos, the 3D split-KV segments and the
  *    (max, expsum, acc) partial triples merged by the online-softmax rule.
  *
@@ -142,6 +145,89 @@ uint16_t or_f32_to_bf16_rne(float x)
     uint32_t rest = u & 0xffffu;              /* the dropped bits */
     if (rest > 0x8000u || (rest == 0x8000u && (lower & 1u))) lower += 1u;  /* carries into the exponent */
     return (uint16_t)lower;
+}
+
+/*
+ * binary32 -> fp8 e4m3 ("e4m3fn": 1 sign, 4 exponent bits of bias 7, 3
+ * mantissa bits, no infinities, NaN = S.1111.111), round to nearest even,
+ * saturating: magnitudes past the largest finite value 448 give 448 (the
+ * midpoint rule would send 464 and up to the NaN pattern).  Written from the
+ * definition: the two fp8 values bracketing |x| are found from its exponent
+ * and the nearer (the even one on a tie) is taken.  NaN gives 0x7f.
+ */
+uint8_t or_f32_to_e4m3(float x)
+{
+    uint8_t sign = (uint8_t)(signbit(x) ? 0x80u : 0u);
+    float a = fabsf(x);
+    if (isnan(x)) return 0x7fu;
+    if (a >= 448.0f) return (uint8_t)(sign | 0x7eu);          /* 448 = 1.75 * 2^8 */
+    /* spacing of e4m3 values at a: 2^(e - 3) for a in [2^e, 2^(e+1)),
+     * e >= -6; 2^-9 below 2^-6 (subnormals) */
+    int e;
+    if (a < ldexpf(1.0f, -6)) {
+        e = -6;
+    } else {
+        (void)frexpf(a, &e);   /* a = m * 2^e, m in [0.5, 1) */
+        e -= 1;
+    }
+    double step = ldexp(1.0, e - 3);
+    double q = (double)a / step;           /* exact */
+    double lo = floor(q), rem = q - lo, n;
+    if (rem > 0.5) n = lo + 1.0;
+    else if (rem < 0.5) n = lo;
+    else n = (fmod(lo, 2.0) == 0.0) ? lo : lo + 1.0;
+    double r = n * step;                   /* rounded magnitude, exact */
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    int re;
+    double m = frexp(r, &re);              /* r = m * 2^re, m in [0.5, 1) */
+    int exp8 = re - 1 + 7;
+    uint8_t man = (uint8_t)((m * 2.0 - 1.0) * 8.0);
+    return (uint8_t)(sign | (uint8_t)(exp8 << 3) | man);
+}
+
+/* fp8 e4m3 bits -> value (exact). */
+float or_e4m3_to_f32(uint8_t b)
+{
+    int sign = b >> 7, exp = (b >> 3) & 0xf, man = b & 7;
+    float mag;
+    if (exp == 15 && man == 7) mag = NAN;
+    else if (exp == 0) mag = ldexpf((float)man, -9);            /* subnormal: man * 2^-9 */
+    else mag = ldexpf((float)(man | 8), exp - 10);             /* 1.man * 2^(exp - 7) */
+    return sign ? -mag : mag;
+}
+
+/*
+ * 4-bit asymmetric quantization of one value row x [d] (bf16 bits), the
+ * value format whose load site the TurboQuant page shows (V = idx * scale +
+ * zero, one fp16 scale and zero per token):
+ *   lo = min x, hi = max x                       (fp32)
+ *   s32 = max((hi - lo) / 15, 1e-8)              (fp32)
+ *   idx = clamp(round_half_away((x - lo) / s32), 0, 15)   (fp32 subtract, divide)
+ *   scale = fp16(s32), zero = fp16(lo)           (round to nearest even)
+ * idx of channel c goes to nibble c of `nib` (byte c / 2, low nibble for even c).
+ */
+void or_v4_quantize_row(const uint16_t *x_bf16, int32_t d, uint8_t *nib, uint16_t *scale_bits,
+                        uint16_t *zero_bits)
+{
+    float lo = INFINITY, hi = -INFINITY;
+    for (int32_t c = 0; c < d; ++c) {
+        float v = or_bf16_to_f32(x_bf16[c]);
+        if (v < lo) lo = v;
+        if (v > hi) hi = v;
+    }
+    float s32 = (hi - lo) / 15.0f;
+    if (s32 < 1e-8f) s32 = 1e-8f;
+    for (int32_t c = 0; c < d; c += 2) nib[c / 2] = 0;
+    for (int32_t c = 0; c < d; ++c) {
+        float r = roundf((or_bf16_to_f32(x_bf16[c]) - lo) / s32);
+        if (r > 15.0f) r = 15.0f;
+        if (r < 0.0f) r = 0.0f;
+        uint8_t i = (uint8_t)r;
+        nib[c / 2] = (uint8_t)(nib[c / 2] | (c & 1 ? (uint8_t)(i << 4) : i));
+    }
+    *scale_bits = or_f32_to_f16_rne(s32);
+    *zero_bits = or_f32_to_f16_rne(lo);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -272,6 +358,50 @@ int64_t or_kv_store(const uint16_t *key, const uint16_t *value,
     for (int32_t i = 0; i < n_threads; ++i) {
         pthread_join(tids[i], NULL);
         bad += jobs[i].bad;
+    }
+    return bad;
+}
+
+/*
+ * kv_store in the alternative format: keys as fp8 e4m3 (or_f32_to_e4m3 of
+ * each bf16 value, no scale), values as 4-bit codes with a per-(token, head)
+ * fp16 scale and zero (or_v4_quantize_row).  Caches (head-major pages):
+ *   k_cache  uint8 [num_blocks][hk][bs][d]        e4m3 bits, token-major
+ *   v_cache  uint8 [num_blocks][hk][d][bs / 2]    channel-major, keys 2j and
+ *                                                  2j + 1 in the low and high
+ *                                                  nibble of byte j
+ *   v_scale, v_zero fp16 [num_blocks][hk][bs]
+ * Scatter as or_kv_store (slot < 0 skipped, slots past the cache counted).
+ */
+int64_t or_kv_store_f8v4(const uint16_t *key, const uint16_t *value,
+                         const int64_t *slot_mapping, int64_t n_tokens, int32_t hk, int32_t d,
+                         uint8_t *k_cache, uint8_t *v_cache, uint16_t *v_scale,
+                         uint16_t *v_zero, int64_t num_blocks, int32_t bs)
+{
+    int64_t bad = 0;
+    uint8_t nib[512];
+    for (int64_t n = 0; n < n_tokens; ++n) {
+        int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * bs) { ++bad; continue; }
+        int64_t block = slot / bs, offset = slot % bs;
+        for (int32_t h = 0; h < hk; ++h) {
+            int64_t page = block * hk + h;
+            const uint16_t *ks = key + (n * hk + h) * (int64_t)d;
+            const uint16_t *vs = value + (n * hk + h) * (int64_t)d;
+            for (int32_t c = 0; c < d; ++c)
+                k_cache[(page * bs + offset) * d + c] = or_f32_to_e4m3(or_bf16_to_f32(ks[c]));
+            uint16_t sb, zb;
+            or_v4_quantize_row(vs, d, nib, &sb, &zb);
+            for (int32_t c = 0; c < d; ++c) {
+                uint8_t idx = (uint8_t)((nib[c / 2] >> (4 * (c & 1))) & 0xfu);
+                uint8_t *byte = v_cache + (page * d + c) * (bs / 2) + offset / 2;
+                if (offset & 1) *byte = (uint8_t)((*byte & 0x0fu) | (idx << 4));
+                else *byte = (uint8_t)((*byte & 0xf0u) | idx);
+            }
+            v_scale[page * bs + offset] = sb;
+            v_zero[page * bs + offset] = zb;
+        }
     }
     return bad;
 }
@@ -469,6 +599,11 @@ typedef struct {
     const float *sinks;
     int32_t window;
     int32_t causal;
+    /* Cache format: 0 = q8 (the caches above); 1 = fp8 keys and 4-bit values
+     * (or_kv_store_f8v4: k_cache holds e4m3 bits, v_cache nibbles, v_scale
+     * and v_zero one fp16 per key; k_scale unused). */
+    int32_t fmt;
+    const uint16_t *v_zero;
 } or_problem;
 
 /* HND row of key j of kv head h of sequence s, through the block table
@@ -488,6 +623,8 @@ static int64_t or_kv_row(const or_problem *p, int32_t s, int32_t h, int64_t j)
  * ("shared/attention_kit.py", `dequantize_q8_into`). */
 static double or_dequant_k(const or_problem *p, int64_t row, int32_t c)
 {
+    if (p->fmt == 1)  /* fp8 key: the e4m3 value itself */
+        return (double)or_e4m3_to_f32((uint8_t)p->k_cache[row * p->d + c]);
     int32_t groups = p->d / OR_GROUP;
     double code = (double)p->k_cache[row * p->d + c];
     double sc = (double)or_f16_to_f32(p->k_scale[row * groups + c / OR_GROUP]);
@@ -498,6 +635,13 @@ static double or_dequant_k(const or_problem *p, int64_t row, int32_t c)
  * row % bs. */
 static double or_dequant_v(const or_problem *p, int64_t row, int32_t c)
 {
+    if (p->fmt == 1) {  /* 4-bit value: idx * scale + zero, exact in fp64 */
+        int64_t page = row / p->bs, off = row % p->bs;
+        uint8_t byte = (uint8_t)p->v_cache[(page * p->d + c) * (p->bs / 2) + off / 2];
+        double idx = (double)((byte >> (4 * (off & 1))) & 0xf);
+        return idx * (double)or_f16_to_f32(p->v_scale[page * p->bs + off]) +
+               (double)or_f16_to_f32(p->v_zero[page * p->bs + off]);
+    }
     int32_t groups = p->d / OR_GROUP;
     int64_t page = row / p->bs, off = row % p->bs;
     double code = (double)p->v_cache[(page * p->d + c) * p->bs + off];
@@ -699,14 +843,14 @@ int or_paged_attention(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
 {
     or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
                     num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
-                    bt_stride, (double)softmax_scale, NULL, 0, 1};
+                    bt_stride, (double)softmax_scale, NULL, 0, 1, 0, NULL};
     return or_run_rows(&p, rows, n_rows, out, lse, n_threads);
 }
 
 /*
  * or_paged_attention with the options of or_problem: per-q-head sinks (or
- * NULL), a sliding window (0 = none; causal only) and causal (1) or
- * full-prefix (0) visibility.  A row that sees no key and has no sink gets
+ * NULL), a sliding window (0 = none; causal only), causal (1) or
+ * full-prefix (0) visibility, and the cache format (fmt, v_zero).  A row that sees no key and has no sink gets
  * out = 0 and lse = -inf; with a sink, lse = ln(exp(sink) + sum exp(s_i)).
  * Returns 0, 1 on invalid metadata, 2 on an invalid option.
  */
@@ -717,13 +861,16 @@ int or_paged_attention_ex(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
                           const int32_t *seq_lens, int32_t S,
                           const int32_t *block_table, int32_t bt_stride,
                           float softmax_scale, const float *sinks, int32_t window,
-                          int32_t causal, const int64_t *rows, int64_t n_rows,
+                          int32_t causal, int32_t fmt, const uint16_t *v_zero,
+                          const int64_t *rows, int64_t n_rows,
                           double *out, double *lse, int32_t n_threads)
 {
-    if (window < 0 || (window > 0 && !causal)) return 2;
+    if (window < 0 || (window > 0 && !causal) || fmt < 0 || fmt > 1 || (fmt == 1 && !v_zero))
+        return 2;
     or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
                     num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
-                    bt_stride, (double)softmax_scale, sinks, window, causal ? 1 : 0};
+                    bt_stride, (double)softmax_scale, sinks, window, causal ? 1 : 0,
+                    fmt, v_zero};
     return or_run_rows(&p, rows, n_rows, out, lse, n_threads);
 }
 
@@ -765,7 +912,7 @@ int or_attention_partial(const uint16_t *q, int32_t T, int32_t hq, int32_t hk,
 {
     or_problem p = {q, T, hq, hk, d, k_cache, k_scale, v_cache, v_scale,
                     num_blocks, bs, cu_seqlens_q, seq_lens, S, block_table,
-                    bt_stride, (double)softmax_scale, NULL, 0, 1};
+                    bt_stride, (double)softmax_scale, NULL, 0, 1, 0, NULL};
     int64_t n = hi > lo ? hi - lo : 1;
     double *scores = (double *)malloc(sizeof(double) * (size_t)n);
     int err = or_partial(&p, token, head, lo, hi, scores, m, l, acc);

@@ -848,3 +848,178 @@ def test_fused_store_quantizes_each_tokens_rotated_row_at_its_slot(interleaved):
                 np.testing.assert_array_equal(kc[slots[t] // bs, h, slots[t] % bs,
                                                  32 * g:32 * g + 32], codes)
                 assert ks[slots[t] // bs, h, slots[t] % bs, g] == sbits
+
+
+# ----------------------------------------------------------------------------- fp8 keys, 4-bit values
+
+V4_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "v4_hand_examples.txt")
+
+
+def _load_v4_golden():
+    cases = []
+    for line in open(V4_GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, xs, nib, sb, zb = [p.strip() for p in line.split(";")]
+        x = np.array([float(v) for v in xs.split(",")], np.float32)
+        cases.append((name, x, np.array([int(b, 16) for b in nib.split(",")], np.uint8),
+                      int(sb, 16), int(zb, 16)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _load_v4_golden(), ids=lambda c: c[0])
+def test_v4_hand_examples(case):
+    name, x, nib, sbits, zbits = case
+    bits = _bf16_bits(torch.from_numpy(x))
+    assert np.array_equal(_bf16_to_f64(bits), x.astype(np.float64))  # bf16-exact inputs
+    got_nib, got_s, got_z = oracle.v4_quantize_rows(bits[None, :])
+    np.testing.assert_array_equal(got_nib[0], nib)
+    assert int(got_s[0]) == sbits and int(got_z[0]) == zbits
+
+
+def test_e4m3_conversion_matches_torch_round_to_nearest_even():
+    rng = np.random.default_rng(31)
+    vals = [rng.standard_normal(3000) * 10.0 ** rng.uniform(-3, 2.6, 3000)]
+    # midpoints between neighbouring e4m3 values (ties), normal and subnormal
+    pos = np.arange(0, 0x7e, dtype=np.uint8)
+    dec = torch.from_numpy(pos.copy()).view(torch.float8_e4m3fn).double().numpy()
+    vals.append(((dec[:-1] + dec[1:]) / 2).astype(np.float32))
+    vals.append(np.array([0.0, 448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10, 1.0, 240.0, 464.0 - 1e-3],
+                         np.float32))
+    x = np.concatenate([np.asarray(v, np.float32) for v in vals])
+    x = x[np.abs(x) < 464.0]  # where rounding to nearest stays at or below 448
+    x = np.concatenate([x, -x])
+    got = np.array([oracle.f32_to_e4m3_bits(float(v)) for v in x], np.uint8)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(got, want)
+    # saturation instead of NaN past the largest finite value
+    for v in (464.0, 480.0, 1e6, float("inf")):
+        assert oracle.f32_to_e4m3_bits(v) == 0x7e and oracle.f32_to_e4m3_bits(-v) == 0xfe
+
+
+def test_e4m3_decode_matches_torch_for_every_pattern():
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).float().numpy()
+    got = np.array([oracle.e4m3_bits_to_f32(int(b)) for b in bits], np.float32)
+    finite = np.isfinite(ref)
+    np.testing.assert_array_equal(got[finite], ref[finite])
+    assert np.all(np.isnan(got[~finite]))
+
+
+def test_v4_invariants_on_random_rows():
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((300, 128)) * 10.0 ** rng.uniform(-3, 2, (300, 1))
+    x[::7] += rng.uniform(-50, 50, (x[::7].shape[0], 1))  # rows far from zero
+    bits = _bf16_bits(torch.from_numpy(x))
+    xf = _bf16_to_f64(bits)
+    nib, sb, zb = oracle.v4_quantize_rows(bits)
+    idx = np.stack([nib & 0xF, nib >> 4], -1).reshape(300, 128).astype(np.float64)
+    s16 = sb.view(np.float16).astype(np.float64)[:, None]
+    z16 = zb.view(np.float16).astype(np.float64)[:, None]
+    lo, hi = xf.min(1, keepdims=True), xf.max(1, keepdims=True)
+    s32 = (hi - lo) / 15
+    # the row's min maps to 0 and its max to 15; a row that bf16 made constant
+    # (small noise on a large offset) maps to 0 throughout
+    flat = (hi == lo)[:, 0]
+    assert 0 < flat.sum() < 300
+    assert np.all(idx[np.arange(300), xf.argmin(1)] == 0)
+    assert np.all(idx[~flat][np.arange((~flat).sum()), xf[~flat].argmax(1)] == 15)
+    assert np.all(idx[flat] == 0)
+    s32 = np.where(flat[:, None], 1e-8, s32)
+    # each value within half a step of its code (plus fp32 rounding of the steps)
+    assert np.all(np.abs(xf - (lo + idx * s32)) <= s32 * (0.5 + 1e-5))
+    # round trip through the fp16 scale and zero: the fp16 rounding of both adds
+    # at most 15 |s32 - s16| + |lo - z16|
+    bound = s32 * 0.5 + 15 * np.abs(s32 - s16) + np.abs(lo - z16) + 1e-6 * s32
+    assert np.all(np.abs(xf - (idx * s16 + z16)) <= bound)
+
+
+def test_f8v4_store_places_each_tokens_row_at_its_slot():
+    # what lands where: keys as e4m3 of each bf16 value (checked against torch's
+    # conversion), values as the row quantizer's nibbles, read back at
+    # (slot / bs, head, slot % bs) with the channel-major nibble layout
+    hk, d, bs = 3, 64, 16
+    rng = np.random.default_rng(33)
+    n_tok, num_blocks = 45, 5
+    slots = rng.permutation(num_blocks * bs)[:n_tok].astype(np.int64)
+    slots[[2, 17]] = -1
+    k = _bf16_bits(torch.from_numpy(rng.standard_normal((n_tok, hk, d)) * 10.0 ** (np.arange(hk) - 1)[None, :, None]))
+    v = _bf16_bits(torch.from_numpy(rng.standard_normal((n_tok, hk, d)) * 3.0 ** np.arange(hk)[None, :, None]))
+    shapes = oracle.f8v4_cache_shapes(num_blocks, hk, bs, d)
+    kc = np.full(shapes[0], 0xff, np.uint8)
+    vc = np.full(shapes[1], 0xff, np.uint8)
+    vs = np.full(shapes[2], 0xffff, np.uint16)
+    vz = np.full(shapes[3], 0xffff, np.uint16)
+    assert oracle.kv_store_f8v4(k, v, slots, kc, vc, vs, vz) == 0
+    for t in range(n_tok):
+        if slots[t] < 0:
+            continue
+        blk, off = slots[t] // bs, slots[t] % bs
+        for h in range(hk):
+            want_k = torch.from_numpy(_bf16_to_f64(k[t, h]).astype(np.float32)).to(
+                torch.float8_e4m3fn).view(torch.uint8).numpy()
+            np.testing.assert_array_equal(kc[blk, h, off], want_k)
+            nib, sb, zb = oracle.v4_quantize_rows(v[t, h][None])
+            idx = np.stack([nib[0] & 0xF, nib[0] >> 4], -1).reshape(d)
+            got = (vc[blk, h, :, off // 2] >> (4 * (off % 2))) & 0xF
+            np.testing.assert_array_equal(got, idx)
+            assert vs[blk, h, off] == sb[0] and vz[blk, h, off] == zb[0]
+    written = np.zeros(num_blocks * bs, bool)
+    written[slots[slots >= 0]] = True
+    unw = np.nonzero(~written)[0]
+    assert np.all(kc[unw // bs, :, unw % bs] == 0xff)
+    assert np.all(vs[unw // bs, :, unw % bs] == 0xffff)
+
+
+def test_attention_over_f8v4_cache_matches_torch_sdpa():
+    # brute force on the dequantized values (e4m3 keys; idx * scale + zero values)
+    # with torch's fp64 scaled_dot_product_attention and an explicit causal mask
+    rng = np.random.default_rng(34)
+    hq, hk, d, bs = 4, 2, 64, 16
+    q_lens, seq_lens = [5, 1, 3], [21, 40, 3]
+    S = 3
+    pages = [(L + bs - 1) // bs for L in seq_lens]
+    num_blocks = sum(pages) + 2
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    bt = np.full((S, max(pages)), -1, np.int32)
+    pos = 0
+    for s, n in enumerate(pages):
+        bt[s, :n] = perm[pos:pos + n]
+        pos += n
+    cu = np.zeros(S + 1, np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    T = int(cu[-1])
+    shapes = oracle.f8v4_cache_shapes(num_blocks, hk, bs, d)
+    kc = rng.integers(0, 256, shapes[0]).astype(np.uint8)
+    kc[(kc & 0x7f) == 0x7f] = 0x3c  # no NaN patterns
+    vc = rng.integers(0, 256, shapes[1]).astype(np.uint8)
+    vs = np.asarray(rng.uniform(0.01, 0.2, shapes[2]), np.float16).view(np.uint16)
+    vz = np.asarray(rng.uniform(-1, 1, shapes[3]), np.float16).view(np.uint16)
+    qb = _bf16_bits(torch.from_numpy(rng.standard_normal((T, hq, d))))
+    scale = d ** -0.5
+    out, lse = oracle.paged_attention(qb, kc, None, vc, vs, cu, np.array(seq_lens, np.int32),
+                                      bt, scale, v_zero=vz)
+    kdeq = torch.from_numpy(kc.copy()).view(torch.float8_e4m3fn).double().numpy()
+    idx = np.stack([vc & 0xF, vc >> 4], -1).reshape(num_blocks, hk, d, bs)
+    vdeq = idx * vs.view(np.float16).astype(np.float64)[:, :, None, :] + \
+        vz.view(np.float16).astype(np.float64)[:, :, None, :]      # [nb, hk, d, bs]
+    qf = _bf16_to_f64(qb)
+    for s in range(S):
+        L, ql = seq_lens[s], q_lens[s]
+        j = np.arange(L)
+        K = kdeq[bt[s, j // bs], :, j % bs, :]                  # [L, hk, d]
+        V = vdeq[bt[s, j // bs], :, :, j % bs]                  # [L, hk, d]
+        qs = torch.from_numpy(qf[cu[s]:cu[s + 1]]).transpose(0, 1)          # [hq, ql, d]
+        Kt = torch.from_numpy(K).transpose(0, 1).repeat_interleave(hq // hk, 0)
+        Vt = torch.from_numpy(V).transpose(0, 1).repeat_interleave(hq // hk, 0)
+        mask = torch.from_numpy(np.arange(L)[None, :] <= (L - ql + np.arange(ql))[:, None])
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, Kt, Vt, attn_mask=mask,
+                                                               scale=scale)
+        sc = (qs @ Kt.transpose(1, 2)) * scale
+        ref_lse = torch.logsumexp(sc.masked_fill(~mask, float("-inf")), -1)
+        rows = (np.arange(cu[s], cu[s + 1])[:, None] * hq + np.arange(hq)[None, :]).T
+        np.testing.assert_allclose(out[rows.reshape(-1)].reshape(hq, ql, d), ref.numpy(),
+                                   rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[rows.reshape(-1)].reshape(hq, ql), ref_lse.numpy(),
+                                   rtol=1e-12, atol=1e-12)
