@@ -8,10 +8,13 @@ paged_attention over the cache (unified causal prefill/decode, split-KV
 segments merged by LSE where the call splits).  The cache prefix is populated
 before timing; inputs live in HBM when the timed region starts.
 
-Default workload: the decode batch (64 sequences, one query token each, KV
-lengths uniform in [512, 8192], 32 q / 8 kv heads, D = 128, block size 16).
-Its KV cache (~0.6 GB) is larger than L2, so no flush is needed between steps;
-a workload whose KV bytes fit in twice the L2 gets a 512 MiB buffer write
+Headline workload: long-context decode at D = 256 (8 sequences x 131072 keys,
+32 q / 8 kv heads, block size 16, 16 KV segments merged by LSE; 4.56 GB of
+KV per step), the largest of the serving workloads that fits one GPU.  The
+same run measures every serving workload (decode batch, chunked prefill,
+mixed batch, long decode at D = 128 and 256) and reports each under
+"workloads" with its own roofline fraction and clocks.
+A workload whose KV bytes fit in twice the L2 gets a 512 MiB buffer write
 between timed steps, outside the per-step CUDA events that time it.
 Metric: algorithmic HBM bytes of a step / step time (GB/s); prefill-only
 workloads report attention TFLOP/s instead.
@@ -455,12 +458,165 @@ def metric_for(spec: inputs.Spec):
     return METRIC, "GB/s", "hbm"
 
 
+# The default line: the largest workload that fits one GPU (4.56 GB of KV per
+# step), with every serving workload measured in the same process beside it.
+HEADLINE = "long_decode_d256"
+SUITE = ("decode_batch", "chunked_prefill", "mixed_batch", "long_decode", "long_decode_d256")
+
+
+def timed_steps(r: Runner, steps: int, flush: bool, world: int, device):
+    """Time exactly `steps` steps between barriers and synchronizes, sampling
+    the SM clocks meanwhile.  Returns (ms of all steps, mean ms of the
+    attention call alone, clocks)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if flush else None
+    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(steps)] if flush else None
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record()
+    for i in range(steps):
+        if flush:
+            # a working set that fits in L2 would be served from it on the
+            # next step: write a buffer larger than L2 between timed steps,
+            # outside the per-step events
+            flush_buf.fill_(i & 0xFF)
+            steps_ev[i][0].record()
+        r.step(ev[i])
+        if flush:
+            steps_ev[i][1].record()
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = clocks.stop(t_wall0, t_wall1)
+    if flush:
+        ms_total = sum(a.elapsed_time(b) for a, b in steps_ev)
+    else:
+        ms_total = e0.elapsed_time(e1)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    del flush_buf
+    return ms_total, attn_ms, clk
+
+
+def roofline_of(name, spec, w, work, attn_ms, ns_eff, hbm_peak, tc_peak, peak_src):
+    """Roofline of the attention call (the dominant kernels of a step).
+
+    HBM-bound workloads: algorithmic bytes per call / call time against the
+    measured copy bandwidth.  Prefill: attention FLOPs / call time against the
+    measured dense bf16 peak.  A batch with both (the mixed batch) also gets
+    both parts, bytes / bandwidth and FLOPs / peak, and the larger of the two
+    as the roofline time."""
+    _, _, bound = metric_for(spec)
+    bytes_ms = work["attn_bytes"] / (hbm_peak * 1e9) * 1e3
+    flops_ms = work["flops"] / (tc_peak * 1e12) * 1e3
+    if bound == "hbm":
+        achieved = work["attn_bytes"] / (attn_ms * 1e-3) * 1e-9
+        peak, runit = hbm_peak, "GB/s"
+    else:
+        achieved = work["flops"] / (attn_ms * 1e-3) * 1e-12
+        peak, runit = tc_peak, "TFLOP/s"
+    traffic = recorded_traffic(name)
+    roof = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "traffic_source": (f"profiles/attention_{name}.md (ncu dram bytes, recorded on the "
+                               "current kernel sources)") if traffic is not None else None,
+            "kernel": "paged_attention call (%d kernel launches)"
+                      % attention_launches(spec, w.max_query_len, ns_eff),
+            "launch_ms": round(attn_ms, 5), "peak_source": peak_src,
+            "algorithmic_per_launch": work["attn_bytes"] if bound == "hbm" else work["flops"]}
+    if spec.n_prefill and (spec.n_decode or spec.fixed_decode_lens):
+        roof["parts"] = {"bytes_ms": round(bytes_ms, 6), "flops_ms": round(flops_ms, 6),
+                         "roofline_ms": round(max(bytes_ms, flops_ms), 6),
+                         "frac_of_roofline_time": round(max(bytes_ms, flops_ms) / attn_ms, 4),
+                         "tflops": round(work["flops"] / (attn_ms * 1e-3) * 1e-12, 2)}
+    return roof
+
+
+def run_workload(name, args, device, rank, world, headline: bool):
+    """Build one workload, time it, and measure its extras.  Returns the
+    entry of the JSON line (and the headline's fields when asked)."""
+    spec = inputs.WORKLOADS[name]
+    metric, unit, bound = metric_for(spec)
+    w = inputs.make_workload(replica_spec(spec, rank))
+    work = step_work(w)
+    r = Runner(w, device, args.num_splits)
+    for _ in range(args.warmup):
+        r.step()
+    r.check()
+    flush = work["kv_bytes"] <= 2 * L2_BYTES
+    ms_total, attn_ms, clk = timed_steps(r, args.steps, flush, world, device)
+    r.check()
+    units_local = work["flops"] if unit == "TFLOP/s" else work["step_bytes"]
+    if world > 1:
+        ms_total, units_per_step = reduce_over_ranks(ms_total, units_local, device)
+    else:
+        units_per_step = units_local
+    ms_step = ms_total / args.steps
+    scale = 1e-12 if unit == "TFLOP/s" else 1e-9
+    value = units_per_step / (ms_step * 1e-3) * scale
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    entry = {"value": round(value, 3), "unit": unit, "ms_per_step": round(ms_step, 5),
+             "roofline": roofline_of(name, spec, w, work, attn_ms, r.ns_eff, hbm_peak, tc_peak,
+                                     peak_src),
+             "clocks": clk,
+             "config": {"workload": name, "num_seqs": w.num_seqs, "num_tokens": w.num_tokens,
+                        "q_heads": spec.hq, "kv_heads": spec.hk, "head_dim": spec.d,
+                        "block_size": spec.bs, "max_seq_len": w.max_seq_len,
+                        "sum_kv_len": int(w.seq_lens.sum()), "num_splits": r.ns_eff,
+                        "l2": ("L2 flushed between steps (%d MiB written, untimed)"
+                               % (FLUSH_BYTES >> 20)) if flush
+                        else "inputs larger than L2 (no flush)"},
+             "step_bytes": work["step_bytes"], "step_flops": work["flops"],
+             "gpu_launches": r.launches_per_step * args.steps}
+    if rank == 0 and not args.no_kv_store:
+        store = kv_store_measure(r)
+        if store is not None:
+            store["peak"] = hbm_peak
+            store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
+        entry["kv_store"] = store
+    if headline and rank == 0:
+        if not args.no_kv_store:
+            merge = merge_measure(r)
+            merge["peak"] = hbm_peak
+            merge["frac"] = round(merge["achieved_gbs"] / hbm_peak, 4)
+            entry["merge_attn_states"] = merge
+        if not args.no_e2e:
+            e2e_ms, h2d, d2h = e2e_measure(r, max(10, args.steps // 10), 5)
+            entry["e2e"] = {"value": units_local / (e2e_ms * 1e-3) * scale, "unit": unit,
+                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                            "ms_per_step": e2e_ms}
+        if world == 1 and not args.no_cpu_baseline:
+            cb = cpu_baseline(w)
+            cv = (cb["flops"] * 1e-12 if unit == "TFLOP/s" else cb["bytes"] * 1e-9) / cb["seconds"]
+            entry["cpu_baseline"] = {
+                "value": round(cv, 4), "unit": unit, "cores": cb["cores"], "kind": "oracle",
+                "sample": f"kv_store of the step's {int(w.new_slots.shape[0])} new rows + "
+                          f"fp64 attention of {cb['rows']} of {cb['rows_total']} (token, q head) "
+                          f"rows, {cb['seconds']:.1f} s"}
+    del r, w
+    torch.cuda.empty_cache()
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="decode_batch", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS),
+                    help="the workload of the line's headline value")
+    ap.add_argument("--only", action="store_true",
+                    help="measure the headline workload alone (no 'workloads' suite)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--num-splits", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -491,119 +647,30 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    w = inputs.make_workload(replica_spec(spec, rank))
-    work = step_work(w)
-    r = Runner(w, device, args.num_splits)
-    for _ in range(args.warmup):
-        r.step()
-    r.check()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    # a working set that fits in L2 would be served from it on the next step:
-    # write a buffer larger than L2 between timed steps, outside the timing
-    flush = work["kv_bytes"] <= 2 * L2_BYTES
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if flush else None
-    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)] if flush else None
-    clocks = ClockSampler(device.index)
-    clocks.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    e0.record()
-    for i in range(args.steps):
-        if flush:
-            flush_buf.fill_(i & 0xFF)
-            steps_ev[i][0].record()
-        r.step(ev[i])
-        if flush:
-            steps_ev[i][1].record()
-    e1.record()
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    clk = clocks.stop(t_wall0, t_wall1)
-    r.check()
-    if flush:
-        ms_total = sum(a.elapsed_time(b) for a, b in steps_ev)
-    else:
-        ms_total = e0.elapsed_time(e1)
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    units_local = work["flops"] if unit == "TFLOP/s" else work["step_bytes"]
-    if world > 1:
-        ms_total, units_per_step = reduce_over_ranks(ms_total, units_local, device)
-    else:
-        units_per_step = units_local
-    ms_step = ms_total / args.steps
-    scale = 1e-12 if unit == "TFLOP/s" else 1e-9
-    value = units_per_step / (ms_step * 1e-3) * scale
-
-    e2e = None
-    if not args.no_e2e and rank == 0:
-        e2e_ms, h2d, d2h = e2e_measure(r, max(10, args.steps // 10), 5)
-        e2e = {"value": units_local / (e2e_ms * 1e-3) * scale, "unit": unit,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
-
-    hbm_peak, tc_peak, peak_src = load_peaks()
-    if bound == "hbm":
-        achieved = work["attn_bytes"] / (attn_ms * 1e-3) * 1e-9
-        peak, runit = hbm_peak, "GB/s"
-    else:
-        achieved = work["flops"] / (attn_ms * 1e-3) * 1e-12
-        peak, runit = tc_peak, "TFLOP/s"
-    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
-                "kernel": "paged_attention call (%d kernel launches)"
-                          % attention_launches(spec, w.max_query_len, r.ns_eff),
-                "launch_ms": round(attn_ms, 5), "peak_source": peak_src,
-                "algorithmic_per_launch": work["attn_bytes"] if bound == "hbm" else work["flops"]}
-
-    store = None
-    if rank == 0 and not args.no_kv_store:
-        store = kv_store_measure(r)
-        if store is not None:
-            store["peak"] = hbm_peak
-            store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
-
-    merge = None
-    if rank == 0 and not args.no_kv_store:
-        merge = merge_measure(r)
-        merge["peak"] = hbm_peak
-        merge["frac"] = round(merge["achieved_gbs"] / hbm_peak, 4)
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(w)
-        cv = (cb["flops"] * 1e-12 if unit == "TFLOP/s" else cb["bytes"] * 1e-9) / cb["seconds"]
-        cpu = {"value": round(cv, 4), "unit": unit, "cores": cb["cores"], "kind": "oracle",
-               "sample": f"kv_store of the step's {int(w.new_slots.shape[0])} new rows + "
-                         f"fp64 attention of {cb['rows']} of {cb['rows_total']} (token, q head) "
-                         f"rows, {cb['seconds']:.1f} s"}
+    suite = {}
+    if not args.only:
+        for name in SUITE:
+            if name != args.workload:
+                suite[name] = run_workload(name, args, device, rank, world, headline=False)
+    head = run_workload(args.workload, args, device, rank, world, headline=True)
+    suite[args.workload] = {k: v for k, v in head.items()
+                            if k not in ("e2e", "cpu_baseline", "merge_attn_states")}
 
     if rank == 0:
         line = {
-            "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "metric": metric, "value": head["value"], "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int8 cache, fp16 mma, fp32 softmax", "data": "synthetic",
-            "config": {"workload": args.workload, "num_seqs": w.num_seqs,
-                       "num_tokens": w.num_tokens, "q_heads": spec.hq, "kv_heads": spec.hk,
-                       "head_dim": spec.d, "block_size": spec.bs, "max_seq_len": w.max_seq_len,
-                       "sum_kv_len": int(w.seq_lens.sum()), "num_splits": r.ns_eff,
-                       "l2": ("L2 flushed between steps (%d MiB written, untimed)"
-                              % (FLUSH_BYTES >> 20)) if flush
-                       else "inputs larger than L2 (no flush)",
-                       "parallelism": f"replicas x{world}"},
-            "roofline": roofline, "kv_store": store, "merge_attn_states": merge,
-            "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": r.launches_per_step * args.steps, "clocks": clk,
-            "step_bytes": work["step_bytes"], "step_flops": work["flops"],
+            "config": dict(head["config"], parallelism=f"replicas x{world}"),
+            "roofline": head["roofline"], "kv_store": head.get("kv_store"),
+            "merge_attn_states": head.get("merge_attn_states"),
+            "cpu_baseline": head.get("cpu_baseline"), "e2e": head.get("e2e"),
+            "gpu_launches": sum(e["gpu_launches"] for e in suite.values()),
+            "clocks": head["clocks"],
+            "step_bytes": head["step_bytes"], "step_flops": head["step_flops"],
+            "workloads": {n: suite[n] for n in SUITE if n in suite},
         }
         print(json.dumps(line))
     if world > 1:
@@ -641,7 +708,11 @@ def run_reference(args, spec, metric, unit, world, rank):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
+            "config": {"workload": args.workload, "num_seqs": w.num_seqs,
+                       "num_tokens": w.num_tokens, "q_heads": spec.hq, "kv_heads": spec.hk,
+                       "head_dim": spec.d, "block_size": spec.bs, "max_seq_len": w.max_seq_len,
+                       "sum_kv_len": int(w.seq_lens.sum()),
+                       "parallelism": f"replicas x{world}"},
             "cpu_baseline": {"value": round(value, 5), "unit": unit, "cores": threads,
                              "kind": "oracle",
                              "sample": f"{n} of {rows_all.size} (token, q head) rows per step"},

@@ -61,6 +61,12 @@ typedef enum {
 #define PA_DEV_BAD_BLOCK 0x2u  /* block_table entry outside [0, num_blocks) or past its row */
 #define PA_DEV_BAD_SEQ   0x4u  /* seq_len < q_len, or cu_seqlens_q inconsistent */
 #define PA_DEV_TIMEOUT   0x8u  /* a pipeline wait gave up after its time limit */
+#define PA_DEV_BAD_Q     0x10u /* a q value outside the fp16 range (|q| >= 65520 or NaN) */
+#define PA_DEV_BAD_POS   0x20u /* kv_store_norm_rope: a position outside the rotation table */
+
+/* Flags of pa_paged_attention / pa_paged_attention_ex. */
+#define PA_ATTN_NON_CAUSAL   0x1u  /* every query of a sequence sees all of its seq_len keys */
+#define PA_ATTN_TEST_TIMEOUT 0x80000000u /* test hook, see pa_paged_attention_ex */
 
 /*
  * kv_store -- quantize new K/V rows to q8 and scatter them into the paged
@@ -87,6 +93,47 @@ pa_status pa_kv_store(const void *key, int64_t key_token_stride,
                       void *k_cache, void *k_scale, void *v_cache, void *v_scale,
                       int32_t num_blocks, int32_t block_size,
                       uint32_t *status, void *stream);
+
+/*
+ * kv_store_norm_rope -- kv_store with each key row normalized and rotated
+ * first, in one pass from the projection output to the q8 cache.
+ * Passage: "shared/kernels/qk_quant_triton.py" (`_norm_rope_quant`, `_rows`):
+ * the weighted RMSNorm with fp32 statistics, its output rounded to the
+ * activation dtype (bf16), then the fp32 rotation of channel pairs, and the
+ * quantization reading the fp32 rotated values (no second bf16 rounding).
+ * Here the quantization is the q8 format above and the scatter is kv_store's.
+ *
+ *   key, value, slot_mapping, caches, status: as pa_kv_store.
+ *   positions     int64 [num_tokens]: the row of `rope` of each token (may be
+ *                 NULL when rope is NULL).  A position outside
+ *                 [0, max_position) skips the token and is flagged
+ *                 PA_DEV_BAD_POS.
+ *   norm_weight   bf16 [head_dim] (2-byte aligned), or NULL: no norm.  Per key
+ *                 row x: total = sum of x_c^2 (lane l of 32 adds channels l,
+ *                 l + 32, ... with fused multiply-adds, the 32 lane sums by an
+ *                 xor butterfly 16, 8, 4, 2, 1), inv = 1 / sqrt(total /
+ *                 head_dim + eps) (sqrt and divide rounded once each),
+ *                 y_c = bf16((x_c * inv) * w_c).
+ *   rope          fp32 [max_position][rotary_dim / 2][2] (cos, sin of each
+ *                 pair), 8-byte aligned, or NULL: no rotation.  Pairs
+ *                 (p, p + rotary_dim / 2), or (2p, 2p + 1) when interleaved;
+ *                 lead = fma(cos, y_lead, (-sin) * y_trail), trail =
+ *                 fma(sin, y_lead, cos * y_trail) in fp32; channels at and
+ *                 past rotary_dim keep y.  rotary_dim even, in
+ *                 [2, head_dim].
+ * Values are stored unchanged, as pa_kv_store stores them.  Every step is
+ * rounded as written, so the codes and scales equal those of a CPU
+ * implementation of the same steps bit for bit.  Asynchronous.
+ */
+pa_status pa_kv_store_norm_rope(const void *key, int64_t key_token_stride,
+                                const void *value, int64_t value_token_stride,
+                                const int64_t *slot_mapping, const int64_t *positions,
+                                int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                const void *norm_weight, float eps, const float *rope,
+                                int32_t max_position, int32_t rotary_dim, int32_t interleaved,
+                                void *k_cache, void *k_scale, void *v_cache, void *v_scale,
+                                int32_t num_blocks, int32_t block_size, uint32_t *status,
+                                void *stream);
 
 /*
  * Split-KV segments chosen when pa_paged_attention gets num_splits == 0, for
@@ -139,12 +186,20 @@ size_t pa_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim
  *                 softmax_scale * q.k over the visible keys, or NULL.
  *   workspace     device buffer of workspace_bytes >= pa_workspace_size(...);
  *                 its first 4 bytes are the status word (zero it once).
- *   flags         must be 0.
+ *   flags         0 (causal) or PA_ATTN_NON_CAUSAL: every query of sequence s
+ *                 sees keys 0 .. seq_len - 1, and seq_len may be below q_len
+ *                 (even 0: such rows get out = 0, lse = -inf).  This is the
+ *                 first pass of attention over a cached prefix plus new keys
+ *                 ("shared/attention_kit.py", `_attend_with_prefix`): attend
+ *                 the prefix non-causally, the new keys causally, and merge
+ *                 the two with pa_merge_attn_states.
  * Rows of tokens no sequence owns are not written.  Asynchronous.
  * Numerics: K codes enter the QK^T product exactly (fp16 integers), each
  * 32-channel group accumulated in fp32 and then scaled; q is rounded to fp16
- * (exact for |q| in [2^-14, 65504]); V is dequantized to fp16 (code * scale);
- * softmax and accumulation in fp32; the output rounded to bf16.
+ * (exact for |q| in [2^-14, 65504]; below 2^-14 the error is under 2^-25;
+ * |q| >= 65520 becomes inf and is flagged PA_DEV_BAD_Q); V is dequantized to
+ * fp16 (code * scale); softmax and accumulation in fp32; the output rounded
+ * to bf16.
  */
 pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_scale,
                              const void *v_cache, const void *v_scale,
@@ -156,6 +211,46 @@ pa_status pa_paged_attention(const void *q, const void *k_cache, const void *k_s
                              float softmax_scale, int32_t num_splits,
                              void *out, float *lse, void *workspace, size_t workspace_bytes,
                              uint32_t flags, void *stream);
+
+/*
+ * paged_attention with attention sinks and a sliding window.
+ * Passages: "triton_turboquant_unified_attention.py", USE_SINKS (a per-q-head
+ * sink logit starts the online softmax as M = sink, L = 1 -- one term of the
+ * denominator with no value -- in segment 0 only when the keys are split);
+ * "attention_impl.py", `window_size = (sliding_window - 1, 0)` (a query sees
+ * only the last sliding_window keys up to its causal limit).
+ *
+ *   sinks           fp32 [num_q_heads] sink logits, in the units of the
+ *                   scaled scores softmax_scale * q.k (natural log), finite
+ *                   or -inf (no sink); NULL = none.  The LSE then includes the
+ *                   sink: lse = ln(exp(sink) + sum_j exp(s_j)).
+ *   sliding_window  0 = none; W > 0: query i of sequence s sees keys
+ *                   max(0, p - W + 1) .. p, p = seq_len - q_len + i.  Needs
+ *                   causal attention (PA_ERR_INVALID_ARG with
+ *                   PA_ATTN_NON_CAUSAL).  Pages wholly before a q-block's
+ *                   first visible key are never read, so their block-table
+ *                   entries may be stale.
+ *   flags           PA_ATTN_NON_CAUSAL as for pa_paged_attention, and
+ *                   PA_ATTN_TEST_TIMEOUT, a test hook: the decode kernel's
+ *                   producer stages nothing and its waits give up after about
+ *                   1 ms, so that the call ends with PA_DEV_TIMEOUT in the
+ *                   status word (pa_check_status: PA_ERR_TIMEOUT) and
+ *                   garbage rows; the context stays usable.  Only on the
+ *                   decode path (max_query_len == 1, at most 8 q heads per kv
+ *                   head); never in production.
+ * Other arguments, errors and numerics as pa_paged_attention, which is this
+ * call with sinks = NULL and sliding_window = 0.
+ */
+pa_status pa_paged_attention_ex(const void *q, const void *k_cache, const void *k_scale,
+                                const void *v_cache, const void *v_scale,
+                                const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                const int32_t *block_table, int32_t block_table_stride,
+                                int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                int32_t block_size, int32_t max_query_len, int32_t max_seq_len,
+                                float softmax_scale, int32_t num_splits, const float *sinks,
+                                int32_t sliding_window, void *out, float *lse, void *workspace,
+                                size_t workspace_bytes, uint32_t flags, void *stream);
 
 /*
  * merge_attn_states -- the attention of queries over the union of two
@@ -209,8 +304,10 @@ pa_status pa_check_status(uint32_t *status, uint32_t *bits_out, void *stream);
  *           (overwritten, not OR-ed); NULL = no reporting.
  * A num_splits > 1 whose partials exceed 8 MiB is rejected
  * (PA_ERR_INVALID_ARG); num_splits == 0 picks the largest automatic count that
- * fits.  The first call on a device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * fits.  Every call looks up the array's device address with the current
+ * device (cheap; it follows the module if a context is recreated); the first
+ * call on a device may load the module, so make it before any stream capture.
+ * Arguments are checked before the array or the stream is touched.
  * Every call shares the one array: calls that overlap on the GPU (other
  * streams, other threads) race and give wrong results; serialize them.
  * Allocates nothing (no cudaMalloc, cudaFree or allocating library call).

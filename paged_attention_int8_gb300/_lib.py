@@ -33,6 +33,11 @@ DEV_BAD_SLOT = 0x1
 DEV_BAD_BLOCK = 0x2
 DEV_BAD_SEQ = 0x4
 DEV_TIMEOUT = 0x8
+DEV_BAD_Q = 0x10
+DEV_BAD_POS = 0x20
+
+ATTN_NON_CAUSAL = 0x1
+ATTN_TEST_TIMEOUT = 0x80000000
 
 
 class PagedAttentionError(RuntimeError):
@@ -60,6 +65,10 @@ def load():
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         lib.pa_kv_store.argtypes = [P, i64, P, i64, P, i32, i32, i32, P, P, P, P, i32, i32, P, P]
         lib.pa_kv_store.restype = ctypes.c_int
+        lib.pa_kv_store_norm_rope.argtypes = [P, i64, P, i64, P, P, i32, i32, i32, P,
+                                              ctypes.c_float, P, i32, i32, i32, P, P, P, P, i32,
+                                              i32, P, P]
+        lib.pa_kv_store_norm_rope.restype = ctypes.c_int
         lib.pa_auto_num_splits.argtypes = [i32, i32, i32, i32]
         lib.pa_auto_num_splits.restype = i32
         lib.pa_workspace_size.argtypes = [i32, i32, i32, i32]
@@ -68,6 +77,10 @@ def load():
                                            i32, i32, i32, i32, ctypes.c_float, i32, P, P, P,
                                            ctypes.c_size_t, ctypes.c_uint32, P]
         lib.pa_paged_attention.restype = ctypes.c_int
+        lib.pa_paged_attention_ex.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                              i32, i32, i32, i32, i32, ctypes.c_float, i32, P,
+                                              i32, P, P, P, ctypes.c_size_t, ctypes.c_uint32, P]
+        lib.pa_paged_attention_ex.restype = ctypes.c_int
         lib.pa_paged_attention_noalloc.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                    i32, i32, i32, i32, i32, i32,
                                                    ctypes.c_float, i32, P, P, P, P]
@@ -95,16 +108,27 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, device=None):
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
 def _check_cuda(*tensors):
+    """Every tensor given is a CUDA tensor, and all are on one device (the
+    library launches on the current device, so a tensor of another GPU would
+    be read through a foreign pointer).  Returns that device."""
+    device = None
     for t in tensors:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError("all tensors must be CUDA tensors")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise ValueError(f"tensors on different devices: {device} and {t.device}")
+    return device
 
 
 def _check16(name, t):
@@ -131,7 +155,7 @@ def kv_store(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, statu
     ``v_cache`` int8 [num_blocks, Hk, D, bs], ``v_scale`` [num_blocks, Hk, D/32, bs]
     (scales fp16 or their int16 bits).
     ``status``: optional int32 CUDA tensor (>= 1 element, zeroed) for device checks."""
-    _check_cuda(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, status)
+    device = _check_cuda(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, status)
     if key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
         raise TypeError("key and value must be bf16")
     if slot_mapping.dtype != torch.int64:
@@ -154,10 +178,59 @@ def kv_store(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, statu
         if not t.is_contiguous():
             raise ValueError("caches and slot_mapping must be contiguous")
     lib = load()
-    st = lib.pa_kv_store(_ptr(key), key.stride(0), _ptr(value), value.stride(0),
-                         _ptr(slot_mapping), n, hk, d, _ptr(k_cache), _ptr(k_scale),
-                         _ptr(v_cache), _ptr(v_scale), num_blocks, bs, _ptr(status),
-                         _stream(stream))
+    with torch.cuda.device(device):
+        st = lib.pa_kv_store(_ptr(key), key.stride(0), _ptr(value), value.stride(0),
+                             _ptr(slot_mapping), n, hk, d, _ptr(k_cache), _ptr(k_scale),
+                             _ptr(v_cache), _ptr(v_scale), num_blocks, bs, _ptr(status),
+                             _stream(stream, device))
+    _raise_if(st)
+
+
+def kv_store_norm_rope(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale,
+                       positions=None, norm_weight=None, eps: float = 1e-6, rope=None,
+                       interleaved: bool = False, status=None, stream=None) -> None:
+    """kv_store with each key row normalized and rotated first
+    (pa_kv_store_norm_rope): ``norm_weight`` bf16 [D] or None (no norm),
+    ``eps`` fp32; ``rope`` fp32 [max_position, rotary_dim / 2, 2] (cos, sin
+    per pair) or None (no rotation), ``positions`` int64 [N] the table row of
+    each token, ``interleaved`` pairs (2p, 2p + 1) instead of (p, p +
+    rotary_dim / 2).  Values are stored as ``kv_store`` stores them."""
+    device = _check_cuda(key, value, slot_mapping, k_cache, k_scale, v_cache, v_scale, status,
+                         positions, norm_weight, rope)
+    if key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
+        raise TypeError("key and value must be bf16")
+    if slot_mapping.dtype != torch.int64 or (positions is not None
+                                             and positions.dtype != torch.int64):
+        raise TypeError("slot_mapping and positions must be int64")
+    n, hk, d = key.shape
+    if value.shape != key.shape or slot_mapping.shape != (n,):
+        raise ValueError("key/value/slot_mapping shapes differ")
+    for t in (key, value):
+        if t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError("key/value head and channel dims must be contiguous")
+    num_blocks, hk2, bs, d2 = k_cache.shape
+    if (hk2, d2) != (hk, d):
+        raise ValueError("cache shape mismatch")
+    _check_cache_shapes(k_cache, k_scale, v_cache, v_scale)
+    if norm_weight is not None and (norm_weight.dtype != torch.bfloat16
+                                    or norm_weight.shape != (d,)
+                                    or not norm_weight.is_contiguous()):
+        raise TypeError("norm_weight must be a contiguous bf16 tensor [head_dim]")
+    max_pos, rot = 0, 0
+    if rope is not None:
+        if rope.dtype != torch.float32 or rope.dim() != 3 or rope.shape[2] != 2 \
+                or not rope.is_contiguous():
+            raise TypeError("rope must be a contiguous fp32 tensor [max_position, pairs, 2]")
+        if positions is None or positions.shape != (n,) or not positions.is_contiguous():
+            raise ValueError("a rotation needs int64 positions [num_tokens]")
+        max_pos, rot = rope.shape[0], 2 * rope.shape[1]
+    lib = load()
+    with torch.cuda.device(device):
+        st = lib.pa_kv_store_norm_rope(
+            _ptr(key), key.stride(0), _ptr(value), value.stride(0), _ptr(slot_mapping),
+            _ptr(positions), n, hk, d, _ptr(norm_weight), float(eps), _ptr(rope), max_pos, rot,
+            1 if interleaved else 0, _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
+            num_blocks, bs, _ptr(status), _stream(stream, device))
     _raise_if(st)
 
 
@@ -173,31 +246,41 @@ def workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, num_splits: i
 def paged_attention(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
                     max_query_len: int, max_seq_len: int, softmax_scale: float | None = None,
                     num_splits: int = 0, out=None, lse=None, workspace=None, stream=None,
-                    return_lse: bool = True):
-    """Unified causal paged attention over the q8 cache.
+                    return_lse: bool = True, causal: bool = True, sinks=None,
+                    sliding_window: int = 0, flags: int = 0):
+    """Unified paged attention over the q8 cache (pa_paged_attention_ex).
 
     q [T, Hq, D] bf16; cu_seqlens_q int32 [S+1]; seq_lens int32 [S] (KV length
     including the new tokens); block_table int32 [S, max_blocks].
     ``max_query_len`` / ``max_seq_len`` are host-side upper bounds (no sync).
+    ``causal=False``: every query sees all seq_len keys of its sequence
+    (seq_len may be below q_len).  ``sinks``: optional fp32 [Hq] sink logits;
+    ``sliding_window``: W > 0 keeps the last W keys of each query (causal
+    only).  ``flags``: extra PA_ATTN_* bits (test hooks).
     Returns (out bf16 [T, Hq, D], lse fp32 [T, Hq]) or out alone when
     ``return_lse`` is False.  ``workspace``: optional uint8 CUDA tensor of at
     least ``workspace_size(S, Hq, D, num_splits)`` bytes whose first 4 bytes
     are zero (the device status word); allocated zeroed when omitted."""
-    _check_cuda(workspace)
+    device = _check_cuda(q, workspace, sinks)
     T, hq, d, num_blocks, hk, bs, S, softmax_scale, out, lse = _attention_args(
         q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
         softmax_scale, out, lse, return_lse)
+    if sinks is not None and (sinks.dtype != torch.float32 or sinks.shape != (hq,)
+                              or not sinks.is_contiguous()):
+        raise TypeError("sinks must be a contiguous fp32 tensor [num_q_heads]")
     lib = load()
     need = int(lib.pa_workspace_size(S, hq, d, num_splits))
     if workspace is None:
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
-    st = lib.pa_paged_attention(_ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
-                                _ptr(v_scale), _ptr(cu_seqlens_q), _ptr(seq_lens),
-                                _ptr(block_table), block_table.stride(0), S, T, hq, hk, d,
-                                num_blocks, bs, int(max_query_len), int(max_seq_len),
-                                float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse),
-                                _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                0, _stream(stream))
+    flags = int(flags) | (0 if causal else ATTN_NON_CAUSAL)
+    with torch.cuda.device(device):
+        st = lib.pa_paged_attention_ex(
+            _ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
+            _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(block_table), block_table.stride(0), S, T,
+            hq, hk, d, num_blocks, bs, int(max_query_len), int(max_seq_len),
+            float(softmax_scale), int(num_splits), _ptr(sinks), int(sliding_window), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), flags,
+            _stream(stream, device))
     _raise_if(st)
     return (out, lse) if return_lse else out
 
@@ -212,17 +295,19 @@ def paged_attention_noalloc(q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q,
     is rejected.  ``status``: optional int32 CUDA tensor that receives this
     call's device status bits.  ``out`` / ``lse``, when omitted, are
     allocated here by PyTorch (the library itself allocates nothing)."""
-    _check_cuda(status)
+    device = _check_cuda(q, status)
     T, hq, d, num_blocks, hk, bs, S, softmax_scale, out, lse = _attention_args(
         q, k_cache, k_scale, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
         softmax_scale, out, lse, return_lse)
     if status is not None and (status.dtype != torch.int32 or status.numel() < 1):
         raise TypeError("status must be an int32 tensor")
-    st = load().pa_paged_attention_noalloc(
-        _ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
-        _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(block_table), block_table.stride(0), S, T,
-        hq, hk, d, num_blocks, bs, int(max_query_len), int(max_seq_len), float(softmax_scale),
-        int(num_splits), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    with torch.cuda.device(device):
+        st = load().pa_paged_attention_noalloc(
+            _ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
+            _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(block_table), block_table.stride(0), S, T,
+            hq, hk, d, num_blocks, bs, int(max_query_len), int(max_seq_len),
+            float(softmax_scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(status),
+            _stream(stream, device))
     _raise_if(st)
     return (out, lse) if return_lse else out
 
@@ -269,7 +354,7 @@ def merge_attn_states(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=Non
     natural-log LSEs lse_a, lse_b fp32 [...] (-inf = no key).  ``out`` may be
     out_a or out_b and ``lse`` lse_a or lse_b (in place).  Returns (out, lse)
     or out alone when ``return_lse`` is False."""
-    _check_cuda(out_a, lse_a, out_b, lse_b, out, lse)
+    device = _check_cuda(out_a, lse_a, out_b, lse_b, out, lse)
     for name, t in (("out_a", out_a), ("out_b", out_b)):
         if t.dtype != torch.bfloat16 or not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous bf16 tensor")
@@ -289,8 +374,9 @@ def merge_attn_states(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=Non
     elif lse is not None and (lse.numel() != rows or lse.dtype != torch.float32
                               or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous fp32 tensor with one value per row")
-    st = load().pa_merge_attn_states(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b),
-                                     _ptr(out), _ptr(lse), rows, d, _stream(stream))
+    with torch.cuda.device(device):
+        st = load().pa_merge_attn_states(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b),
+                                         _ptr(out), _ptr(lse), rows, d, _stream(stream, device))
     _raise_if(st)
     return (out, lse) if return_lse else out
 
@@ -300,8 +386,11 @@ def check_status(status_tensor, stream=None) -> int:
     tensor or an attention workspace).  Returns the raw bits; raises
     PagedAttentionError when any bit is set."""
     lib = load()
+    device = _check_cuda(status_tensor)
     bits = ctypes.c_uint32(0)
-    st = lib.pa_check_status(_ptr(status_tensor), ctypes.byref(bits), _stream(stream))
+    with torch.cuda.device(device):
+        st = lib.pa_check_status(_ptr(status_tensor), ctypes.byref(bits),
+                                 _stream(stream, device))
     if st == Status.CUDA:
         _raise_if(st)
     if st != Status.OK:

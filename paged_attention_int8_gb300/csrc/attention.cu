@@ -14,6 +14,7 @@
 //                      log-sum-exp (the pages' reduce_segments step).
 // A batch that holds only decode rows (max_query_len == 1) launches no
 // prefill kernel; both kernels exit at once for rows that are not theirs.
+#include <algorithm>
 #include <mutex>
 
 #include "attn_common.cuh"
@@ -36,7 +37,8 @@ constexpr int kPrefillTile = 64;
 // online-softmax merge rule (the pages' reduce_segments is not shown):
 //   M = max m_k;  w_k = 2^(m_k - M);  out = sum w_k acc_k / sum w_k l_k;
 //   lse = (M + log2 sum w_k l_k) * ln 2.
-// One warp per (sequence, q head); segment k exists when k * seg_keys < seq_len.
+// One warp per (sequence, q head); the segments that exist are those the
+// kernel that wrote them counts (segments_of over the visible keys).
 template <int D>
 __global__ void __launch_bounds__(128) reduce_kernel(const float *__restrict__ part_acc,
                                                      const float *__restrict__ part_ml,
@@ -44,7 +46,8 @@ __global__ void __launch_bounds__(128) reduce_kernel(const float *__restrict__ p
                                                      const int32_t *__restrict__ seq_lens,
                                                      int32_t num_seqs, int32_t num_tokens,
                                                      int32_t hq, int32_t num_splits,
-                                                     int32_t seg_keys, uint16_t *__restrict__ out,
+                                                     int32_t seg_tile, int32_t seg_tiles,
+                                                     int32_t window, uint16_t *__restrict__ out,
                                                      float *__restrict__ lse) {
   constexpr int V = D / 32;  // channels per lane
   // launched as a programmatic dependent of the decode / prefill kernel:
@@ -59,7 +62,8 @@ __global__ void __launch_bounds__(128) reduce_kernel(const float *__restrict__ p
   if (cu[seq + 1] - q0 != 1 || q0 < 0 || q0 >= num_tokens) return;
   const int L = seq_lens[seq];
   if (L < 1) return;
-  const int nseg = min(num_splits, static_cast<int>((L + seg_keys - 1) / seg_keys));
+  const int kv_begin = window > 0 ? max(0, L - window) : 0;
+  const int nseg = segments_of(kv_begin, L, seg_tile, seg_tiles, num_splits);
   const int64_t prow = gw * num_splits;
   float m = -INFINITY, l = 0.0f;
   if (lane < nseg) {
@@ -201,7 +205,12 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   a.num_blocks = L.num_blocks;
   a.bt_stride = L.bt_stride;
   a.num_splits = L.num_splits;
-  a.scale_log2 = L.softmax_scale * 1.4426950408889634f;
+  a.scale_log2 = L.softmax_scale * kLog2e;
+  a.causal = L.causal ? 1 : 0;
+  a.window = L.window;
+  a.sinks = L.sinks;
+  a.test_timeout = L.test_timeout ? 1 : 0;
+  a.wait_limit_ns = L.test_timeout ? kTestWaitLimitNs : kWaitLimitNs;
   a.part_acc = reinterpret_cast<float *>(L.workspace + 256);
   a.part_ml = a.part_acc + static_cast<int64_t>(L.num_seqs) * L.hq * L.num_splits * L.d;
 
@@ -216,10 +225,17 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
                   L.bs == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
 
+  // keys a single-token row sees at most: the hint, or the window plus the
+  // tile that a window start may fall into
+  auto hint_tiles = [&](int tile) {
+    int tiles = (L.max_seq_len + tile - 1) / tile;
+    if (L.window > 0) tiles = std::min(tiles, (L.window + tile - 1) / tile + 1);
+    return tiles;
+  };
   int seg_tile = kPrefillTile;
   if (use_decode) {
     seg_tile = decode_tile(L.d);
-    const int tiles = (L.max_seq_len + seg_tile - 1) / seg_tile;
+    const int tiles = hint_tiles(seg_tile);
     a.seg_tiles = (tiles + L.num_splits - 1) / L.num_splits;
     if (a.seg_tiles < 1) a.seg_tiles = 1;
     a.block_q = 1;
@@ -266,7 +282,7 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     p.n_qblocks = p.block_q == 1 ? L.num_tokens : L.num_tokens / p.block_q + L.num_seqs;
     p.skip_single = use_decode ? 1 : 0;
     if (!use_decode) {
-      const int tiles = (L.max_seq_len + kPrefillTile - 1) / kPrefillTile;
+      const int tiles = hint_tiles(kPrefillTile);
       p.seg_tiles = (tiles + L.num_splits - 1) / L.num_splits;
       if (p.seg_tiles < 1) p.seg_tiles = 1;
       a.seg_tiles = p.seg_tiles;
@@ -278,7 +294,6 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
 
   const int64_t warps = static_cast<int64_t>(L.num_seqs) * L.hq;
   const unsigned blocks = static_cast<unsigned>((warps + 3) / 4);
-  const int seg_keys = a.seg_tiles * seg_tile;
   // programmatic dependent launch: the reduce's blocks are scheduled while
   // the previous kernel drains, and wait for it inside (griddepcontrol.wait)
   cudaLaunchConfig_t cfg = {};
@@ -295,8 +310,8 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     cudaError_t e = cudaLaunchKernelEx(&cfg, reduce_kernel<DD>,                                  \
                                        static_cast<const float *>(a.part_acc),                   \
                                        static_cast<const float *>(a.part_ml), L.cu, L.seq_lens,  \
-                                       L.num_seqs, L.num_tokens, L.hq, L.num_splits, seg_keys,   \
-                                       a.out, L.lse);                                            \
+                                       L.num_seqs, L.num_tokens, L.hq, L.num_splits, seg_tile,   \
+                                       a.seg_tiles, L.window, a.out, L.lse);                     \
     if (e != cudaSuccess) return e;                                                              \
     break;                                                                                       \
   }

@@ -35,7 +35,60 @@ struct AttnArgs {
   int32_t skip_single;          // prefill kernel: leave single-token sequences alone
   int32_t multi_token_ok;       // decode kernel: a prefill kernel runs for q_len > 1
   float scale_log2;             // softmax_scale * log2(e)
+  // Visibility.  causal: query i of a sequence sees keys up to
+  // seq_len - q_len + i; otherwise every key of the sequence (seq_len may then
+  // be below q_len, even 0).  window > 0: a query whose last visible key is p
+  // sees keys p - window + 1 .. p only (causal only).
+  int32_t causal;
+  int32_t window;
+  const float *sinks;           // [Hq] sink logits (units of the scaled scores) or null
+  int32_t test_timeout;         // test hook: the decode producer stages nothing
+  uint64_t wait_limit_ns;       // bound of every pipeline wait of the decode kernel
 };
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Last visible key of local query token i of a sequence (-1: none).
+__device__ __forceinline__ int last_key(const AttnArgs &a, int seq_len, int q_len, int i) {
+  return a.causal ? seq_len - q_len + i : seq_len - 1;
+}
+
+// First visible key of a query whose last visible key is `last`.
+__device__ __forceinline__ int first_key(const AttnArgs &a, int last) {
+  return a.window > 0 ? max(0, last - a.window + 1) : 0;
+}
+
+// Sink logit of q head hh in log2 units, -inf without sinks.
+__device__ __forceinline__ float sink_log2(const AttnArgs &a, int hh) {
+  return a.sinks ? a.sinks[hh] * kLog2e : -INFINITY;
+}
+
+// Tiles of `tile` keys holding the visible keys [kv_begin, kv_end) of a
+// single-token row, and how many of them each split segment takes: the
+// decode kernel, the generic kernel and the segment reduce all use this
+// rule, so they agree on which segments exist.
+__device__ __forceinline__ int segments_of(int kv_begin, int kv_end, int tile, int seg_tiles,
+                                           int num_splits) {
+  const int vis_tiles = (kv_end + tile - 1) / tile - kv_begin / tile;
+  return min(num_splits, (vis_tiles + seg_tiles - 1) / seg_tiles);
+}
+
+// out = 0 and lse = sink (or -inf) for the q heads [hh0, hh0 + n) of token
+// `tok`: a row that sees no key (only in non-causal mode, seq_len == 0).
+// Called by one warp.
+template <int D>
+__device__ __forceinline__ void write_empty_rows(const AttnArgs &a, int tok, int hh0, int n,
+                                                 int lane) {
+  for (int r = 0; r < n; ++r) {
+    uint16_t *dst = a.out + (static_cast<int64_t>(tok) * a.hq + hh0 + r) * D;
+    for (int c = lane * 8; c < D; c += 256)
+      *reinterpret_cast<uint4 *>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0 && a.lse) {
+      const float s = a.sinks ? a.sinks[hh0 + r] : -INFINITY;
+      a.lse[static_cast<int64_t>(tok) * a.hq + hh0 + r] = s;
+    }
+  }
+}
 
 // Layout of one pipeline stage of TILE keys (a whole number of pages):
 //   K codes  [TILE][D]    token-major pages in the 128-byte swizzle pattern
@@ -128,12 +181,14 @@ __device__ __forceinline__ int perm16(int k) {
 // `seq`, kv head h, staging each tile's pages through an NST-stage mbarrier
 // ring (stage s at smem_base + s * L::kBytes).
 // Block-table entries are read 32 pages at a time, one per lane.
+// Pages wholly before kv_begin (keys no query of the tile range sees) or at or
+// past kv_end are not staged; the consumers mask their keys.
 template <class L, int BS, int NST = kStages>
 __device__ __forceinline__ void produce_tiles(const AttnArgs &a, const CUtensorMap *tmap_k,
                                               const CUtensorMap *tmap_v, uint32_t smem_base,
                                               uint32_t bar_full, uint32_t bar_empty, int seq,
-                                              int h, int tile_lo, int n_iter, int kv_end,
-                                              int lane) {
+                                              int h, int tile_lo, int n_iter, int kv_begin,
+                                              int kv_end, int lane) {
   const int n_pages = (kv_end + BS - 1) / BS;
   const int32_t *bt_row = a.block_table + static_cast<int64_t>(seq) * a.bt_stride;
   int page_base = -(1 << 30);
@@ -142,7 +197,7 @@ __device__ __forceinline__ void produce_tiles(const AttnArgs &a, const CUtensorM
     const int stage = it % NST;
     if (it >= NST) {
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / NST) - 1) & 1);
+      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / NST) - 1) & 1, a.wait_limit_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
@@ -154,7 +209,7 @@ __device__ __forceinline__ void produce_tiles(const AttnArgs &a, const CUtensorM
       page_base = lp0;
       const int lp = page_base + lane;
       my_blk = -1;
-      if (lp < n_pages) {
+      if (lp < n_pages && (lp + 1) * BS > kv_begin) {
         const int b = lp < a.bt_stride ? bt_row[lp] : -1;
         if (b >= 0 && b < a.num_blocks) my_blk = b;
         else flag_status(a.status, PA_DEV_BAD_BLOCK);
@@ -209,11 +264,13 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 // expects 32 arrivals) when its copies land.  A page costs 2 * BS * (D +
 // D/16) / 16 chunks spread over the 32 lanes, instead of four TMA requests:
 // the TMA unit's per-request cost, not bandwidth, limited small pages.
+// it0: ring position of the first tile (a persistent kernel keeps one ring
+// position across its work items).  Returns false when a wait gave up.
 template <class L, int BS, int NST = kStages>
-__device__ __forceinline__ void produce_tiles_lsu(const AttnArgs &a, uint32_t smem_base,
+__device__ __forceinline__ bool produce_tiles_lsu(const AttnArgs &a, uint32_t smem_base,
                                                   uint32_t bar_full, uint32_t bar_empty, int seq,
-                                                  int h, int tile_lo, int n_iter, int kv_end,
-                                                  int lane) {
+                                                  int h, int tile_lo, int n_iter, int kv_begin,
+                                                  int kv_end, int lane, int it0 = 0) {
   constexpr int D = L::kD;
   constexpr int kKChunks = BS * D / 16;        // K (or V) code chunks of a page
   constexpr int kPer = kKChunks / 32;          // ... per lane
@@ -244,14 +301,15 @@ __device__ __forceinline__ void produce_tiles_lsu(const AttnArgs &a, uint32_t sm
   int page_base = -(1 << 30);
   int my_blk = -1;
   for (int it = 0; it < n_iter; ++it) {
-    const int stage = it % NST;
-    if (it >= NST) {
+    const int g = it0 + it;  // ring position
+    const int stage = g % NST;
+    if (g >= NST) {
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / NST) - 1) & 1);
+      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((g / NST) - 1) & 1, a.wait_limit_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
-        return;
+        return false;
       }
     }
     const int lp0 = (tile_lo + it) * L::kPages;
@@ -259,7 +317,7 @@ __device__ __forceinline__ void produce_tiles_lsu(const AttnArgs &a, uint32_t sm
       page_base = lp0;
       const int lp = page_base + lane;
       my_blk = -1;
-      if (lp < n_pages) {
+      if (lp < n_pages && (lp + 1) * BS > kv_begin) {
         const int b = lp < a.bt_stride ? bt_row[lp] : -1;
         if (b >= 0 && b < a.num_blocks) my_blk = b;
         else flag_status(a.status, PA_DEV_BAD_BLOCK);
@@ -289,20 +347,21 @@ __device__ __forceinline__ void produce_tiles_lsu(const AttnArgs &a, uint32_t sm
     }
     cp_async_arrive(bar_full + 8 * stage);
   }
+  return true;
 }
 
 // Load 4 consecutive fp16 V scales (keys 4t..4t+3 of group g) as two half2
-// words, zeroing keys at or beyond kv_end (stale bytes may sit there).
+// words, zeroing keys outside [kv_begin, kv_end) (stale bytes may sit there).
 template <class L>
-__device__ __forceinline__ uint2 v_scales4(uint32_t st, int key, int g, bool tail, int key0,
-                                           int kv_end) {
+__device__ __forceinline__ uint2 v_scales4(uint32_t st, int key, int g, bool edge, int key0,
+                                           int kv_begin, int kv_end) {
   uint2 s = lds64(st + L::vs_off(key, g));
-  if (tail) {
+  if (edge) {
     const int k = key0 + key;
-    if (k + 0 >= kv_end) s.x &= 0xffff0000u;
-    if (k + 1 >= kv_end) s.x &= 0x0000ffffu;
-    if (k + 2 >= kv_end) s.y &= 0xffff0000u;
-    if (k + 3 >= kv_end) s.y &= 0x0000ffffu;
+    if (k + 0 >= kv_end || k + 0 < kv_begin) s.x &= 0xffff0000u;
+    if (k + 1 >= kv_end || k + 1 < kv_begin) s.x &= 0x0000ffffu;
+    if (k + 2 >= kv_end || k + 2 < kv_begin) s.y &= 0xffff0000u;
+    if (k + 3 >= kv_end || k + 3 < kv_begin) s.y &= 0x0000ffffu;
   }
   return s;
 }

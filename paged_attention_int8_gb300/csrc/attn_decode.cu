@@ -6,6 +6,10 @@
 // (3D split-KV kernel): m = max_j s_j, l = sum_j exp(s_j - m),
 // acc = sum_j exp(s_j - m) v_j over the segment's keys, s_j = scale * q.k_j.
 // Unsplit, it writes out = acc / l and lse = m + ln l directly.
+// The visible keys are [kv_begin, seq_len): kv_begin = seq_len - window with
+// a sliding window ("attention_impl.py", window_size = (window - 1, 0)),
+// else 0.  A sink logit (the USE_SINKS rule of the same Triton page) joins
+// the denominator of segment 0 only, as one term with no value.
 //
 // Swap-AB form: with one token the GQA group has only qpk <= 8 rows, so the
 // keys take the MMA's M dimension and the heads its N dimension:
@@ -25,6 +29,7 @@
 // Grid: num_splits * num_seqs * num_kv_heads CTAs, segment-major (then
 // sequence, then kv head).
 #include "attn_common.cuh"
+#include "launch.h"
 
 namespace paq8 {
 
@@ -110,17 +115,24 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
     return;
   }
   const int seq_len = a.seq_lens[seq];
-  if (seq_len < 1) {
+  if (seq_len < (a.causal ? 1 : 0)) {
     if (threadIdx.x == 0 && sigma == 0) flag_status(a.status, PA_DEV_BAD_SEQ);
+    return;
+  }
+  if (seq_len == 0) {  // non-causal, no key: out = 0, lse = sink or -inf
+    if (sigma == 0 && threadIdx.x < 32)
+      write_empty_rows<D>(a, q_start, h * a.qpk, a.qpk, threadIdx.x);
     return;
   }
   const bool split = a.num_splits > 1;
   const int kv_end = seq_len;
+  const int kv_begin = first_key(a, seq_len - 1);
+  const int first_tile = kv_begin / kTile;
   const int num_tiles = (kv_end + kTile - 1) / kTile;
-  int tile_lo = 0, tile_hi = num_tiles;
+  int tile_lo = first_tile, tile_hi = num_tiles;
   if (split) {
-    if (static_cast<int64_t>(sigma) * a.seg_tiles * kTile >= seq_len) return;
-    tile_lo = sigma * a.seg_tiles;
+    if (sigma >= segments_of(kv_begin, kv_end, kTile, a.seg_tiles, a.num_splits)) return;
+    tile_lo = first_tile + sigma * a.seg_tiles;
     tile_hi = sigma == a.num_splits - 1 ? num_tiles : min(num_tiles, tile_lo + a.seg_tiles);
   }
   const int n_iter = tile_hi - tile_lo;
@@ -141,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    produce_tiles_lsu<L, BS, kStages>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter,
-                                      kv_end, lane);
+    // test hook: stage nothing, so that every consumer wait runs out
+    if (!a.test_timeout)
+      produce_tiles_lsu<L, BS, kStages>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo,
+                                        n_iter, kv_begin, kv_end, lane);
     return;
   }
 
@@ -157,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
     const uint16_t *src =
         a.q + (static_cast<int64_t>(q_start) * a.hq + h * a.qpk + (hv ? g : 0)) * D + t * 8;
 #pragma unroll
+    bool bad_q = false;
     for (int gq = 0; gq < G; ++gq) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (hv) v = *reinterpret_cast<const uint4 *>(src + gq * 32);
@@ -164,7 +179,12 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
       qb[gq][0][1] = pack_half2(bf16_lo(v.y), bf16_hi(v.y));
       qb[gq][1][0] = pack_half2(bf16_lo(v.z), bf16_hi(v.z));
       qb[gq][1][1] = pack_half2(bf16_lo(v.w), bf16_hi(v.w));
+      bad_q |= half2_nonfinite(qb[gq][0][0]) || half2_nonfinite(qb[gq][0][1]) ||
+               half2_nonfinite(qb[gq][1][0]) || half2_nonfinite(qb[gq][1][1]);
     }
+    // q values beyond the fp16 range (|q| >= 65520) would give inf scores
+    if (__any_sync(0xffffffffu, bad_q) && warp == 0 && lane == 0 && sigma == 0)
+      flag_status(a.status, PA_DEV_BAD_Q);
   }
   const int r0 = perm16(g);      // key (within a 16-key block) of score row g
   const int r1 = perm16(g + 8);  // ... of score row g + 8
@@ -185,13 +205,14 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
   bool timed_out = false;
   for (int it = kg; it < n_iter; it += kKg) {
     const int stage = it % kStages;
-    if (!mbar_wait(bar_full + 8 * stage, (it / kStages) & 1)) {
+    if (!mbar_wait(bar_full + 8 * stage, (it / kStages) & 1, a.wait_limit_ns)) {
       timed_out = true;
       break;
     }
     const uint32_t st = smem_base + stage * L::kBytes;
     const int key0 = (tile_lo + it) * kTile + my_mt * 16;  // first key of this warp's block
-    const bool tail = key0 + 16 > kv_end;
+    // keys outside [kv_begin, kv_end) in this block: masked, V scales zeroed
+    const bool tail = key0 + 16 > kv_end || key0 < kv_begin;
 
     // ---------------- S^T = K Q^T with exact codes, scaled per group
     float s[4];
@@ -226,7 +247,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float v = s[e] * a.scale_log2;
-      if (tail && key0 + (e < 2 ? r0 : r1) >= kv_end) v = -INFINITY;
+      if (tail) {
+        const int key = key0 + (e < 2 ? r0 : r1);
+        if (key >= kv_end || key < kv_begin) v = -INFINITY;
+      }
       s[e] = v;
       mx[e & 1] = fmaxf(mx[e & 1], v);
     }
@@ -266,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
     // ---------------- O^T += V'^T P^T, V' = code * scale in fp16
 #pragma unroll
     for (int gv = 0; gv < G; ++gv) {
-      const uint2 vsc = v_scales4<L>(st, my_mt * 16 + 4 * t, gv, tail, key0 - my_mt * 16, kv_end);
+      const uint2 vsc =
+          v_scales4<L>(st, my_mt * 16 + 4 * t, gv, tail, key0 - my_mt * 16, kv_begin, kv_end);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cm = gv * 2 + half;
@@ -330,6 +355,25 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
         o[i][e] = o[i][e] * wa[e & 1] + src[(4 + i * 4 + e) * 32] * wb[e & 1];
   }
 
+  // ---------------- the sink joins segment 0 as one term (m = sink, l = 1, no value)
+  if (a.sinks && sigma == 0) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int hh = min(2 * t + c, a.qpk - 1);
+      const float sk = sink_log2(a, h * a.qpk + hh);
+      const float mn = fmaxf(m_run[c], sk);
+      if (mn == -INFINITY) continue;
+      const float wa = fast_exp2(m_run[c] - mn);
+      l_run[c] = l_run[c] * wa + fast_exp2(sk - mn);
+      m_run[c] = mn;
+#pragma unroll
+      for (int i = 0; i < Cfg::kCm; ++i) {
+        o[i][c] *= wa;
+        o[i][2 + c] *= wa;
+      }
+    }
+  }
+
   // ---------------- write: lane (g, t) holds channels cm*16 + g (+8) of heads 2t, 2t+1
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
@@ -365,15 +409,12 @@ cudaError_t launch_decode_t(const AttnArgs &a, const CUtensorMap &tk, const CUte
                             cudaStream_t stream) {
   using L = StageLayout<D, BS, DecodeCfg<D>::kTile>;
   constexpr int kSmem = DecodeCfg<D>::kSt * L::kBytes + 2 * DecodeCfg<D>::kSt * 8 + 1024;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  static DeviceOnce configured;
+  cudaError_t e = configured.get(nullptr, [](int, int *) {
+    return cudaFuncSetAttribute(decode_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmem);
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.num_seqs) * a.num_splits * a.hk, 1);
   decode_kernel<D, BS><<<grid, kThreads, kSmem, stream>>>(a, tk, tv);
   return cudaGetLastError();

@@ -4,7 +4,10 @@
 // m / qpk, q head kv * qpk + m % qpk.  For query token i of a sequence
 //   out = softmax_j(scale * q . k_j) v_j over keys j <= seq_len - q_len + i,
 //   lse = ln sum_j exp(scale * q . k_j),
-// with the dequantized q8 rows of the kv head read page by page.
+// with the dequantized q8 rows of the kv head read page by page.  In
+// non-causal mode every query sees keys j < seq_len; a sliding window keeps
+// the last `window` of a query's keys; a sink logit joins the denominator
+// (the options of the AttnArgs visibility fields).
 //
 // CTA = one q-block x one kv head (x one segment for split single-token
 // rows), 5 warps: warp 4 stages each 64-key tile's pages through a 4-deep
@@ -15,6 +18,7 @@
 // scale in fp32; PV multiplies P (fp16) by V' = code * scale (fp16), read
 // from the channel-major V pages 4 keys per 32-bit load.
 #include "attn_common.cuh"
+#include "launch.h"
 
 namespace paq8 {
 
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   }
   const int seq_len = a.seq_lens[seq];
   const int ctx = seq_len - q_len;
-  if (ctx < 0) {
+  if (a.causal ? ctx < 0 : seq_len < 0) {
     if (threadIdx.x == 0 && sigma == 0 && tok0 == 0) flag_status(a.status, PA_DEV_BAD_SEQ);
     return;
   }
@@ -82,12 +86,21 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   if (!split && sigma > 0) return;
   const int n_tok = min(a.block_q, q_len - tok0);
   const int n_rows = n_tok * a.qpk;
-  const int kv_end = ctx + tok0 + n_tok;  // keys visible to the last row
+  // keys visible to some row of the block: [kv_begin, kv_end)
+  const int kv_end = last_key(a, seq_len, q_len, tok0 + n_tok - 1) + 1;
+  const int kv_begin = first_key(a, last_key(a, seq_len, q_len, tok0));
+  if (kv_end == 0) {  // non-causal, seq_len == 0: no row sees a key
+    if (sigma == 0 && warp < 4)
+      for (int idx = warp; idx < n_tok; idx += 4)
+        write_empty_rows<D>(a, q_start + tok0 + idx, h * a.qpk, a.qpk, lane);
+    return;
+  }
+  const int first_tile = kv_begin / kTile;
   const int num_tiles = (kv_end + kTile - 1) / kTile;
-  int tile_lo = 0, tile_hi = num_tiles;
+  int tile_lo = first_tile, tile_hi = num_tiles;
   if (split) {
-    if (static_cast<int64_t>(sigma) * a.seg_tiles * kTile >= seq_len) return;
-    tile_lo = sigma * a.seg_tiles;
+    if (sigma >= segments_of(kv_begin, kv_end, kTile, a.seg_tiles, a.num_splits)) return;
+    tile_lo = first_tile + sigma * a.seg_tiles;
     tile_hi = sigma == a.num_splits - 1 ? num_tiles : min(num_tiles, tile_lo + a.seg_tiles);
   }
   const int n_iter = tile_hi - tile_lo;
@@ -107,8 +120,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    produce_tiles_lsu<L, BS>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter, kv_end,
-                             lane);
+    produce_tiles_lsu<L, BS>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter, kv_begin,
+                             kv_end, lane);
     return;
   }
 
@@ -123,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   // Channel order inside a k-step: cols 2t, 2t+1 <- 32gq + 8t + 4s + {0,1},
   // cols 2t+8, 2t+9 <- 32gq + 8t + 4s + {2,3}; K rows use the same order.
   if (warp < R) {
+    bool bad_q = false;
 #pragma unroll
     for (int gq = 0; gq < G; ++gq) {
       uint32_t f[2][4];
@@ -141,26 +155,36 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
         f[0][2 + half] = pack_half2(bf16_lo(v.y), bf16_hi(v.y));
         f[1][half] = pack_half2(bf16_lo(v.z), bf16_hi(v.z));
         f[1][2 + half] = pack_half2(bf16_lo(v.w), bf16_hi(v.w));
+        bad_q |= half2_nonfinite(f[0][half]) || half2_nonfinite(f[0][2 + half]) ||
+                 half2_nonfinite(f[1][half]) || half2_nonfinite(f[1][2 + half]);
       }
 #pragma unroll
       for (int s = 0; s < 2; ++s)
         sts128(q_frag + (((warp * G + gq) * 2 + s) * 32 + lane) * 16,
                make_uint4(f[s][0], f[s][1], f[s][2], f[s][3]));
     }
+    // q values beyond the fp16 range (|q| >= 65520) would give inf scores
+    if (__any_sync(0xffffffffu, bad_q) && lane == 0 && sigma == 0)
+      flag_status(a.status, PA_DEV_BAD_Q);
   }
   named_barrier(1, kConsumerWarps * 32);
 
-  // causal limits (last visible key) of rows g and g + 8; padding rows copy
-  // the block's last row so their arithmetic stays finite
-  int lim[2];
+  // visible keys [lo, lim] of rows g and g + 8; padding rows copy the
+  // block's last row so their arithmetic stays finite
+  int lim[2], lo[2];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int idx = rg * 16 + g + 8 * half;
-    lim[half] = idx < n_rows ? ctx + tok0 + idx / a.qpk : kv_end - 1;
+    lim[half] = idx < n_rows ? last_key(a, seq_len, q_len, tok0 + idx / a.qpk) : kv_end - 1;
+    lo[half] = first_key(a, lim[half]);
   }
   int min_lim = min(lim[0], lim[1]);
+  int max_lo = max(lo[0], lo[1]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) min_lim = min(min_lim, __shfl_xor_sync(0xffffffffu, min_lim, o));
+  for (int o = 16; o > 0; o >>= 1) {
+    min_lim = min(min_lim, __shfl_xor_sync(0xffffffffu, min_lim, o));
+    max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, o));
+  }
 
   // key (within its 16-key block) of score column n of an even / odd n-tile
   const int kc0 = perm16(2 * t), kc1 = perm16(2 * t + 1);  // even n-tile, cols 2t, 2t+1
@@ -177,7 +201,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   bool timed_out = false;
   for (int it = kg; it < n_iter; it += KG) {
     const int stage = it % kStages;
-    if (!mbar_wait(bar_full + 8 * stage, (it / kStages) & 1)) {
+    if (!mbar_wait(bar_full + 8 * stage, (it / kStages) & 1, a.wait_limit_ns)) {
       timed_out = true;
       break;
     }
@@ -215,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     }
 
     // ---------------- mask, online softmax (log2 domain)
-    const bool need_mask = key0 + kTile - 1 > min_lim;
+    const bool need_mask = key0 + kTile - 1 > min_lim || key0 < max_lo;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
@@ -224,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
         float v = sc[nt][e] * a.scale_log2;
         if (need_mask) {
           const int key = key0 + (nt >> 1) * 16 + ((e & 1) ? kc1 : kc0) + ((nt & 1) ? 2 : 0);
-          if (key > lim[e >> 1]) v = -INFINITY;
+          if (key > lim[e >> 1] || key < lo[e >> 1]) v = -INFINITY;
         }
         sc[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
@@ -257,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     }
 
     // ---------------- O += P V', V' = code * scale in fp16 from channel-major pages
-    const bool tail = key0 + kTile > kv_end;
+    const bool tail = key0 + kTile > kv_end || key0 < kv_begin;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint32_t pa0 = pack_half2(sc[2 * kk][0], sc[2 * kk][1]);
@@ -266,7 +290,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
       const uint32_t pa3 = pack_half2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
       for (int gq = 0; gq < G; ++gq) {
-        const uint2 vsc = v_scales4<L>(st, kk * 16 + 4 * t, gq, tail, key0, kv_end);
+        const uint2 vsc = v_scales4<L>(st, kk * 16 + 4 * t, gq, tail, key0, kv_begin, kv_end);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const uint32_t w = lds32(st + L::v_off(gq * 32 + jj * 8 + g, kk * 16 + 4 * t));
@@ -328,6 +352,25 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     }
   }
 
+  // ---------------- the sink joins segment 0 as one term (m = sink, l = 1, no value)
+  if (a.sinks && sigma == 0) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int idx = min(rg * 16 + g + 8 * half, n_rows - 1);
+      const float sk = sink_log2(a, h * a.qpk + idx % a.qpk);
+      const float mn = fmaxf(m_run[half], sk);
+      if (mn == -INFINITY) continue;
+      const float wa = fast_exp2(m_run[half] - mn);
+      l_run[half] = l_run[half] * wa + fast_exp2(sk - mn);
+      m_run[half] = mn;
+#pragma unroll
+      for (int i = 0; i < 4 * G; ++i) {
+        o_acc[i][2 * half] *= wa;
+        o_acc[i][2 * half + 1] *= wa;
+      }
+    }
+  }
+
   // ---------------- write: final output, or this segment's partial triple
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
@@ -361,16 +404,12 @@ template <int D, int BS>
 static cudaError_t launch_prefill_t(const AttnArgs &args, const CUtensorMap &tk,
                                     const CUtensorMap &tv, dim3 grid, cudaStream_t stream) {
   using C = AttnCfg<D, BS>;
-  static int configured_device = -1;  // the attribute is per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  static DeviceOnce configured;  // the attribute is per device
+  cudaError_t e = configured.get(nullptr, [](int, int *) {
+    return cudaFuncSetAttribute(prefill_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   prefill_kernel<D, BS><<<grid, kThreads, C::kSmemBytes, stream>>>(args, tk, tv);
   return cudaGetLastError();
 }

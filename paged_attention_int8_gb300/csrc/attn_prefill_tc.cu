@@ -6,6 +6,11 @@
 //   out = softmax_j(scale * q . k_j) v_j over keys j <= seq_len - q_len + i,
 //   lse = ln sum_j exp(scale * q . k_j),
 // over the dequantized q8 pages, in 64-key tiles with an online softmax.
+// In non-causal mode every query sees keys j < seq_len (seq_len may be below
+// q_len); a sliding window keeps the last `window` keys of each query; a sink
+// logit starts each row's softmax as one term with no value (the options of
+// the AttnArgs visibility fields).  Tiles before the block's first visible
+// key are not visited.
 //
 // Exact scores with one accumulator: each dequantized key value
 // k = code * scale (exact in fp32, 7 x 11 significant bits) is split into two
@@ -51,6 +56,7 @@
 // rescale O as soon as S(j) is ready.
 #include "attn_common.cuh"
 #include "tcgen05.cuh"
+#include "launch.h"
 
 namespace paq8 {
 
@@ -124,14 +130,23 @@ __global__ void __launch_bounds__(512, 1)
   }
   const int seq_len = a.seq_lens[seq];
   const int ctx = seq_len - q_len;
-  if (ctx < 0) {
+  if (a.causal ? ctx < 0 : seq_len < 0) {
     if (threadIdx.x == 0 && tok0 == 0) flag_status(a.status, PA_DEV_BAD_SEQ);
     return;
   }
   const int n_tok = min(a.block_q, q_len - tok0);
   const int n_rows = n_tok * a.qpk;
-  const int kv_end = ctx + tok0 + n_tok;
-  const int nt = (kv_end + C::kTile - 1) / C::kTile;
+  // keys visible to some row of the block: [kv_begin, kv_end)
+  const int kv_end = last_key(a, seq_len, q_len, tok0 + n_tok - 1) + 1;
+  const int kv_begin = first_key(a, last_key(a, seq_len, q_len, tok0));
+  if (kv_end == 0) {  // non-causal, seq_len == 0: no row sees a key
+    for (int idx = warp; idx < n_tok; idx += C::kWarps)
+      write_empty_rows<D>(a, q_start + tok0 + idx, h * a.qpk, a.qpk, lane);
+    return;
+  }
+  // the block visits tiles t0 .. t0 + nt - 1; iteration j works on tile t0 + j
+  const int t0 = kv_begin / C::kTile;
+  const int nt = (kv_end + C::kTile - 1) / C::kTile - t0;
   // half 1 holds no valid row when the block is short: it is then skipped
   const int halves = n_rows > 128 ? 2 : 1;
 
@@ -171,7 +186,7 @@ __global__ void __launch_bounds__(512, 1)
       prefetch_tensormap(&tmap_v);
     }
     produce_tiles<L, BS, C::kSt>(a, &tmap_k, &tmap_v, smem_base, bar(kBarStFull),
-                                 bar(kBarStEmpty), seq, h, 0, nt, kv_end, lane);
+                                 bar(kBarStEmpty), seq, h, t0, nt, kv_begin, kv_end, lane);
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     // The whole warp runs this loop (uniform values, no divergence); the
@@ -242,14 +257,15 @@ __global__ void __launch_bounds__(512, 1)
       const int sb = j % C::kSt, b = j & 1;
       if (!mbar_wait(bar(kBarStFull + sb), (j / C::kSt) & 1)) { ok = false; break; }
       const uint32_t st = smem_base + sb * L::kBytes;
-      const int key0 = j * C::kTile;
-      const bool tail = key0 + C::kTile > kv_end;
+      const int key0 = (t0 + j) * C::kTile;
+      // keys outside [kv_begin, kv_end) may hold stale bytes: converted as zeros
+      const bool tail = key0 + C::kTile > kv_end || key0 < kv_begin;
       if (k_side) {
         if (j >= 2 && !mbar_wait(bar(kBarKEmpty + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
         const uint32_t kdst = smem_base + C::kKOff + b * C::kKSlot;
         const int r = t & 63;
         const int c0 = (t >> 6) * (D / 2);
-        const bool dead = tail && key0 + r >= kv_end;  // stale bytes: write zeros
+        const bool dead = tail && (key0 + r >= kv_end || key0 + r < kv_begin);
 #pragma unroll
         for (int c = c0; c < c0 + D / 2; c += 16) {
           const uint4 codes = lds128(st + L::k_off(r, c));
@@ -308,8 +324,9 @@ __global__ void __launch_bounds__(512, 1)
           if (tail) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              if (key0 + key + 2 * i >= kv_end) sc[i] &= 0xffff0000u;
-              if (key0 + key + 2 * i + 1 >= kv_end) sc[i] &= 0x0000ffffu;
+              const int k0 = key0 + key + 2 * i;
+              if (k0 >= kv_end || k0 < kv_begin) sc[i] &= 0xffff0000u;
+              if (k0 + 1 >= kv_end || k0 + 1 < kv_begin) sc[i] &= 0x0000ffffu;
             }
           }
 #pragma unroll
@@ -347,11 +364,14 @@ __global__ void __launch_bounds__(512, 1)
     const bool valid = row < n_rows;
     const int tq = valid ? row / a.qpk : 0;
     const int hh = h * a.qpk + (valid ? row % a.qpk : 0);
-    const int limit = valid ? ctx + tok0 + tq : kv_end - 1;
+    // visible keys of this row: [lo, limit]
+    const int limit = valid ? last_key(a, seq_len, q_len, tok0 + tq) : kv_end - 1;
+    const int lo = first_key(a, limit);
     const float sl2 = a.scale_log2;
     // q row -> fp16 pairs in this lane's q columns (the QK MMA's A operand)
     {
       const uint16_t *src = a.q + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
+      bool bad_q = false;
 #pragma unroll 1
       for (int cb = 0; cb < D / 64; ++cb) {
         uint32_t qw[32];
@@ -363,9 +383,13 @@ __global__ void __launch_bounds__(512, 1)
           qw[4 * c16 + 1] = pack_half2(bf16_lo(v.y), bf16_hi(v.y));
           qw[4 * c16 + 2] = pack_half2(bf16_lo(v.z), bf16_hi(v.z));
           qw[4 * c16 + 3] = pack_half2(bf16_lo(v.w), bf16_hi(v.w));
+          bad_q |= half2_nonfinite(qw[4 * c16]) || half2_nonfinite(qw[4 * c16 + 1]) ||
+                   half2_nonfinite(qw[4 * c16 + 2]) || half2_nonfinite(qw[4 * c16 + 3]);
         }
         tc::st32(t_lane + C::kQCol + cb * 32, qw);
       }
+      // q values beyond the fp16 range (|q| >= 65520) would give inf scores
+      if (__any_sync(0xffffffffu, bad_q) && lane == 0) flag_status(a.status, PA_DEV_BAD_Q);
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
@@ -378,8 +402,8 @@ __global__ void __launch_bounds__(512, 1)
       for (int j = 0; j < nt; ++j) {
         if (!mbar_wait(bar(kBarSFull + hf), j & 1)) { ok = false; break; }
         tc::fence_after();
-        const int key0 = j * C::kTile;
-        const bool need_mask = key0 + C::kTile - 1 > limit;
+        const int key0 = (t0 + j) * C::kTile;
+        const bool need_mask = key0 + C::kTile - 1 > limit || key0 < lo;
         uint32_t sr[64];
         // S from TMEM; masked columns -> -inf, the rest pre-scaled (only on
         // tiles that cross this row's causal limit)
@@ -390,7 +414,8 @@ __global__ void __launch_bounds__(512, 1)
           if (need_mask) {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-              sr[c] = __float_as_uint(key0 + c > limit ? -INFINITY : __uint_as_float(sr[c]) * sl2);
+              sr[c] = __float_as_uint(key0 + c > limit || key0 + c < lo ? -INFINITY
+                                                                         : __uint_as_float(sr[c]) * sl2);
           }
         };
         load_s();
@@ -400,7 +425,10 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t pw[32];
         float ts;
         auto exp_tile = [&]() {
-          const uint64_t mul2 = f32x2_pack(mul, mul), neg_m2 = f32x2_pack(-m_used, -m_used);
+          // no visible key yet (m_used = -inf): every column of this tile is
+          // masked or the slow path below takes it, so any finite offset works
+          const float neg_m = m_used == -INFINITY ? 0.0f : -m_used;
+          const uint64_t mul2 = f32x2_pack(mul, mul), neg_m2 = f32x2_pack(neg_m, neg_m);
           uint64_t ls2[4] = {0, 0, 0, 0};  // +0.0f pairs
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
@@ -419,10 +447,10 @@ __global__ void __launch_bounds__(512, 1)
         };
         // The max the accumulator is scaled to moves only when this tile's
         // P would exceed C::kMaxTileSum (2^15, inside fp16): no row max is
-        // taken on the common path.  The first tile (m_used = -inf) gives an
-        // infinite or NaN sum and always takes the slow path.
+        // taken on the common path.  A row with no max yet (m_used = -inf)
+        // always takes the slow path, which sets it once a key is visible.
         exp_tile();
-        const bool grow = !(ts <= C::kMaxTileSum);
+        const bool grow = !(ts <= C::kMaxTileSum) || m_used == -INFINITY;
         if (__any_sync(0xffffffffu, grow)) {
           float f = 1.0f;  // factor for what O and l hold
           load_s();        // S is still in TMEM (P not yet written)
@@ -431,9 +459,11 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c) e[c & 3] = fmaxf(e[c & 3], __uint_as_float(sr[c]) * mul);
             const float m_new = fmaxf(m_used, fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])));
-            f = fast_exp2(m_used - m_new);  // 0 on the first tile
-            l *= f;
-            m_used = m_new;
+            if (m_new > -INFINITY) {  // else nothing visible yet: P stays 0
+              f = fast_exp2(m_used - m_new);  // 0 when the row had no max
+              l *= f;
+              m_used = m_new;
+            }
           }
           exp_tile();
           if (j > 0) {
@@ -461,7 +491,21 @@ __global__ void __launch_bounds__(512, 1)
       // ---- epilogue: O / l -> bf16, lse
       if (ok && mbar_wait(bar(kBarPvDone + hf), 0)) {
         tc::fence_after();
-        const float inv = 1.0f / l;
+        // a sink joins the denominator as one term with no value: the same
+        // sum as starting the softmax from (max = sink, sum = 1), taken here
+        // so that P stays scaled to the scores' own max (no fp16 underflow
+        // when the sink dominates)
+        float o_mul = 1.0f;
+        if (a.sinks) {
+          const float sk = sink_log2(a, hh);
+          const float mn = fmaxf(m_used, sk);
+          if (mn > -INFINITY) {
+            o_mul = fast_exp2(m_used - mn);
+            l = l * o_mul + fast_exp2(sk - mn);
+            m_used = mn;
+          }
+        }
+        const float inv = o_mul / l;
         uint16_t *dst = a.out + (static_cast<int64_t>(q_start + tok0 + tq) * a.hq + hh) * D;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -501,15 +545,12 @@ template <int D, int BS>
 static cudaError_t launch_prefill_tc_t(const AttnArgs &a, const CUtensorMap &tk,
                                        const CUtensorMap &tv, cudaStream_t stream) {
   using C = TcCfg<D, BS>;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, BS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  static DeviceOnce configured;
+  cudaError_t e = configured.get(nullptr, [](int, int *) {
+    return cudaFuncSetAttribute(prefill_tc_kernel<D, BS>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.n_qblocks), static_cast<unsigned>(a.hk), 1);
   prefill_tc_kernel<D, BS><<<grid, C::kWarps * 32, C::kSmem, stream>>>(a, tk, tv);
   return cudaGetLastError();

@@ -16,6 +16,8 @@ namespace paq8 {
 // A device-side wait gives up after this long and reports PA_DEV_TIMEOUT.
 // Normal waits last microseconds; the limit only bounds a broken pipeline.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// The shortened limit of the test hook that makes the waits run out.
+constexpr uint64_t kTestWaitLimitNs = 1000000ull;
 constexpr uint32_t kSuspendHintNs = 1000000u;  // 1 ms
 
 __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t bits) {
@@ -69,13 +71,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// limit_ns (kWaitLimitNs unless a caller shortens it).  Returns false on
+// timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -177,6 +181,12 @@ __device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
   return d;
 }
 
+// True when either fp16 half of w is infinite or NaN (a q value outside the
+// fp16 range after conversion).
+__device__ __forceinline__ bool half2_nonfinite(uint32_t w) {
+  return (w & 0x7c00u) == 0x7c00u || (w & 0x7c000000u) == 0x7c000000u;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -193,6 +203,11 @@ __device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi) {
 __device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {

@@ -23,20 +23,9 @@
 // issue: each channel-major V page takes one byte per (token, channel).
 #include "common.cuh"
 #include "launch.h"
+#include "q8_quant.cuh"
 
 namespace paq8 {
-
-// fp32 group scale from the group's max |x|: max(amax / 127, 1e-8).
-__device__ __forceinline__ float group_scale(float amax) {
-  const float s = __fdiv_rn(amax, 127.0f);
-  return s < 1e-8f ? 1e-8f : s;
-}
-
-// Exact q8 code of x for the group scale s: clamp(round_half_away(x / s)).
-__device__ __forceinline__ int32_t code_exact(float x, float s) {
-  const float r = fminf(fmaxf(roundf(__fdiv_rn(x, s)), -127.0f), 127.0f);
-  return static_cast<int32_t>(r);
-}
 
 // Four codes (each in [-127, 127]) -> one little-endian word.
 __device__ __forceinline__ uint32_t pack4(int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
@@ -99,16 +88,19 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
     int64_t value_stride, const int64_t *__restrict__ slot_mapping, int32_t num_tokens,
     int32_t hk, int8_t *__restrict__ k_cache, uint16_t *__restrict__ k_scale,
     int8_t *__restrict__ v_cache, uint16_t *__restrict__ v_scale, int64_t num_slots,
-    uint32_t *status) {
+    uint32_t *status, int32_t values_only, const int64_t *__restrict__ positions,
+    int32_t max_position) {
   constexpr int G = D / 32;
   constexpr int block_size = BS;
   extern __shared__ __align__(16) uint8_t store_smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int combo = blockIdx.y * kStoreWarps + warp;
-  if (combo >= 2 * hk * G) return;
-  const bool is_v = combo & 1;
-  const int h = (combo >> 1) / G, g = (combo >> 1) % G;
+  // (kv head, group) of K (even combos) or V (odd); values_only: V only
+  if (combo >= (values_only ? 1 : 2) * hk * G) return;
+  const bool is_v = values_only || (combo & 1);
+  const int hg = values_only ? combo : combo >> 1;
+  const int h = hg / G, g = hg % G;
   const uint16_t *src = (is_v ? value : key) + h * D + g * 32;
   const int64_t stride = is_v ? value_stride : key_stride;
   const int n_tblocks = (num_tokens + 31) / 32;
@@ -135,87 +127,158 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
     issue(tb + 2 * gridDim.x, (i + 2) % kStoreStages);
     cp_async_wait<2>();  // this lane's copies of `stage` have landed
     const int64_t n = static_cast<int64_t>(tb) * 32 + lane;
-    if (n >= num_tokens) continue;
     const uint32_t sbase = ring + stage * kStoreStageBytes;
-    int64_t slot;
-    asm volatile("ld.shared.s64 %0, [%1];" : "=l"(slot) : "r"(sbase + 32 * 64 + lane * 8));
-    if (slot < 0) continue;
+    // Every lane runs the whole body (the V stores below are warp-wide);
+    // lanes without a token, padding rows and bad slots store nothing.
+    int64_t slot = -1;
+    if (n < num_tokens)
+      asm volatile("ld.shared.s64 %0, [%1];" : "=l"(slot) : "r"(sbase + 32 * 64 + lane * 8));
     if (slot >= num_slots) {
-      if (combo == 0) flag_status(status, PA_DEV_BAD_SLOT);
-      continue;
+      if (combo == 0 && !values_only) flag_status(status, PA_DEV_BAD_SLOT);
+      slot = -1;
     }
-    float x[32];
-    uint32_t w[8];
-    load32(sbase, lane, x);
-    const int64_t blk = slot / block_size;
-    const int64_t off = slot % block_size;
-    const int64_t page = blk * hk + h;
+    // the fused store skips a token whose rotation position is outside the
+    // table (its keys are skipped and flagged by the key kernel)
+    if (positions && slot >= 0) {
+      const int64_t pos = positions[n];
+      if (pos < 0 || pos >= max_position) slot = -1;
+    }
+    const bool active = slot >= 0;
+
+    // ---- group scale from the group max
+    uint32_t xw[16];  // the lane's 32 bf16 values, two per word
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = lds128(sbase + row_chunk(lane, j));
+      xw[4 * j] = v.x;
+      xw[4 * j + 1] = v.y;
+      xw[4 * j + 2] = v.z;
+      xw[4 * j + 3] = v.w;
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(x[k]));
+    for (int k = 0; k < 16; ++k) amax = fmax3(amax, fabsf(bf16_lo(xw[k])), fabsf(bf16_hi(xw[k])));
     const float sc = group_scale(amax);
     const float rs = __frcp_rn(sc);
-    // Codes: q = x * rs rounded to the nearest integer (ties to even).  q
-    // and the IEEE quotient x / s differ by under 2.27e-5 (|q| <= 127.00002:
-    // two roundings of at most 2^-24 relative each in q, one in x / s), so
-    // where q lies 2^-15 or more from a rounding tie both round alike, and
-    // nearest-even there is also half away from zero; no clamp is needed.
-    // A value closer to a tie is redone: exactly from q when the scale is a
-    // power of two (then 1/s and x * rs are exact, and exact ties are common),
-    // otherwise from the IEEE quotient.  x is reloaded from the ring, whose
-    // stage is refilled two token blocks later.
-    constexpr float kFar = 0.5f - 0x1p-15f;  // |q - rint(q)| below this: not near a tie
-    bool far = true;  // every q of the group is far from a tie (false on NaN)
+
+    // ---- codes.  q = x * (1/s) is rounded to the nearest integer (ties to
+    // even) by adding 1.5 * 2^23, whose low byte is then the code.  q and the
+    // IEEE quotient x / s differ by under 2.27e-5 (|q| <= 127.00002: two
+    // roundings of at most 2^-24 relative each in q, one in x / s), so where
+    // q lies 2^-15 or more from a rounding tie both round alike, and nearest
+    // even there is also half away from zero; no clamp is needed.  Values
+    // closer to a tie are marked and decided exactly below.
+    constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+    constexpr float kFar = 0.5f - 0x1p-15f;
+    const uint64_t rs2 = f32x2_pack(rs, rs);
+    const uint64_t shift2 = f32x2_pack(kShift, kShift), unshift2 = f32x2_pack(-kShift, -kShift);
+    const uint64_t minus1 = f32x2_pack(-1.0f, -1.0f);
+    uint32_t w[8];
+    uint32_t near = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      int32_t c[4];
+      uint32_t tb2[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float q = x[4 * k + u] * rs;
-        const float r = rintf(q);
-        far = far && fabsf(q - r) < kFar;
-        c[u] = __float2int_rn(r);
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t xx = xw[2 * k + u];
+        const uint64_t q2 = f32x2_mul(f32x2_pack(bf16_lo(xx), bf16_hi(xx)), rs2);
+        const uint64_t t2 = f32x2_add(q2, shift2);
+        const uint64_t d2 = f32x2_fma(f32x2_add(t2, unshift2), minus1, q2);  // q - rint(q)
+        float t0, t1, d0, d1;
+        f32x2_unpack(t2, t0, t1);
+        f32x2_unpack(d2, d0, d1);
+        tb2[2 * u] = __float_as_uint(t0);
+        tb2[2 * u + 1] = __float_as_uint(t1);
+        near |= (fabsf(d0) >= kFar ? 1u : 0u) << (4 * k + 2 * u);
+        near |= (fabsf(d1) >= kFar ? 1u : 0u) << (4 * k + 2 * u + 1);
       }
-      w[k] = pack4(c[0], c[1], c[2], c[3]);
+      w[k] = __byte_perm(__byte_perm(tb2[0], tb2[1], 0x0040), __byte_perm(tb2[2], tb2[3], 0x0040),
+                         0x5410);
     }
-    if (!far) {
-      const bool pow2 = (__float_as_uint(sc) & 0x7fffffu) == 0u && sc < INFINITY;
-      load32(sbase, lane, x);
+    // Values within 2^-15 of a tie (with bf16 inputs, e.g. every x = max/2
+    // exactly) take the code of the IEEE quotient, decided without a divide.
+    if (!active) near = 0;
+    while (near) {
+      const int k = __ffs(near) - 1;
+      near &= near - 1;
+      const float x = __uint_as_float(
+          static_cast<uint32_t>(lds16(sbase + row_chunk(lane, k >> 3) + (k & 7) * 2)) << 16);
+      const uint32_t c = static_cast<uint32_t>(tie_code(x, sc, rs)) & 0xffu;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        int32_t c[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float q = x[4 * k + u] * rs;
-          const float r = rintf(q);
-          if (fabsf(q - r) < kFar)
-            c[u] = __float2int_rn(r);
-          else if (pow2 && fabsf(q) < INFINITY)
-            c[u] = static_cast<int32_t>(roundf(q));
-          else
-            c[u] = code_exact(x[4 * k + u], sc);
-        }
-        w[k] = pack4(c[0], c[1], c[2], c[3]);
-      }
+      for (int j = 0; j < 8; ++j)
+        if (j == (k >> 2)) w[j] = (w[j] & ~(0xffu << (8 * (k & 3)))) | (c << (8 * (k & 3)));
     }
     const uint16_t sbits = __half_as_ushort(__float2half_rn(sc));
+    const int64_t blk = active ? slot / block_size : 0;
+    const int64_t off = active ? slot % block_size : 0;
+    const int64_t page = blk * hk + h;
     if (!is_v) {
       // K: token-major page row, 32 codes of group g; scale [page][bs][G]
-      const int64_t row = page * block_size + off;
-      uint4 *kdst = reinterpret_cast<uint4 *>(k_cache + row * D + g * 32);
-      kdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      kdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      k_scale[row * G + g] = sbits;
+      if (active) {
+        const int64_t row = page * block_size + off;
+        uint4 *kdst = reinterpret_cast<uint4 *>(k_cache + row * D + g * 32);
+        kdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        kdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        k_scale[row * G + g] = sbits;
+      }
     } else {
-      // V: channel-major page, channel c of this token at (page * D + c) * bs + off;
+      // V: channel-major pages, channel c of this token at (page * D + c) * bs + off;
       // scale [page][G][bs]
-      int8_t *vdst = v_cache + (page * D + g * 32) * block_size + off;
+      if (active) v_scale[(page * G + g) * block_size + off] = sbits;
+      // A run of lanes that fills one whole page in slot order (BS lanes with
+      // offsets 0 .. BS-1 of one page: prefill chunks, cache population) is
+      // written as 16-byte rows: the codes are transposed through shared
+      // memory (the stage, no longer needed) so that lane c gathers channel
+      // c's bytes of the run.  Other lanes store their 32 bytes one by one.
+      constexpr int kRun = BS;  // lanes per page
+      const int64_t base = slot - (lane % kRun);
+      const int64_t lead = __shfl_sync(0xffffffffu, base, lane & ~(kRun - 1));
+      const bool fits = active && off == lane % kRun && base == lead;
+      const uint32_t ball = __ballot_sync(0xffffffffu, fits);
+      const uint32_t run_mask = kRun == 32 ? 0xffffffffu : (0xffffu << (lane & 16));
+      const bool whole = (ball & run_mask) == run_mask;
+      if (ball == 0xffffffffu || (kRun == 16 && (ball & 0xffffu) == 0xffffu) ||
+          (kRun == 16 && (ball >> 16) == 0xffffu)) {
+        // T[k][lane]: word k (codes of channels 4k .. 4k+3) of token `lane`;
+        // a row stride of 36 words keeps the gathers below free of conflicts
+        __syncwarp();
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
-        vdst[static_cast<int64_t>(k) * block_size] =
-            static_cast<int8_t>((w[k >> 2] >> (8 * (k & 3))) & 0xffu);
-      v_scale[(page * G + g) * block_size + off] = sbits;
+        for (int k = 0; k < 8; ++k)
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(sbase + (k * 36 + lane) * 4), "r"(w[k])
+                       : "memory");
+        __syncwarp();
+        const int c = lane;  // channel within the group
+        const uint32_t sel = (c & 3) | (((c & 3) + 4) << 4);
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {  // BS 16: page half p; BS 32: bytes 16p .. 16p+15
+          const uint32_t rbase = sbase + ((c >> 2) * 36 + 16 * p) * 4;
+          const uint4 a0 = lds128(rbase), a1 = lds128(rbase + 16);
+          const uint4 a2 = lds128(rbase + 32), a3 = lds128(rbase + 48);
+          uint4 o;
+          o.x = __byte_perm(__byte_perm(a0.x, a0.y, sel), __byte_perm(a0.z, a0.w, sel), 0x5410);
+          o.y = __byte_perm(__byte_perm(a1.x, a1.y, sel), __byte_perm(a1.z, a1.w, sel), 0x5410);
+          o.z = __byte_perm(__byte_perm(a2.x, a2.y, sel), __byte_perm(a2.z, a2.w, sel), 0x5410);
+          o.w = __byte_perm(__byte_perm(a3.x, a3.y, sel), __byte_perm(a3.z, a3.w, sel), 0x5410);
+          // the run holding tokens 16p .. 16p+15
+          const int src_lane = kRun == 16 ? 16 * p : 0;
+          const uint32_t run_ok = kRun == 16 ? (ball >> (16 * p)) & 0xffffu : ball;
+          const int64_t run_page = __shfl_sync(0xffffffffu, page, src_lane);
+          if (run_ok == (kRun == 16 ? 0xffffu : 0xffffffffu)) {
+            int8_t *dst = v_cache + (run_page * D + g * 32 + c) * block_size +
+                          (kRun == 16 ? 0 : 16 * p);
+            *reinterpret_cast<uint4 *>(dst) = o;
+          }
+        }
+      }
+      if (active && !whole) {
+        int8_t *vdst = v_cache + (page * D + g * 32) * block_size + off;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          vdst[static_cast<int64_t>(k) * block_size] =
+              static_cast<int8_t>((w[k >> 2] >> (8 * (k & 3))) & 0xffu);
+      }
     }
+    __syncwarp();  // the stage (and its transpose) is refilled next iteration
   }
   cp_async_wait<0>();
 }
@@ -223,24 +286,24 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
 // token-block slots of the grid
 template <int D, int BS>
 static cudaError_t store_grid_x(int n_tblocks, unsigned grid_y, unsigned *grid_x) {
-  static int cached_device = -1;
-  static unsigned resident = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (cached_device != dev) {
-    e = cudaFuncSetAttribute(kv_store_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStoreSmem);
-    if (e != cudaSuccess) return e;
+  // blocks of the kernel resident at once on the current device
+  static DeviceOnce resident_blocks;
+  int res = 0;
+  cudaError_t e = resident_blocks.get(&res, [](int dev, int *v) {
+    cudaError_t err = cudaFuncSetAttribute(
+        kv_store_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStoreSmem);
+    if (err != cudaSuccess) return err;
     int sms = 0, per_sm = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_store_kernel<D, BS>,
-                                                      32 * kStoreWarps, kStoreSmem);
-    if (e != cudaSuccess) return e;
-    resident = static_cast<unsigned>(sms > 0 ? sms : 1) * static_cast<unsigned>(per_sm > 0 ? per_sm : 1);
-    cached_device = dev;
-  }
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_store_kernel<D, BS>,
+                                                        32 * kStoreWarps, kStoreSmem);
+    if (err != cudaSuccess) return err;
+    *v = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
+  const unsigned resident = static_cast<unsigned>(res);
   // up to 16 waves: one block per token block (every block starts at once
   // with its own loads); beyond that, one resident set of blocks that walks
   // the token blocks with its loads two steps ahead
@@ -250,16 +313,18 @@ static cudaError_t store_grid_x(int n_tblocks, unsigned grid_y, unsigned *grid_x
   return cudaSuccess;
 }
 
-cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint16_t *value,
-                            int64_t value_stride, const int64_t *slot_mapping,
-                            int32_t num_tokens, int32_t hk, int32_t d, int8_t *k_cache,
-                            uint16_t *k_scale, int8_t *v_cache, uint16_t *v_scale,
-                            int32_t num_blocks, int32_t block_size, uint32_t *status,
-                            cudaStream_t stream) {
+static cudaError_t launch_store(const uint16_t *key, int64_t key_stride, const uint16_t *value,
+                                int64_t value_stride, const int64_t *slot_mapping,
+                                int32_t num_tokens, int32_t hk, int32_t d, int8_t *k_cache,
+                                uint16_t *k_scale, int8_t *v_cache, uint16_t *v_scale,
+                                int32_t num_blocks, int32_t block_size, uint32_t *status,
+                                int32_t values_only, const int64_t *positions,
+                                int32_t max_position, cudaStream_t stream) {
   const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
   const dim3 block(32 * kStoreWarps);
   const int n_tblocks = (num_tokens + 31) / 32;
-  const unsigned grid_y = static_cast<unsigned>((2 * hk * (d / 32) + kStoreWarps - 1) / kStoreWarps);
+  const int combos = (values_only ? 1 : 2) * hk * (d / 32);
+  const unsigned grid_y = static_cast<unsigned>((combos + kStoreWarps - 1) / kStoreWarps);
   unsigned grid_x = 0;
 #define PAQ8_STORE_CASE(DD, BB)                                                               \
   if (d == DD && block_size == BB) {                                                          \
@@ -267,7 +332,7 @@ cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint1
       return e;                                                                               \
     kv_store_kernel<DD, BB><<<dim3(grid_x, grid_y), block, kStoreSmem, stream>>>(              \
         key, key_stride, value, value_stride, slot_mapping, num_tokens, hk, k_cache, k_scale, \
-        v_cache, v_scale, num_slots, status);                                                 \
+        v_cache, v_scale, num_slots, status, values_only, positions, max_position);           \
     return cudaGetLastError();                                                                \
   }
   PAQ8_STORE_CASE(64, 16)
@@ -278,6 +343,31 @@ cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint1
   PAQ8_STORE_CASE(256, 32)
 #undef PAQ8_STORE_CASE
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint16_t *value,
+                            int64_t value_stride, const int64_t *slot_mapping,
+                            int32_t num_tokens, int32_t hk, int32_t d, int8_t *k_cache,
+                            uint16_t *k_scale, int8_t *v_cache, uint16_t *v_scale,
+                            int32_t num_blocks, int32_t block_size, uint32_t *status,
+                            cudaStream_t stream) {
+  return launch_store(key, key_stride, value, value_stride, slot_mapping, num_tokens, hk, d,
+                      k_cache, k_scale, v_cache, v_scale, num_blocks, block_size, status, 0,
+                      nullptr, 0, stream);
+}
+
+// The values of a store whose keys another kernel writes (the fused norm and
+// rotation store): the same kernel, value warps only; with `positions`, a
+// token whose position is outside [0, max_position) is skipped.
+cudaError_t launch_kv_store_values(const uint16_t *value, int64_t value_stride,
+                                   const int64_t *slot_mapping, int32_t num_tokens, int32_t hk,
+                                   int32_t d, int8_t *v_cache, uint16_t *v_scale,
+                                   int32_t num_blocks, int32_t block_size, uint32_t *status,
+                                   const int64_t *positions, int32_t max_position,
+                                   cudaStream_t stream) {
+  return launch_store(value, value_stride, value, value_stride, slot_mapping, num_tokens, hk, d,
+                      nullptr, nullptr, v_cache, v_scale, num_blocks, block_size, status, 1,
+                      positions, max_position, stream);
 }
 
 }  // namespace paq8

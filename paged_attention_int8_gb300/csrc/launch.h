@@ -4,7 +4,41 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace paq8 {
+
+constexpr int kMaxDevices = 64;
+
+// One-time set-up per device (a kernel's shared-memory attribute, an SM
+// count), safe when several host threads launch on several devices: init(dev,
+// &value) runs once for each device, with that device current, and later
+// calls return its value.
+class DeviceOnce {
+ public:
+  template <class F>
+  cudaError_t get(int *value, F &&init) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!done_[dev]) {
+      int v = 0;
+      e = init(dev, &v);
+      if (e != cudaSuccess) return e;
+      value_[dev] = v;
+      done_[dev] = true;
+    }
+    if (value) *value = value_[dev];
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+  int value_[kMaxDevices] = {};
+};
 
 cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint16_t *value,
                             int64_t value_stride, const int64_t *slot_mapping,
@@ -12,6 +46,26 @@ cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint1
                             uint16_t *k_scale, int8_t *v_cache, uint16_t *v_scale,
                             int32_t num_blocks, int32_t block_size, uint32_t *status,
                             cudaStream_t stream);
+
+// The fused store: keys normalized (norm_weight, or none) and rotated (rope,
+// or none), then stored with the values as launch_kv_store stores them.
+struct KvNormRope {
+  const uint16_t *key, *value;
+  int64_t key_stride, value_stride;
+  const int64_t *slot_mapping, *positions;
+  int32_t num_tokens, hk, d;
+  const uint16_t *norm_weight;
+  float eps;
+  const float *rope;  // [max_position][rotary_dim / 2][2] (cos, sin)
+  int32_t max_position, rotary_dim;
+  bool interleaved;
+  int8_t *k_cache, *v_cache;
+  uint16_t *k_scale, *v_scale;
+  int32_t num_blocks, block_size;
+  uint32_t *status;
+};
+
+cudaError_t launch_kv_store_norm_rope(const KvNormRope &p, cudaStream_t stream);
 
 int32_t auto_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_query_len,
                         int32_t max_seq_len);
@@ -26,6 +80,10 @@ struct AttnLaunch {
   float *lse;
   uint8_t *workspace;
   bool side_stream_ok = true;  // a mixed batch may run prefill on the side stream
+  bool causal = true;          // false: every query sees all seq_len keys
+  int32_t window = 0;          // sliding window in keys, 0 = none (causal only)
+  const float *sinks = nullptr;  // [hq] sink logits or null
+  bool test_timeout = false;   // test hook: decode waits run out after ~1 ms
 };
 
 cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream);

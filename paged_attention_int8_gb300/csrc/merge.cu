@@ -15,6 +15,7 @@
 // its threads before one of them writes the merged LSE (which may overwrite
 // lse_a or lse_b in place).
 #include "common.cuh"
+#include "launch.h"
 #include "merge.h"
 
 namespace paq8 {
@@ -69,16 +70,12 @@ __global__ void __launch_bounds__(256) merge_states_kernel(
 cudaError_t launch_merge_states(const uint16_t *out_a, const float *lse_a, const uint16_t *out_b,
                                 const float *lse_b, uint16_t *out, float *lse, int64_t num_rows,
                                 int32_t d, cudaStream_t stream) {
-  static int cached_device = -1;
-  static int sms = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static DeviceOnce sm_count;
+  int sms = 0;
+  cudaError_t e = sm_count.get(&sms, [](int dev, int *v) {
+    return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+  });
   if (e != cudaSuccess) return e;
-  if (cached_device != dev) {
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    cached_device = dev;
-  }
   const int64_t chunks = num_rows * (d / 8);
   const int64_t blocks_needed = (chunks + 255) / 256;
   // at most 8 blocks of 256 per SM resident at once; beyond that, grid-stride

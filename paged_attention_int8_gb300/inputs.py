@@ -41,6 +41,9 @@ class Spec:
     n_prefill: int = 0
     prefill_qlen: int = 0
     prefix_lens: tuple[int, int] = (0, 0)
+    # explicit prefix lengths of the prefill chunks (overrides n_prefill and
+    # the uniform draw)
+    fixed_prefix_lens: tuple[int, ...] = ()
     # key distribution: N(0,1) + per-(kv head, channel) bias of this std,
     # and a fraction of (kv head, channel) slots multiplied by outlier_mult
     k_bias_std: float = 0.0
@@ -143,7 +146,11 @@ def make_workload(spec: Spec) -> Workload:
 
     # --- lengths: prefill chunks first, then decodes
     q_lens, seq_lens = [], []
-    if spec.n_prefill:
+    if spec.fixed_prefix_lens:
+        for p in spec.fixed_prefix_lens:
+            q_lens.append(spec.prefill_qlen)
+            seq_lens.append(int(p) + spec.prefill_qlen)
+    elif spec.n_prefill:
         lo, hi = spec.prefix_lens
         prefixes = torch.randint(lo, hi + 1, (spec.n_prefill,), generator=gen)
         for p in prefixes.tolist():

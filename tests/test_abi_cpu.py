@@ -108,7 +108,9 @@ def _attn_args(**kw):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(flags=1), _lib.Status.INVALID_ARG),
+    (dict(flags=2), _lib.Status.INVALID_ARG),              # unknown flag bit
+    (dict(flags=_lib.ATTN_TEST_TIMEOUT, mq=4), _lib.Status.INVALID_ARG),  # decode path only
+    (dict(flags=_lib.ATTN_TEST_TIMEOUT, hq=32, hk=2), _lib.Status.INVALID_ARG),
     (dict(ws=None), _lib.Status.INVALID_ARG),
     (dict(q=None), _lib.Status.INVALID_ARG),
     (dict(hq=7), _lib.Status.INVALID_ARG),
@@ -128,6 +130,28 @@ def test_paged_attention_rejects_bad_arguments(lib, kw, expect):
 
 def test_paged_attention_empty_batch_is_a_no_op(lib):
     assert lib.pa_paged_attention(*_attn_args(S=0, T=0, q=None)) == _lib.Status.OK
+
+
+def _attn_ex_args(sinks=None, window=0, **kw):
+    a = _attn_args(**kw)
+    sk = ctypes.c_void_p(sinks) if sinks is not None else None
+    return a[:20] + [sk, window] + a[20:]
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(window=-1), _lib.Status.INVALID_ARG),
+    (dict(window=16, flags=_lib.ATTN_NON_CAUSAL), _lib.Status.INVALID_ARG),  # window is causal
+    (dict(sinks=18), _lib.Status.INVALID_ARG),                               # not 4-byte aligned
+    (dict(sinks=16, flags=4), _lib.Status.INVALID_ARG),
+    (dict(window=8, q=None), _lib.Status.INVALID_ARG),
+])
+def test_paged_attention_ex_rejects_bad_arguments(lib, kw, expect):
+    assert lib.pa_paged_attention_ex(*_attn_ex_args(**kw)) == expect
+    assert lib.pa_last_error().decode()
+
+
+def test_paged_attention_ex_empty_batch_is_a_no_op(lib):
+    assert lib.pa_paged_attention_ex(*_attn_ex_args(S=0, T=0, q=None, window=4)) == _lib.Status.OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
@@ -165,7 +189,7 @@ def test_merge_attn_states_zero_rows_is_a_no_op(lib):
 def test_bindings_mirror_the_boundary():
     # every compute entry point of the header has a binding of the same name
     import paged_attention_int8_gb300 as pkg
-    for name in ("kv_store", "paged_attention", "paged_attention_noalloc",
+    for name in ("kv_store", "kv_store_norm_rope", "paged_attention", "paged_attention_noalloc",
                  "merge_attn_states", "workspace_size", "auto_num_splits", "check_status"):
         assert name in pkg.__all__ and callable(getattr(pkg, name))
 
@@ -185,3 +209,37 @@ def test_bindings_refuse_host_tensors():
             fn(q, kc, ks, vc, vs, cu, sl, bt, 1, 9)
     with pytest.raises(ValueError):
         _lib.merge_attn_states(q, sl.float(), q, sl.float())
+
+
+def _fused_args(**kw):
+    a = dict(key=16, kstride=256, value=16, vstride=256, slots=16, pos=16, n=4, hk=2, d=128,
+             w=16, eps=1e-6, rope=16, maxpos=64, rot=128, inter=0, kc=16, ks=16, vc=16, vs=16,
+             nb=4, bs=16, status=None, stream=None)
+    a.update(kw)
+    v = lambda x: ctypes.c_void_p(x) if x is not None else None  # noqa: E731
+    return [v(a["key"]), a["kstride"], v(a["value"]), a["vstride"], v(a["slots"]), v(a["pos"]),
+            a["n"], a["hk"], a["d"], v(a["w"]), ctypes.c_float(a["eps"]), v(a["rope"]),
+            a["maxpos"], a["rot"], a["inter"], v(a["kc"]), v(a["ks"]), v(a["vc"]), v(a["vs"]),
+            a["nb"], a["bs"], v(a["status"]), v(a["stream"])]
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(key=None), _lib.Status.INVALID_ARG),
+    (dict(pos=None), _lib.Status.INVALID_ARG),        # a rotation needs positions
+    (dict(rot=130), _lib.Status.INVALID_ARG),         # past head_dim
+    (dict(rot=63), _lib.Status.INVALID_ARG),          # odd
+    (dict(rot=0), _lib.Status.INVALID_ARG),
+    (dict(rope=20), _lib.Status.INVALID_ARG),         # not 8-byte aligned
+    (dict(maxpos=0), _lib.Status.INVALID_ARG),
+    (dict(w=17), _lib.Status.INVALID_ARG),            # not 2-byte aligned
+    (dict(d=96), _lib.Status.UNSUPPORTED),
+    (dict(bs=8), _lib.Status.UNSUPPORTED),
+    (dict(vstride=100), _lib.Status.INVALID_ARG),
+])
+def test_kv_store_norm_rope_rejects_bad_arguments(lib, kw, expect):
+    assert lib.pa_kv_store_norm_rope(*_fused_args(**kw)) == expect
+    assert lib.pa_last_error().decode()
+
+
+def test_kv_store_norm_rope_zero_tokens_is_a_no_op(lib):
+    assert lib.pa_kv_store_norm_rope(*_fused_args(n=0, key=None)) == _lib.Status.OK

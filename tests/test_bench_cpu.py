@@ -69,3 +69,30 @@ def test_recorded_traffic_holds_only_for_the_same_attention_sources(tmp_path, mo
     attn = tmp_path / "paged_attention_int8_gb300" / "csrc" / "attn_decode.cu"
     attn.write_text(attn.read_text() + "\n// edit\n")
     assert bench.recorded_traffic("x") is None
+
+
+def test_roofline_reports_both_parts_for_a_mixed_batch():
+    spec = SPECS[2]
+    w = inputs.make_workload(spec)
+    work = bench.step_work(w)
+    roof = bench.roofline_of("cpu_mixed", spec, w, work, attn_ms=0.5, ns_eff=2,
+                             hbm_peak=6000.0, tc_peak=2000.0, peak_src="test")
+    parts = roof["parts"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    assert parts["bytes_ms"] == pytest.approx(work["attn_bytes"] / 6000e9 * 1e3, abs=2e-6)
+    assert parts["flops_ms"] == pytest.approx(work["flops"] / 2000e12 * 1e3, abs=2e-6)
+    assert parts["roofline_ms"] == max(parts["bytes_ms"], parts["flops_ms"])
+    assert roof["frac"] == pytest.approx(work["attn_bytes"] / 0.5e-3 / 6000e9, abs=1e-4)
+    prefill = bench.roofline_of("cpu_prefill", SPECS[1], inputs.make_workload(SPECS[1]),
+                                bench.step_work(inputs.make_workload(SPECS[1])), attn_ms=1.0,
+                                ns_eff=1, hbm_peak=6000.0, tc_peak=2000.0, peak_src="test")
+    assert prefill["bound"] == "tensor" and "parts" not in prefill
+
+
+def test_the_suite_holds_every_serving_workload_and_the_headline_is_the_largest():
+    assert set(bench.SUITE) == set(inputs.WORKLOADS) - {"tiny_decode"}
+    kv = {n: bench.step_work(inputs.make_workload(inputs.WORKLOADS[n].replace(
+        fixed_decode_lens=tuple(min(L, 4096) for L in inputs.WORKLOADS[n].fixed_decode_lens))))
+        ["kv_bytes"] for n in ("long_decode", "long_decode_d256")}
+    assert kv["long_decode_d256"] > kv["long_decode"]
+    assert bench.HEADLINE == "long_decode_d256"

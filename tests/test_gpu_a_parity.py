@@ -321,8 +321,8 @@ def test_attention_flags_bad_block_table_and_bad_lengths(cuda_device):
 
 
 def test_workspace_reused_across_calls(cuda_device):
-    # one workspace for calls of different shapes and split counts: the
-    # decode kernel's segment counters must be back at zero after each call
+    # one workspace for calls of different shapes and split counts: nothing a
+    # call leaves in it (split partials, a cleared status word) changes the next
     ws = torch.zeros(_lib.workspace_size(16, 32, 128, 16), dtype=torch.uint8, device=cuda_device)
     for name, ns in (("decode", 16), ("long_split", 4), ("decode", 2), ("long_split", 16)):
         w = inputs.make_workload(SMALL[name])

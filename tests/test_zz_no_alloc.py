@@ -6,8 +6,9 @@ wait on the allocator): the split-KV scratch lives in a static device array
 inside the library instead of a caller workspace.  This test calls it through
 the C ABI twice in a row -- the second call finds the first call's leftovers
 in the shared array -- and checks both results against the regular entry
-point, which uses a freshly allocated workspace, with the parity tolerances
-of the other GPU tests.  It lives in a file of its own, collected last.
+point, which uses a freshly allocated workspace, and against the CPU oracle,
+with the parity tolerances of the other GPU tests.  It lives in a file of its
+own, collected last.
 """
 import ctypes
 import math
@@ -54,6 +55,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls(num_splits, cuda_device):
     rows = H.owned_rows(w)
     ref_rows_out = ref_out.float().cpu().numpy().reshape(-1, w.spec.d)[rows].astype(np.float64)
     ref_rows_lse = ref_lse.cpu().numpy().reshape(-1)[rows].astype(np.float64)
+    oracle_out, oracle_lse = H.OracleState(w).attention(rows=rows)
     status = torch.full((1,), 7, dtype=torch.int32, device=cuda_device)
     for _ in range(2):
         out = torch.full_like(g.q, float("nan"))
@@ -63,6 +65,8 @@ def test_noalloc_matches_workspace_entry_on_two_calls(num_splits, cuda_device):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         H.compare(out, lse, ref_rows_out, ref_rows_lse, rows, label=f"noalloc splits={num_splits}")
+        H.compare(out, lse, oracle_out, oracle_lse, rows,
+                  label=f"noalloc vs oracle splits={num_splits}")
 
 
 def test_noalloc_rejects_splits_beyond_its_scratch(cuda_device):
