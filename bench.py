@@ -352,6 +352,56 @@ def merge_measure(r: Runner, reps: int = 20):
             "l2": "inputs larger than L2" if rows * (4 * d + 8) > L2_BYTES else "inputs fit in L2"}
 
 
+def f8v4_measure(w: inputs.Workload, device, reps: int = 20):
+    """The same decode batch stored in the fp8 / 4-bit format (e4m3 keys,
+    4-bit values with a per-key fp16 scale and zero) and attended by
+    paged_attention_f8v4: algorithmic bytes per call (D + D/2 + 4 per visible
+    (key, kv head), q, out, lse, block-table entries, metadata) per CUDA-event
+    time, and the time against the q8 call's."""
+    s = w.spec
+    kc, vc, vs, vz = inputs.empty_cache_f8v4(w.num_blocks, s.hk, s.bs, s.d, device=device,
+                                             canary=False)
+    k, v, sl = w.all_key_value()
+    chunk = 1 << 18
+    for a in range(0, k.shape[0], chunk):
+        _lib.kv_store_f8v4(k[a:a + chunk].to(device), v[a:a + chunk].to(device),
+                           sl[a:a + chunk].to(device), kc, vc, vs, vz)
+    q, cu = w.q.to(device), w.cu_seqlens_q.to(device)
+    seq_lens, bt = w.seq_lens.to(device), w.block_table.to(device)
+    ns = _lib.auto_num_splits(w.num_seqs, s.hk, w.max_query_len, w.max_seq_len)
+    ws = torch.zeros(_lib.workspace_size(w.num_seqs, s.hq, s.d, ns), dtype=torch.uint8,
+                     device=device)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.num_tokens, s.hq), dtype=torch.float32, device=device)
+
+    def call():
+        _lib.paged_attention_f8v4(q, kc, vc, vs, vz, cu, seq_lens, bt, 1, w.max_seq_len,
+                                  w.softmax_scale, num_splits=ns, out=out, lse=lse, workspace=ws)
+
+    for _ in range(3):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    assert _lib.check_status(ws) == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    L = w.seq_lens.to(torch.int64)
+    kv = int(L.sum()) * s.hk * (s.d + s.d // 2 + 4)
+    T = w.num_tokens
+    nbytes = kv + T * s.hq * s.d * 4 + T * s.hq * 4 + int(((L + s.bs - 1) // s.bs).sum()) * 4 \
+        + (2 * w.num_seqs + 1) * 4
+    hbm_peak, _, _ = load_peaks()
+    gbs = nbytes / (ms * 1e-3) * 1e-9
+    del kc, vc, vs, vz, ws
+    return {"format": "fp8 e4m3 keys, 4-bit values with fp16 scale and zero per key",
+            "bytes": nbytes, "ms": round(ms, 5), "achieved_gbs": round(gbs, 2),
+            "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "num_splits": ns}
+
+
 def e2e_measure(r: Runner, steps: int, warmup: int):
     """Same step through the public API with the step's inputs copied from
     pinned host memory and the outputs read back, all inside the timed region."""
@@ -584,6 +634,11 @@ def run_workload(name, args, device, rank, world, headline: bool):
             store["peak"] = hbm_peak
             store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
         entry["kv_store"] = store
+    if rank == 0 and name == "decode_batch" and not args.no_kv_store:
+        # the alternative format on the same batch: fewer bytes per key
+        f8 = f8v4_measure(w, device)
+        f8["vs_q8_call"] = round(f8["ms"] / attn_ms, 4)
+        entry["f8v4"] = f8
     if headline and rank == 0:
         if not args.no_kv_store:
             merge = merge_measure(r)

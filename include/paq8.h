@@ -253,6 +253,60 @@ pa_status pa_paged_attention_ex(const void *q, const void *k_cache, const void *
                                 size_t workspace_bytes, uint32_t flags, void *stream);
 
 /*
+ * The alternative cache format: fp8 keys and 4-bit values.
+ * Passage: "triton_turboquant_unified_attention.py", the FP8-key and 4-bit
+ * value load sites of the unified kernel (`_tq_load_k_tile`: an FP8 key is
+ * read as its e4m3 value, no scale; `_tq_load_v_tile`: V = idx * scale +
+ * zero with one fp16 scale and zero per token).  The page shows only the
+ * load sites; the store used here (a reading):
+ *     K     = e4m3(x), round to nearest even, saturating at +-448
+ *     lo, hi = min, max of the token's D values (fp32)
+ *     s     = max((hi - lo) / 15, 1e-8)                        (fp32)
+ *     idx   = clamp(round_half_away((x - lo) / s), 0, 15)      (fp32 divide)
+ *     scale = fp16(s), zero = fp16(lo)
+ * Caches (head-major pages; per (key, kv head) D + D/2 + 4 bytes instead of
+ * q8's 2 * (D + D/16)):
+ *     k_cache : uint8 [num_blocks][num_kv_heads][block_size][head_dim]   e4m3
+ *     v_cache : uint8 [num_blocks][num_kv_heads][head_dim][block_size/2] byte j
+ *               of a channel row: keys 2j (low nibble) and 2j + 1 (high)
+ *     v_scale, v_zero : fp16 [num_blocks][num_kv_heads][block_size]
+ * All base pointers 16-byte aligned.
+ */
+
+/*
+ * kv_store in the fp8 / 4-bit format.  Arguments as pa_kv_store.  Two tokens
+ * of one call whose slots share a nibble byte are both written; a token whose
+ * byte mate is not in the call keeps the mate's nibble (it updates its own
+ * with 32-bit atomics).  Asynchronous.
+ */
+pa_status pa_kv_store_f8v4(const void *key, int64_t key_token_stride,
+                           const void *value, int64_t value_token_stride,
+                           const int64_t *slot_mapping, int32_t num_tokens,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           void *k_cache, void *v_cache, void *v_scale, void *v_zero,
+                           int32_t num_blocks, int32_t block_size,
+                           uint32_t *status, void *stream);
+
+/*
+ * paged_attention over the fp8 / 4-bit format: as pa_paged_attention_ex
+ * (sinks, sliding window, flags), for decode rows (max_query_len == 1, at
+ * most 8 q heads per kv head; otherwise PA_ERR_UNSUPPORTED).  Numerics: K is
+ * exact in fp16 (every e4m3 value is an fp16 value), QK^T accumulates in
+ * fp32; V' = idx * scale + zero in one fp16 FMA; softmax and accumulation in
+ * fp32; output bf16.
+ */
+pa_status pa_paged_attention_f8v4(const void *q, const void *k_cache, const void *v_cache,
+                                  const void *v_scale, const void *v_zero,
+                                  const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                  const int32_t *block_table, int32_t block_table_stride,
+                                  int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                  int32_t block_size, int32_t max_query_len, int32_t max_seq_len,
+                                  float softmax_scale, int32_t num_splits, const float *sinks,
+                                  int32_t sliding_window, void *out, float *lse, void *workspace,
+                                  size_t workspace_bytes, uint32_t flags, void *stream);
+
+/*
  * merge_attn_states -- the attention of queries over the union of two
  * disjoint key sets, from their attention over each set (e.g. a cached
  * prefix attended in one pass and the new keys in another, or two calls'

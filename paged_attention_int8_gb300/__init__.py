@@ -13,7 +13,8 @@ fails loudly if it has not been built.
 """
 from __future__ import annotations
 
-__all__ = ["kv_store", "kv_store_norm_rope", "paged_attention", "paged_attention_noalloc", "merge_attn_states",
+__all__ = ["kv_store", "kv_store_norm_rope", "kv_store_f8v4", "paged_attention",
+           "paged_attention_f8v4", "paged_attention_noalloc", "merge_attn_states",
            "workspace_size", "check_status",
            "auto_num_splits", "Status", "PagedAttentionError", "library_path"]
 

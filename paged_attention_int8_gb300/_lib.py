@@ -69,6 +69,13 @@ def load():
                                               ctypes.c_float, P, i32, i32, i32, P, P, P, P, i32,
                                               i32, P, P]
         lib.pa_kv_store_norm_rope.restype = ctypes.c_int
+        lib.pa_kv_store_f8v4.argtypes = [P, i64, P, i64, P, i32, i32, i32, P, P, P, P, i32,
+                                         i32, P, P]
+        lib.pa_kv_store_f8v4.restype = ctypes.c_int
+        lib.pa_paged_attention_f8v4.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                i32, i32, i32, i32, i32, ctypes.c_float, i32, P,
+                                                i32, P, P, P, ctypes.c_size_t, ctypes.c_uint32, P]
+        lib.pa_paged_attention_f8v4.restype = ctypes.c_int
         lib.pa_auto_num_splits.argtypes = [i32, i32, i32, i32]
         lib.pa_auto_num_splits.restype = i32
         lib.pa_workspace_size.argtypes = [i32, i32, i32, i32]
@@ -232,6 +239,103 @@ def kv_store_norm_rope(key, value, slot_mapping, k_cache, k_scale, v_cache, v_sc
             1 if interleaved else 0, _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
             num_blocks, bs, _ptr(status), _stream(stream, device))
     _raise_if(st)
+
+
+def _check_f8v4_shapes(k_cache, v_cache, v_scale, v_zero):
+    """fp8 keys [nb, Hk, bs, D] uint8; 4-bit values [nb, Hk, D, bs / 2]
+    uint8; scale and zero [nb, Hk, bs] of 16-bit words (see include/paq8.h)."""
+    nb, hk, bs, d = k_cache.shape
+    want = ((nb, hk, d, bs // 2), (nb, hk, bs), (nb, hk, bs))
+    got = (tuple(v_cache.shape), tuple(v_scale.shape), tuple(v_zero.shape))
+    if got != want:
+        raise ValueError(f"cache shapes {got} != {want} (v_cache, v_scale, v_zero)")
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("fp8 / 4-bit caches: uint8 codes")
+    _check16("v_scale", v_scale)
+    _check16("v_zero", v_zero)
+    for t in (k_cache, v_cache, v_scale, v_zero):
+        if not t.is_contiguous():
+            raise ValueError("caches must be contiguous")
+
+
+def kv_store_f8v4(key, value, slot_mapping, k_cache, v_cache, v_scale, v_zero, status=None,
+                  stream=None) -> None:
+    """Store key/value rows [N, Hk, D] (bf16) in the fp8 / 4-bit format
+    (pa_kv_store_f8v4): keys as e4m3, values as 4-bit codes with one fp16
+    scale and zero per (token, kv head)."""
+    device = _check_cuda(key, value, slot_mapping, k_cache, v_cache, v_scale, v_zero, status)
+    if key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
+        raise TypeError("key and value must be bf16")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
+        raise TypeError("slot_mapping must be a contiguous int64 tensor")
+    n, hk, d = key.shape
+    if value.shape != key.shape or slot_mapping.shape != (n,):
+        raise ValueError("key/value/slot_mapping shapes differ")
+    for t in (key, value):
+        if t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError("key/value head and channel dims must be contiguous")
+    num_blocks, hk2, bs, d2 = k_cache.shape
+    if (hk2, d2) != (hk, d):
+        raise ValueError("cache shape mismatch")
+    _check_f8v4_shapes(k_cache, v_cache, v_scale, v_zero)
+    lib = load()
+    with torch.cuda.device(device):
+        st = lib.pa_kv_store_f8v4(_ptr(key), key.stride(0), _ptr(value), value.stride(0),
+                                  _ptr(slot_mapping), n, hk, d, _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(v_scale), _ptr(v_zero), num_blocks, bs, _ptr(status),
+                                  _stream(stream, device))
+    _raise_if(st)
+
+
+def paged_attention_f8v4(q, k_cache, v_cache, v_scale, v_zero, cu_seqlens_q, seq_lens,
+                         block_table, max_query_len: int, max_seq_len: int,
+                         softmax_scale: float | None = None, num_splits: int = 0, out=None,
+                         lse=None, workspace=None, stream=None, return_lse: bool = True,
+                         causal: bool = True, sinks=None, sliding_window: int = 0,
+                         flags: int = 0):
+    """paged_attention over the fp8 / 4-bit format (pa_paged_attention_f8v4):
+    decode rows only (max_query_len 1).  Other arguments as paged_attention."""
+    device = _check_cuda(q, k_cache, v_cache, v_scale, v_zero, cu_seqlens_q, seq_lens,
+                         block_table, out, lse, workspace, sinks)
+    _check_f8v4_shapes(k_cache, v_cache, v_scale, v_zero)
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise TypeError("q must be a contiguous bf16 tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens", seq_lens),
+                    ("block_table", block_table)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [S, max_blocks] with unit column stride")
+    T, hq, d = q.shape
+    num_blocks, hk, bs, d2 = k_cache.shape
+    if d2 != d:
+        raise ValueError("cache shape mismatch")
+    S = seq_lens.shape[0]
+    if cu_seqlens_q.shape != (S + 1,) or block_table.shape[0] != S:
+        raise ValueError("metadata shapes disagree with seq_lens")
+    if sinks is not None and (sinks.dtype != torch.float32 or sinks.shape != (hq,)):
+        raise TypeError("sinks must be an fp32 tensor [num_q_heads]")
+    if softmax_scale is None:
+        softmax_scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    lib = load()
+    need = int(lib.pa_workspace_size(S, hq, d, num_splits))
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    flags = int(flags) | (0 if causal else ATTN_NON_CAUSAL)
+    with torch.cuda.device(device):
+        st = lib.pa_paged_attention_f8v4(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(v_scale), _ptr(v_zero),
+            _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(block_table), block_table.stride(0), S, T,
+            hq, hk, d, num_blocks, bs, int(max_query_len), int(max_seq_len),
+            float(softmax_scale), int(num_splits), _ptr(sinks), int(sliding_window), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), flags,
+            _stream(stream, device))
+    _raise_if(st)
+    return (out, lse) if return_lse else out
 
 
 def auto_num_splits(num_seqs: int, num_kv_heads: int, max_query_len: int,

@@ -164,8 +164,11 @@ pa_status attention_args(const void *q, const void *k_cache, const void *k_scale
                          int32_t max_seq_len, float softmax_scale, int32_t num_splits,
                          const float *sinks, int32_t sliding_window, void *out, float *lse,
                          void *workspace, size_t workspace_bytes, uint32_t flags,
-                         paq8::AttnLaunch *L, bool *nothing_to_do) {
+                         paq8::AttnLaunch *L, bool *nothing_to_do,
+                         const void *v_zero = nullptr) {
   *nothing_to_do = false;
+  const bool f8v4 = v_zero != nullptr;
+  if (f8v4) k_scale = v_zero;  // the fp8 / 4-bit format has no key scales
   if (flags & ~(PA_ATTN_NON_CAUSAL | PA_ATTN_TEST_TIMEOUT))
     return fail(PA_ERR_INVALID_ARG, "unknown flag bits");
   const bool causal = !(flags & PA_ATTN_NON_CAUSAL);
@@ -200,6 +203,10 @@ pa_status attention_args(const void *q, const void *k_cache, const void *k_scale
   if ((lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
       (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3u)))
     return fail(PA_ERR_INVALID_ARG, "lse and sinks must be 4-byte aligned");
+  if (f8v4 && (max_query_len != 1 || num_q_heads / num_kv_heads > 8))
+    return fail(PA_ERR_UNSUPPORTED,
+                "the fp8 / 4-bit format is read by the decode path: max_query_len 1, <= 8 q heads "
+                "per kv head");
   if ((flags & PA_ATTN_TEST_TIMEOUT) &&
       (max_query_len != 1 || num_q_heads / num_kv_heads > 8))
     return fail(PA_ERR_INVALID_ARG,
@@ -245,6 +252,8 @@ pa_status attention_args(const void *q, const void *k_cache, const void *k_scale
   a.window = sliding_window;
   a.sinks = sinks;
   a.test_timeout = (flags & PA_ATTN_TEST_TIMEOUT) != 0;
+  a.f8v4 = f8v4;
+  a.v_zero = v_zero;
   return PA_OK;
 }
 
@@ -272,6 +281,65 @@ pa_status pa_paged_attention_ex(const void *q, const void *k_cache, const void *
       out, lse, workspace, workspace_bytes, flags, &L, &nothing);
   if (st != PA_OK || nothing) return st;
   cudaError_t e = paq8::launch_paged_attention(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_paged_attention_f8v4(const void *q, const void *k_cache, const void *v_cache,
+                                  const void *v_scale, const void *v_zero,
+                                  const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                  const int32_t *block_table, int32_t block_table_stride,
+                                  int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                  int32_t block_size, int32_t max_query_len, int32_t max_seq_len,
+                                  float softmax_scale, int32_t num_splits, const float *sinks,
+                                  int32_t sliding_window, void *out, float *lse, void *workspace,
+                                  size_t workspace_bytes, uint32_t flags, void *stream) {
+  g_last_error[0] = '\0';
+  if (!v_zero) return fail(PA_ERR_INVALID_ARG, "null v_zero");
+  paq8::AttnLaunch L;
+  bool nothing = false;
+  pa_status st = attention_args(
+      q, k_cache, nullptr, v_cache, v_scale, cu_seqlens_q, seq_lens, block_table,
+      block_table_stride, num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, num_blocks,
+      block_size, max_query_len, max_seq_len, softmax_scale, num_splits, sinks, sliding_window,
+      out, lse, workspace, workspace_bytes, flags, &L, &nothing, v_zero);
+  if (st != PA_OK || nothing) return st;
+  cudaError_t e = paq8::launch_paged_attention(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_kv_store_f8v4(const void *key, int64_t key_token_stride, const void *value,
+                           int64_t value_token_stride, const int64_t *slot_mapping,
+                           int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                           void *k_cache, void *v_cache, void *v_scale, void *v_zero,
+                           int32_t num_blocks, int32_t block_size, uint32_t *status,
+                           void *stream) {
+  g_last_error[0] = '\0';
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !slot_mapping || !k_cache || !v_cache || !v_scale || !v_zero)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be positive");
+  if (!supported_dim(head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (!supported_bs(block_size)) return fail(PA_ERR_UNSUPPORTED, "block_size must be 16 or 32");
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row)
+    return fail(PA_ERR_INVALID_ARG, "token stride smaller than num_kv_heads * head_dim");
+  if (key_token_stride % 8 || value_token_stride % 8 || !aligned16(key) || !aligned16(value))
+    return fail(PA_ERR_INVALID_ARG, "key/value rows must be 16-byte aligned");
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(v_scale) || !aligned16(v_zero))
+    return fail(PA_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)
+    return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * head_dim >= (int64_t{1} << 31))
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * head_dim must be < 2^31");
+  cudaError_t e = paq8::launch_kv_store_f8v4(
+      static_cast<const uint16_t *>(key), key_token_stride, static_cast<const uint16_t *>(value),
+      value_token_stride, slot_mapping, num_tokens, num_kv_heads, head_dim,
+      static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache),
+      static_cast<uint16_t *>(v_scale), static_cast<uint16_t *>(v_zero), num_blocks, block_size,
+      status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

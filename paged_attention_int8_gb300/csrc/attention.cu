@@ -28,6 +28,7 @@ cudaError_t launch_prefill(const AttnArgs &a, const CUtensorMap &tk, const CUten
                            int d, int bs, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                               int d, int bs, cudaStream_t stream);
+cudaError_t launch_decode_f8v4(const AttnArgs &a, int d, int bs, cudaStream_t stream);
 bool prefill_tc_supported(int d);
 int prefill_tc_rows();
 int decode_tile(int d);
@@ -194,6 +195,7 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   a.v_cache = static_cast<const int8_t *>(L.v_cache);
   a.k_scale = static_cast<const uint16_t *>(L.k_scale);
   a.v_scale = static_cast<const uint16_t *>(L.v_scale);
+  a.v_zero = static_cast<const uint16_t *>(L.v_zero);
   a.out = static_cast<uint16_t *>(L.out);
   a.lse = L.lse;
   a.status = reinterpret_cast<uint32_t *>(L.workspace);
@@ -216,13 +218,16 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
 
   const bool use_decode = a.qpk <= 8;
   const bool use_prefill = !use_decode || L.max_query_len > 1;
+  if (L.f8v4 && use_prefill) return cudaErrorInvalidValue;  // rejected by the API first
   const int64_t pages = static_cast<int64_t>(L.num_blocks) * L.hk;
   CUtensorMap tk, tv;
   const int krow = L.d >= 128 ? 128 : L.d;
-  if (!encode_map(&tk, L.k_cache, pages * L.bs, L.d, krow, L.bs,
-                  krow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_map(&tv, L.v_cache, pages * L.d, L.bs, L.bs, L.d,
-                  L.bs == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE))
+  // the fp8 / 4-bit decode kernel copies its pages with cp.async only
+  if (!L.f8v4 &&
+      (!encode_map(&tk, L.k_cache, pages * L.bs, L.d, krow, L.bs,
+                   krow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
+       !encode_map(&tv, L.v_cache, pages * L.d, L.bs, L.bs, L.d,
+                   L.bs == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE)))
     return cudaErrorInvalidValue;
 
   // keys a single-token row sees at most: the hint, or the window plus the
@@ -263,6 +268,9 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     if ((e = launch_decode(a, tk, tv, L.d, L.bs, stream)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(stream, ss->join, 0)) != cudaSuccess) return e;
+  } else if (use_decode && L.f8v4) {
+    cudaError_t e = launch_decode_f8v4(a, L.d, L.bs, stream);
+    if (e != cudaSuccess) return e;
   } else if (use_decode) {
     cudaError_t e = launch_decode(a, tk, tv, L.d, L.bs, stream);
     if (e != cudaSuccess) return e;

@@ -21,7 +21,8 @@ struct AttnArgs {
   const int8_t *k_cache;        // [nb, Hk, bs, D] int8
   const int8_t *v_cache;        // [nb, Hk, D, bs] int8
   const uint16_t *k_scale;      // [nb, Hk, bs, G] fp16
-  const uint16_t *v_scale;      // [nb, Hk, G, bs] fp16
+  const uint16_t *v_scale;      // [nb, Hk, G, bs] fp16 (fp8/4-bit format: [nb, Hk, bs])
+  const uint16_t *v_zero;       // fp8/4-bit format only: [nb, Hk, bs] fp16
   uint16_t *out;                // [T, Hq, D] bf16
   float *lse;                   // [T, Hq] or null
   float *part_acc;              // [S, Hq, NS, D]

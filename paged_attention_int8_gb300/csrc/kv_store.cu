@@ -106,15 +106,22 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
   const int n_tblocks = (num_tokens + 31) / 32;
   const uint32_t ring = smem_u32(store_smem) + warp * (kStoreStages * kStoreStageBytes);
   // copies of token block tb into a stage (one commit group per call, empty
-  // past the end)
+  // past the end).  Each token's 64-byte slice is two 32-byte sectors; in
+  // copy j the lanes 2i and 2i+1 fetch the two halves of sector j / 2 of
+  // token 2i + (j & 1), so every request covers whole sectors.
   auto issue = [&](int tb, int stage) {
-    const int64_t n = static_cast<int64_t>(tb) * 32 + lane;
-    if (tb < n_tblocks && n < num_tokens) {
+    if (tb < n_tblocks) {
       const uint32_t dst = ring + stage * kStoreStageBytes;
-      const uint16_t *row = src + n * stride;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) cp_async_16(dst + row_chunk(lane, j), row + 8 * j);
-      cp_async_8(dst + 32 * 64 + lane * 8, slot_mapping + n);
+      for (int j = 0; j < 4; ++j) {
+        const int tl = (lane & ~1) | (j & 1);           // token (lane) served
+        const int chunk = 2 * (j >> 1) + (lane & 1);    // its 16-byte chunk
+        const int64_t n = static_cast<int64_t>(tb) * 32 + tl;
+        if (n < num_tokens)
+          cp_async_16(dst + row_chunk(tl, chunk), src + n * stride + 8 * chunk);
+      }
+      const int64_t n = static_cast<int64_t>(tb) * 32 + lane;
+      if (n < num_tokens) cp_async_8(dst + 32 * 64 + lane * 8, slot_mapping + n);
     }
     cp_async_commit();
   };
@@ -126,6 +133,7 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
     const int stage = i % kStoreStages;
     issue(tb + 2 * gridDim.x, (i + 2) % kStoreStages);
     cp_async_wait<2>();  // this lane's copies of `stage` have landed
+    __syncwarp();        // ... and those of its partner lane (half of its row)
     const int64_t n = static_cast<int64_t>(tb) * 32 + lane;
     const uint32_t sbase = ring + stage * kStoreStageBytes;
     // Every lane runs the whole body (the V stores below are warp-wide);
@@ -213,14 +221,33 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
     const int64_t off = active ? slot % block_size : 0;
     const int64_t page = blk * hk + h;
     if (!is_v) {
-      // K: token-major page row, 32 codes of group g; scale [page][bs][G]
-      if (active) {
-        const int64_t row = page * block_size + off;
-        uint4 *kdst = reinterpret_cast<uint4 *>(k_cache + row * D + g * 32);
-        kdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        kdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        k_scale[row * G + g] = sbits;
+      // K: token-major page row, 32 codes (one sector) of group g; scale
+      // [page][bs][G].  Lanes 2i and 2i+1 write the two halves of token
+      // 2i's sector in one store and of token 2i+1's in the next, so each
+      // store covers whole sectors: they swap the half the other one writes.
+      const int64_t row = page * block_size + off;
+      uint8_t *mine = reinterpret_cast<uint8_t *>(k_cache + row * D + g * 32);
+      const bool odd = lane & 1;
+      uint32_t send[4], recv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        send[k] = odd ? w[k] : w[4 + k];
+        recv[k] = __shfl_xor_sync(0xffffffffu, send[k], 1);
       }
+      uint8_t *other = reinterpret_cast<uint8_t *>(
+          __shfl_xor_sync(0xffffffffu, reinterpret_cast<uintptr_t>(mine), 1));
+      const bool other_active = __shfl_xor_sync(0xffffffffu, active ? 1 : 0, 1) != 0;
+      // store 1: the even lane's token (even lane: bytes 0-15, odd: 16-31)
+      if (odd ? other_active : active)
+        *reinterpret_cast<uint4 *>((odd ? other : mine) + (odd ? 16 : 0)) =
+            odd ? make_uint4(recv[0], recv[1], recv[2], recv[3])
+                : make_uint4(w[0], w[1], w[2], w[3]);
+      // store 2: the odd lane's token
+      if (odd ? active : other_active)
+        *reinterpret_cast<uint4 *>((odd ? mine : other) + (odd ? 16 : 0)) =
+            odd ? make_uint4(w[4], w[5], w[6], w[7])
+                : make_uint4(recv[0], recv[1], recv[2], recv[3]);
+      if (active) k_scale[row * G + g] = sbits;
     } else {
       // V: channel-major pages, channel c of this token at (page * D + c) * bs + off;
       // scale [page][G][bs]

@@ -1,0 +1,194 @@
+// kv_store for the alternative cache format of the TurboQuant unified kernel
+// ("triton_turboquant_unified_attention.py": FP8 keys read as their e4m3
+// values; 4-bit values read as idx * scale + zero with one fp16 scale and zero
+// per token).  The page shows only the load sites; the store is:
+//   K: e4m3 of each bf16 value, round to nearest even, saturating at +-448;
+//   V: per (token, kv head) lo = min, hi = max over the D channels (fp32),
+//      s = max((hi - lo) / 15, 1e-8), idx = clamp(round_half_away((x - lo) / s),
+//      0, 15) of the IEEE fp32 quotient, scale = fp16(s), zero = fp16(lo).
+// Caches (head-major pages):
+//   k_cache uint8 [num_blocks][hk][bs][D]       e4m3, token-major
+//   v_cache uint8 [num_blocks][hk][D][bs / 2]   channel-major nibbles: byte j
+//                                               of a channel row holds keys 2j
+//                                               (low nibble) and 2j + 1
+//   v_scale, v_zero fp16 [num_blocks][hk][bs]
+//
+// One warp per (32 consecutive tokens, kv head); lane = token.  Two tokens
+// whose slots share a nibble byte (offsets 2j, 2j + 1 of one page) and sit in
+// the same warp -- consecutive tokens of a prefill chunk -- are written
+// together by the even one; a token whose byte mate is not in the warp
+// updates its nibbles with 32-bit atomics (so a mate in another warp or from
+// an earlier call is never overwritten).
+#include "common.cuh"
+#include "launch.h"
+#include "q8_quant.cuh"
+
+namespace paq8 {
+
+constexpr int kF8v4Warps = 8;
+
+// two fp32 -> e4m3x2 (x0 in byte 0), round to nearest even, saturating
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float x0, float x1) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(x1), "f"(x0));
+  return d;
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
+    const uint16_t *__restrict__ key, int64_t key_stride, const uint16_t *__restrict__ value,
+    int64_t value_stride, const int64_t *__restrict__ slot_mapping, int32_t num_tokens,
+    int32_t hk, uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
+    uint16_t *__restrict__ v_scale, uint16_t *__restrict__ v_zero, int64_t num_slots,
+    int32_t block_size, uint32_t *status) {
+  constexpr int W = D / 8;  // nibble words of a row (8 channels each)
+  const int lane = threadIdx.x & 31;
+  const int n_tblocks = (num_tokens + 31) / 32;
+  const int64_t units = static_cast<int64_t>(n_tblocks) * hk;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kF8v4Warps;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kF8v4Warps + (threadIdx.x >> 5); u < units;
+       u += stride) {
+    const int h = static_cast<int>(u % hk);
+    const int64_t n = (u / hk) * 32 + lane;
+    int64_t slot = n < num_tokens ? slot_mapping[n] : -1;
+    if (slot >= num_slots) {
+      if (h == 0) flag_status(status, PA_DEV_BAD_SLOT);
+      slot = -1;
+    }
+    const bool active = slot >= 0;
+    const int64_t blk = active ? slot / block_size : 0, off = active ? slot % block_size : 0;
+    const int64_t page = blk * hk + h;
+
+    // ---- keys: e4m3 of each value, one 16-byte store per 16 channels
+    if (active) {
+      const uint16_t *ks = key + n * key_stride + static_cast<int64_t>(h) * D;
+      uint8_t *kd = k_cache + (page * block_size + off) * D;
+#pragma unroll 4
+      for (int c = 0; c < D; c += 16) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(ks + c);
+        const uint4 b = *reinterpret_cast<const uint4 *>(ks + c + 8);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * i]), bf16_hi(w[2 * i]));
+          const uint32_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * i + 1]), bf16_hi(w[2 * i + 1]));
+          o[i] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4 *>(kd + c) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+
+    // ---- values: 4-bit codes with the row's scale and zero
+    uint32_t nib[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) nib[i] = 0u;
+    if (active) {
+      const uint16_t *vs = value + n * value_stride + static_cast<int64_t>(h) * D;
+      float lo = INFINITY, hi = -INFINITY;
+#pragma unroll 4
+      for (int c = 0; c < D; c += 8) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(vs + c);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lo = fmin3(lo, bf16_lo(w[i]), bf16_hi(w[i]));
+          hi = fmax3(hi, bf16_lo(w[i]), bf16_hi(w[i]));
+        }
+      }
+      float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+      if (s < 1e-8f) s = 1e-8f;
+      const float rs = __frcp_rn(s);
+      constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+      constexpr float kFar = 0.5f - 0x1p-15f;
+#pragma unroll
+      for (int c = 0; c < D; c += 8) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(vs + c);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+        uint32_t word = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float x = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+          // (x - lo) / s as in kv_store: the product with 1/s, exact near ties
+          const float v = __fsub_rn(x, lo);
+          const float q = __fmul_rn(v, rs);
+          const float t = __fadd_rn(q, kShift);
+          int32_t code = static_cast<int32_t>(__float_as_uint(t) & 0xffu);
+          if (fabsf(__fsub_rn(q, __fsub_rn(t, kShift))) >= kFar) code = tie_code(v, s, rs);
+          code = min(max(code, 0), 15);
+          word |= static_cast<uint32_t>(code) << (4 * i);
+        }
+        nib[c / 8] = word;
+      }
+      v_scale[page * block_size + off] = __half_as_ushort(__float2half_rn(s));
+      v_zero[page * block_size + off] = __half_as_ushort(__float2half_rn(lo));
+    }
+
+    // ---- nibble bytes: pair the two tokens of a byte when both are here
+    const uint32_t pair_mask = __match_any_sync(0xffffffffu, active ? (slot >> 1) : -1 - lane);
+    const bool paired = __popc(pair_mask) == 2;
+    const int mate = paired ? __ffs(pair_mask & ~(1u << lane)) - 1 : lane;
+    uint32_t mate_nib[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) mate_nib[i] = __shfl_sync(0xffffffffu, nib[i], mate);
+    if (!active) continue;
+    uint8_t *vrow = v_cache + page * D * (block_size / 2) + off / 2;  // channel 0's byte
+    if (paired) {
+      if (off & 1) continue;  // the even-offset token writes the byte
+#pragma unroll 4
+      for (int c = 0; c < D; ++c) {
+        const uint32_t lo4 = (nib[c / 8] >> (4 * (c % 8))) & 0xfu;
+        const uint32_t hi4 = (mate_nib[c / 8] >> (4 * (c % 8))) & 0xfu;
+        vrow[static_cast<int64_t>(c) * (block_size / 2)] = static_cast<uint8_t>(lo4 | (hi4 << 4));
+      }
+    } else {
+#pragma unroll 4
+      for (int c = 0; c < D; ++c) {
+        const uint32_t v4 = (nib[c / 8] >> (4 * (c % 8))) & 0xfu;
+        uint8_t *byte = vrow + static_cast<int64_t>(c) * (block_size / 2);
+        unsigned int *word = reinterpret_cast<unsigned int *>(
+            reinterpret_cast<uintptr_t>(byte) & ~static_cast<uintptr_t>(3));
+        const uint32_t shift = 8u * static_cast<uint32_t>(reinterpret_cast<uintptr_t>(byte) & 3u) +
+                               4u * static_cast<uint32_t>(off & 1);
+        atomicAnd(word, ~(0xfu << shift));
+        atomicOr(word, v4 << shift);
+      }
+    }
+  }
+}
+
+cudaError_t launch_kv_store_f8v4(const uint16_t *key, int64_t key_stride, const uint16_t *value,
+                                 int64_t value_stride, const int64_t *slot_mapping,
+                                 int32_t num_tokens, int32_t hk, int32_t d, uint8_t *k_cache,
+                                 uint8_t *v_cache, uint16_t *v_scale, uint16_t *v_zero,
+                                 int32_t num_blocks, int32_t block_size, uint32_t *status,
+                                 cudaStream_t stream) {
+  static DeviceOnce sm_count;
+  int sms = 0;
+  cudaError_t e = sm_count.get(&sms, [](int dev, int *v) {
+    return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (e != cudaSuccess) return e;
+  const int64_t units = static_cast<int64_t>((num_tokens + 31) / 32) * hk;
+  const int64_t want = (units + kF8v4Warps - 1) / kF8v4Warps;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
+#define PAQ8_F8V4_STORE(DD)                                                                       \
+  case DD:                                                                                        \
+    kv_store_f8v4_kernel<DD><<<grid, 32 * kF8v4Warps, 0, stream>>>(                               \
+        key, key_stride, value, value_stride, slot_mapping, num_tokens, hk, k_cache, v_cache,     \
+        v_scale, v_zero, num_slots, block_size, status);                                          \
+    break;
+  switch (d) {
+    PAQ8_F8V4_STORE(64)
+    PAQ8_F8V4_STORE(128)
+    PAQ8_F8V4_STORE(256)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef PAQ8_F8V4_STORE
+  return cudaGetLastError();
+}
+
+}  // namespace paq8

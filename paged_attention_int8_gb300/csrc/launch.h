@@ -67,6 +67,13 @@ struct KvNormRope {
 
 cudaError_t launch_kv_store_norm_rope(const KvNormRope &p, cudaStream_t stream);
 
+cudaError_t launch_kv_store_f8v4(const uint16_t *key, int64_t key_stride, const uint16_t *value,
+                                 int64_t value_stride, const int64_t *slot_mapping,
+                                 int32_t num_tokens, int32_t hk, int32_t d, uint8_t *k_cache,
+                                 uint8_t *v_cache, uint16_t *v_scale, uint16_t *v_zero,
+                                 int32_t num_blocks, int32_t block_size, uint32_t *status,
+                                 cudaStream_t stream);
+
 int32_t auto_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_query_len,
                         int32_t max_seq_len);
 
@@ -84,6 +91,10 @@ struct AttnLaunch {
   int32_t window = 0;          // sliding window in keys, 0 = none (causal only)
   const float *sinks = nullptr;  // [hq] sink logits or null
   bool test_timeout = false;   // test hook: decode waits run out after ~1 ms
+  // cache format: false = q8; true = fp8 keys and 4-bit values (k_scale
+  // unused, v_scale / v_zero one fp16 per key), decode rows only
+  bool f8v4 = false;
+  const void *v_zero = nullptr;
 };
 
 cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream);

@@ -273,6 +273,30 @@ def empty_cache(num_blocks: int, hk: int, bs: int, d: int, device="cpu", canary:
             torch.full(vs, fill_s, dtype=torch.int16, device=device))
 
 
+def cache_shapes_f8v4(num_blocks: int, hk: int, bs: int, d: int):
+    """Shapes of (k_cache, v_cache, v_scale, v_zero) in the fp8 / 4-bit
+    format: e4m3 keys [num_blocks, Hk, bs, D] (token-major), 4-bit values
+    [num_blocks, Hk, D, bs / 2] (channel-major, two keys per byte), fp16
+    scale and zero [num_blocks, Hk, bs]."""
+    return ((num_blocks, hk, bs, d), (num_blocks, hk, d, bs // 2), (num_blocks, hk, bs),
+            (num_blocks, hk, bs))
+
+
+def empty_cache_f8v4(num_blocks: int, hk: int, bs: int, d: int, device="cpu",
+                     canary: bool = True):
+    """Cache tensors (k_cache, v_cache, v_scale, v_zero) of the fp8 / 4-bit
+    format, shapes as in ``cache_shapes_f8v4``; codes uint8, scale and zero as
+    int16 bit patterns of fp16.  With ``canary`` every byte is 0xFF (a NaN
+    e4m3 key, which the store never writes for finite inputs below 448)."""
+    kc, vc, vs, vz = cache_shapes_f8v4(num_blocks, hk, bs, d)
+    fill_c = 0xFF if canary else 0
+    fill_s = -1 if canary else 0
+    return (torch.full(kc, fill_c, dtype=torch.uint8, device=device),
+            torch.full(vc, fill_c, dtype=torch.uint8, device=device),
+            torch.full(vs, fill_s, dtype=torch.int16, device=device),
+            torch.full(vz, fill_s, dtype=torch.int16, device=device))
+
+
 def bf16_bits(t: torch.Tensor):
     """bf16 tensor -> numpy uint16 bit patterns (no arithmetic)."""
     return t.contiguous().view(torch.int16).numpy().view("uint16")

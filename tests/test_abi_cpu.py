@@ -189,7 +189,8 @@ def test_merge_attn_states_zero_rows_is_a_no_op(lib):
 def test_bindings_mirror_the_boundary():
     # every compute entry point of the header has a binding of the same name
     import paged_attention_int8_gb300 as pkg
-    for name in ("kv_store", "kv_store_norm_rope", "paged_attention", "paged_attention_noalloc",
+    for name in ("kv_store", "kv_store_norm_rope", "kv_store_f8v4", "paged_attention",
+                 "paged_attention_f8v4", "paged_attention_noalloc",
                  "merge_attn_states", "workspace_size", "auto_num_splits", "check_status"):
         assert name in pkg.__all__ and callable(getattr(pkg, name))
 
@@ -243,3 +244,26 @@ def test_kv_store_norm_rope_rejects_bad_arguments(lib, kw, expect):
 
 def test_kv_store_norm_rope_zero_tokens_is_a_no_op(lib):
     assert lib.pa_kv_store_norm_rope(*_fused_args(n=0, key=None)) == _lib.Status.OK
+
+
+def test_f8v4_entries_reject_bad_arguments(lib):
+    args = _attn_ex_args()
+    # pa_paged_attention_f8v4(q, k_cache, v_cache, v_scale, v_zero, ...): same tail as _ex
+    f8 = lambda **kw: [v for v in _attn_ex_args(**kw)]  # noqa: E731
+    base = f8()
+    call = base[:2] + [base[3], base[4], ctypes.c_void_p(16)] + base[5:]
+    assert len(call) == len(args)
+    # no v_zero
+    bad = base[:2] + [base[3], base[4], None] + base[5:]
+    assert lib.pa_paged_attention_f8v4(*bad) == _lib.Status.INVALID_ARG
+    # multi-token rows are not read in this format
+    multi = f8(mq=4)
+    call = multi[:2] + [multi[3], multi[4], ctypes.c_void_p(16)] + multi[5:]
+    assert lib.pa_paged_attention_f8v4(*call) == _lib.Status.UNSUPPORTED
+    # the store: a null zero array, an odd row stride
+    st = _store_args()
+    store = st[:8] + [st[8], st[10], st[11], ctypes.c_void_p(16)] + st[12:]
+    assert lib.pa_kv_store_f8v4(*(store[:11] + [None] + store[12:])) == _lib.Status.INVALID_ARG
+    odd = _store_args(kstride=260)
+    store = odd[:8] + [odd[8], odd[10], odd[11], ctypes.c_void_p(16)] + odd[12:]
+    assert lib.pa_kv_store_f8v4(*store) == _lib.Status.INVALID_ARG

@@ -1,0 +1,142 @@
+"""GPU parity of the alternative cache format -- fp8 (e4m3) keys and 4-bit
+values with one fp16 scale and zero per key -- against the CPU oracle: the
+store bit for bit (codes, nibbles, scales, zeros and placement, for tokens
+that share a nibble byte within one call and for tokens whose byte mate is
+already in the cache), then decode attention over that cache element by
+element, split and unsplit, with sinks and a sliding window."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_attention_int8_gb300 import _lib, inputs
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+
+SQRT2 = math.sqrt(2.0)
+
+SPECS = {
+    "decode": inputs.Spec("f8_decode", 501, hq=32, hk=8, d=128, bs=16, n_decode=6,
+                          decode_lens=(100, 900), k_bias_std=SQRT2),
+    "d256": inputs.Spec("f8_d256", 502, hq=16, hk=4, d=256, bs=32, n_decode=4,
+                        decode_lens=(40, 700), k_bias_std=SQRT2),
+    "d64": inputs.Spec("f8_d64", 503, hq=8, hk=2, d=64, bs=16, n_decode=5,
+                       decode_lens=(1, 300)),
+    "long": inputs.Spec("f8_long", 504, hq=32, hk=8, d=128, bs=32,
+                        fixed_decode_lens=(3000, 2111, 17), k_bias_std=SQRT2, num_splits=16),
+}
+
+
+class F8State:
+    """The workload stored in the fp8 / 4-bit format on the GPU (by the
+    library) and on the host (by the oracle), from the same generated rows."""
+
+    def __init__(self, w, device, batches=None):
+        s = w.spec
+        self.w, self.device = w, device
+        self.kc, self.vc, self.vs, self.vz = inputs.empty_cache_f8v4(w.num_blocks, s.hk, s.bs, s.d,
+                                                                     device=device)
+        okc, ovc, ovs, ovz = inputs.empty_cache_f8v4(w.num_blocks, s.hk, s.bs, s.d)
+        self.okc, self.ovc = okc.numpy(), ovc.numpy()
+        self.ovs, self.ovz = ovs.numpy().view(np.uint16), ovz.numpy().view(np.uint16)
+        status = torch.zeros(4, dtype=torch.int32, device=device)
+        if batches is None:
+            batches = [(w.prefix_key, w.prefix_value, w.prefix_slots),
+                       (w.new_key, w.new_value, w.new_slots)]
+        for k, v, sl in batches:
+            if k.shape[0] == 0:
+                continue
+            _lib.kv_store_f8v4(k.to(device), v.to(device), sl.to(device), self.kc, self.vc,
+                               self.vs, self.vz, status=status)
+            assert oracle.kv_store_f8v4(inputs.bf16_bits(k), inputs.bf16_bits(v), sl.numpy(),
+                                        self.okc, self.ovc, self.ovs, self.ovz) == 0
+        assert _lib.check_status(status) == 0
+        self.q = w.q.to(device)
+        self.cu = w.cu_seqlens_q.to(device)
+        self.seq_lens = w.seq_lens.to(device)
+        self.bt = w.block_table.to(device)
+
+    def assert_cache_equal(self):
+        np.testing.assert_array_equal(self.kc.cpu().numpy(), self.okc)
+        np.testing.assert_array_equal(self.vc.cpu().numpy(), self.ovc)
+        np.testing.assert_array_equal(self.vs.cpu().numpy().view(np.uint16), self.ovs)
+        np.testing.assert_array_equal(self.vz.cpu().numpy().view(np.uint16), self.ovz)
+
+    def gpu(self, num_splits=0, sinks=None, window=0):
+        w = self.w
+        ws = torch.zeros(_lib.workspace_size(w.num_seqs, w.spec.hq, w.spec.d, num_splits),
+                         dtype=torch.uint8, device=self.device)
+        out = torch.full_like(self.q, float("nan"))
+        lse = torch.full((w.num_tokens, w.spec.hq), float("nan"), device=self.device)
+        sk = None if sinks is None else torch.from_numpy(sinks).to(self.device)
+        _lib.paged_attention_f8v4(self.q, self.kc, self.vc, self.vs, self.vz, self.cu,
+                                  self.seq_lens, self.bt, 1, w.max_seq_len, w.softmax_scale,
+                                  num_splits=num_splits, out=out, lse=lse, workspace=ws,
+                                  sinks=sk, sliding_window=window)
+        assert _lib.check_status(ws) == 0
+        return out, lse
+
+    def oracle(self, rows, sinks=None, window=0):
+        w = self.w
+        return oracle.paged_attention(inputs.bf16_bits(w.q), self.okc, None, self.ovc, self.ovs,
+                                      w.cu_seqlens_q.numpy(), w.seq_lens.numpy(),
+                                      w.block_table.numpy(), w.softmax_scale, rows=rows,
+                                      sinks=sinks, window=window, v_zero=self.ovz)
+
+
+_cache = {}
+
+
+def _state(name, device):
+    if name not in _cache:
+        _cache[name] = F8State(inputs.make_workload(SPECS[name]), device)
+    return _cache[name]
+
+
+@pytest.mark.parametrize("name", sorted(SPECS))
+def test_f8v4_store_is_bit_exact(name, cuda_device):
+    _state(name, cuda_device).assert_cache_equal()
+
+
+def test_f8v4_store_keeps_byte_mates_from_earlier_calls(cuda_device):
+    # one token per call (decode steps): each token's nibble byte is shared
+    # with a token stored by an earlier call, and both must survive
+    spec = inputs.Spec("f8_steps", 505, hq=8, hk=2, d=64, bs=16, fixed_decode_lens=(40,))
+    w = inputs.make_workload(spec)
+    k, v, sl = w.all_key_value()
+    order = np.random.default_rng(0).permutation(k.shape[0])
+    batches = [(k[i:i + 1], v[i:i + 1], sl[i:i + 1]) for i in order]
+    F8State(w, cuda_device, batches=batches).assert_cache_equal()
+
+
+@pytest.mark.parametrize("name", sorted(SPECS))
+def test_f8v4_decode_attention_matches_oracle(name, cuda_device):
+    g = _state(name, cuda_device)
+    rows = H.owned_rows(g.w)
+    ref_out, ref_lse = g.oracle(rows)
+    for ns in (1, 4, 0):
+        out, lse = g.gpu(num_splits=ns)
+        H.compare(out, lse, ref_out, ref_lse, rows, label=f"f8v4 {name} splits={ns}")
+
+
+@pytest.mark.parametrize("window,sink", [(37, 1.5), (1000, None), (0, -2.0)])
+def test_f8v4_sinks_and_window(window, sink, cuda_device):
+    g = _state("decode", cuda_device)
+    rows = H.owned_rows(g.w)
+    sinks = None if sink is None else np.full(g.w.spec.hq, sink, np.float32)
+    ref_out, ref_lse = g.oracle(rows, sinks=sinks, window=window)
+    for ns in (1, 3):
+        out, lse = g.gpu(num_splits=ns, sinks=sinks, window=window)
+        H.compare(out, lse, ref_out, ref_lse, rows, label=f"f8v4 window={window} sink={sink}")
+
+
+def test_f8v4_rejects_multi_token_rows(cuda_device):
+    g = _state("decode", cuda_device)
+    w = g.w
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        _lib.paged_attention_f8v4(g.q, g.kc, g.vc, g.vs, g.vz, g.cu, g.seq_lens, g.bt, 2,
+                                  w.max_seq_len)
+    assert e.value.status == _lib.Status.UNSUPPORTED
