@@ -83,7 +83,7 @@ __device__ __forceinline__ void load32(uint32_t stage, int lane, float (&x)[32])
 // what it copied, so loads stay in flight without holding registers and no
 // barrier is needed.
 template <int D, int BS>
-__global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
+__global__ void __launch_bounds__(32 * kStoreWarps, 4) kv_store_kernel(
     const uint16_t *__restrict__ key, int64_t key_stride, const uint16_t *__restrict__ value,
     int64_t value_stride, const int64_t *__restrict__ slot_mapping, int32_t num_tokens,
     int32_t hk, int8_t *__restrict__ k_cache, uint16_t *__restrict__ k_scale,
@@ -182,10 +182,10 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
     const uint64_t shift2 = f32x2_pack(kShift, kShift), unshift2 = f32x2_pack(-kShift, -kShift);
     const uint64_t minus1 = f32x2_pack(-1.0f, -1.0f);
     uint32_t w[8];
-    uint32_t near = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       uint32_t tb2[4];
+      uint32_t near = 0;  // values of this word within 2^-15 of a tie
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const uint32_t xx = xw[2 * k + u];
@@ -197,24 +197,22 @@ __global__ void __launch_bounds__(32 * kStoreWarps) kv_store_kernel(
         f32x2_unpack(d2, d0, d1);
         tb2[2 * u] = __float_as_uint(t0);
         tb2[2 * u + 1] = __float_as_uint(t1);
-        near |= (fabsf(d0) >= kFar ? 1u : 0u) << (4 * k + 2 * u);
-        near |= (fabsf(d1) >= kFar ? 1u : 0u) << (4 * k + 2 * u + 1);
+        near |= (fabsf(d0) >= kFar ? 1u : 0u) << (2 * u);
+        near |= (fabsf(d1) >= kFar ? 1u : 0u) << (2 * u + 1);
+      }
+      // Values within 2^-15 of a tie (with bf16 inputs, e.g. every x = max/2
+      // exactly) take the code of the IEEE quotient, decided without a
+      // divide.  Rare; patched here so that the words stay in registers.
+      if (near != 0u && active) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (near & (1u << e)) {
+            const uint32_t xx = xw[2 * k + (e >> 1)];
+            tb2[e] = static_cast<uint32_t>(tie_code((e & 1) ? bf16_hi(xx) : bf16_lo(xx), sc, rs));
+          }
       }
       w[k] = __byte_perm(__byte_perm(tb2[0], tb2[1], 0x0040), __byte_perm(tb2[2], tb2[3], 0x0040),
                          0x5410);
-    }
-    // Values within 2^-15 of a tie (with bf16 inputs, e.g. every x = max/2
-    // exactly) take the code of the IEEE quotient, decided without a divide.
-    if (!active) near = 0;
-    while (near) {
-      const int k = __ffs(near) - 1;
-      near &= near - 1;
-      const float x = __uint_as_float(
-          static_cast<uint32_t>(lds16(sbase + row_chunk(lane, k >> 3) + (k & 7) * 2)) << 16);
-      const uint32_t c = static_cast<uint32_t>(tie_code(x, sc, rs)) & 0xffu;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j == (k >> 2)) w[j] = (w[j] & ~(0xffu << (8 * (k & 3)))) | (c << (8 * (k & 3)));
     }
     const uint16_t sbits = __half_as_ushort(__float2half_rn(sc));
     const int64_t blk = active ? slot / block_size : 0;

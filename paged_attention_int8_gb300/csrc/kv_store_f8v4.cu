@@ -133,26 +133,33 @@ __global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
     for (int i = 0; i < W; ++i) mate_nib[i] = __shfl_sync(0xffffffffu, nib[i], mate);
     if (!active) continue;
     uint8_t *vrow = v_cache + page * D * (block_size / 2) + off / 2;  // channel 0's byte
+    // (loops fully unrolled: the nibble words stay in registers)
     if (paired) {
       if (off & 1) continue;  // the even-offset token writes the byte
-#pragma unroll 4
-      for (int c = 0; c < D; ++c) {
-        const uint32_t lo4 = (nib[c / 8] >> (4 * (c % 8))) & 0xfu;
-        const uint32_t hi4 = (mate_nib[c / 8] >> (4 * (c % 8))) & 0xfu;
-        vrow[static_cast<int64_t>(c) * (block_size / 2)] = static_cast<uint8_t>(lo4 | (hi4 << 4));
-      }
+#pragma unroll
+      for (int i = 0; i < W; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t lo4 = (nib[i] >> (4 * j)) & 0xfu;
+          const uint32_t hi4 = (mate_nib[i] >> (4 * j)) & 0xfu;
+          vrow[static_cast<int64_t>(8 * i + j) * (block_size / 2)] =
+              static_cast<uint8_t>(lo4 | (hi4 << 4));
+        }
     } else {
-#pragma unroll 4
-      for (int c = 0; c < D; ++c) {
-        const uint32_t v4 = (nib[c / 8] >> (4 * (c % 8))) & 0xfu;
-        uint8_t *byte = vrow + static_cast<int64_t>(c) * (block_size / 2);
-        unsigned int *word = reinterpret_cast<unsigned int *>(
-            reinterpret_cast<uintptr_t>(byte) & ~static_cast<uintptr_t>(3));
-        const uint32_t shift = 8u * static_cast<uint32_t>(reinterpret_cast<uintptr_t>(byte) & 3u) +
-                               4u * static_cast<uint32_t>(off & 1);
-        atomicAnd(word, ~(0xfu << shift));
-        atomicOr(word, v4 << shift);
-      }
+#pragma unroll
+      for (int i = 0; i < W; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t v4 = (nib[i] >> (4 * j)) & 0xfu;
+          uint8_t *byte = vrow + static_cast<int64_t>(8 * i + j) * (block_size / 2);
+          unsigned int *word = reinterpret_cast<unsigned int *>(
+              reinterpret_cast<uintptr_t>(byte) & ~static_cast<uintptr_t>(3));
+          const uint32_t shift =
+              8u * static_cast<uint32_t>(reinterpret_cast<uintptr_t>(byte) & 3u) +
+              4u * static_cast<uint32_t>(off & 1);
+          atomicAnd(word, ~(0xfu << shift));
+          atomicOr(word, v4 << shift);
+        }
     }
   }
 }
