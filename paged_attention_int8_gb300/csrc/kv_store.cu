@@ -15,9 +15,10 @@
 // the byte stores into the channel-major V pages (and the V scale stores)
 // coalesce across lanes whenever consecutive tokens fill consecutive slots
 // of a page (prefill chunks, cache population).  The quotient x / s is
-// formed as x * (1/s) and rounded there unless it lies within 2^-15 of a
-// rounding tie, where the IEEE quotient decides (the two differ by less than
-// 2.27e-5 for |x / s| <= 127.00002).
+// formed as x * (1/s) (fused, unrounded) and rounded to an integer there
+// unless it lies within 2^-15 of a rounding tie, where the IEEE quotient
+// decides (the two round alike elsewhere: they differ by less than 1.6e-5
+// for |x / s| <= 127.00002).
 // Its roofline is HBM: per (token, kv head) it reads 4*D bytes and writes
 // 2*(D + D/16) bytes.  The V side is bound instead by memory-instruction
 // issue: each channel-major V page takes one byte per (token, channel).
@@ -27,11 +28,11 @@
 
 namespace paq8 {
 
-// Four codes (each in [-127, 127]) -> one little-endian word.
-__device__ __forceinline__ uint32_t pack4(int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
-  const uint32_t lo = __byte_perm(static_cast<uint32_t>(c0), static_cast<uint32_t>(c1), 0x0040);
-  const uint32_t hi = __byte_perm(static_cast<uint32_t>(c2), static_cast<uint32_t>(c3), 0x0040);
-  return __byte_perm(lo, hi, 0x5410);
+// Lane-wise unsigned max of two pairs of 16-bit values.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // copies into shared memory that complete asynchronously (per thread)
@@ -57,21 +58,6 @@ constexpr int kStoreSmem = kStoreWarps * kStoreStages * kStoreStageBytes;
 // groups
 __device__ __forceinline__ uint32_t row_chunk(int lane, int j) {
   return static_cast<uint32_t>(lane * 64 + ((j + (lane >> 1)) & 3) * 16);
-}
-
-// this lane's 32 bf16 values of a stage -> fp32
-__device__ __forceinline__ void load32(uint32_t stage, int lane, float (&x)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(stage + row_chunk(lane, j)));
-    x[8 * j + 0] = bf16_lo(v.x); x[8 * j + 1] = bf16_hi(v.x);
-    x[8 * j + 2] = bf16_lo(v.y); x[8 * j + 3] = bf16_hi(v.y);
-    x[8 * j + 4] = bf16_lo(v.z); x[8 * j + 5] = bf16_hi(v.z);
-    x[8 * j + 6] = bf16_lo(v.w); x[8 * j + 7] = bf16_hi(v.w);
-  }
 }
 
 // grid: (token-block slots, ceil(2 * hk * D/32 / kStoreWarps)); block: 32 x
@@ -163,52 +149,59 @@ __global__ void __launch_bounds__(32 * kStoreWarps, 4) kv_store_kernel(
       xw[4 * j + 2] = v.z;
       xw[4 * j + 3] = v.w;
     }
-    float amax = 0.0f;
+    // group max |x| on the bf16 bit patterns, two at a time: with the sign
+    // cleared, their unsigned order is that of |x| (finite values)
+    uint32_t m2 = 0u;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) amax = fmax3(amax, fabsf(bf16_lo(xw[k])), fabsf(bf16_hi(xw[k])));
+    for (int k = 0; k < 16; ++k) m2 = max_u16x2(m2, xw[k] & 0x7fff7fffu);
+    const float amax = __uint_as_float(max(m2 & 0xffffu, m2 >> 16) << 16);
     const float sc = group_scale(amax);
     const float rs = __frcp_rn(sc);
 
-    // ---- codes.  q = x * (1/s) is rounded to the nearest integer (ties to
-    // even) by adding 1.5 * 2^23, whose low byte is then the code.  q and the
-    // IEEE quotient x / s differ by under 2.27e-5 (|q| <= 127.00002: two
-    // roundings of at most 2^-24 relative each in q, one in x / s), so where
-    // q lies 2^-15 or more from a rounding tie both round alike, and nearest
-    // even there is also half away from zero; no clamp is needed.  Values
-    // closer to a tie are marked and decided exactly below.
+    // ---- codes.  c = the integer nearest to q = x * (1/s), taken exactly
+    // from one fused multiply-add of 1.5 * 2^23 (its low byte is then the
+    // code); d = q - c from a second one.  q and the IEEE quotient x / s
+    // differ by under 7.6e-6 (|x / s| <= 127.00002, one rounding of 1/s),
+    // and RN(x / s) by under 1.6e-5, so where |d| < 1/2 - 2^-15 all three
+    // round to c and nearest even is also half away from zero; no clamp is
+    // needed.  Values closer to a tie are marked and decided exactly.
     constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
     constexpr float kFar = 0.5f - 0x1p-15f;
     const uint64_t rs2 = f32x2_pack(rs, rs);
-    const uint64_t shift2 = f32x2_pack(kShift, kShift), unshift2 = f32x2_pack(-kShift, -kShift);
+    const uint64_t shift2 = f32x2_pack(kShift, kShift);
     const uint64_t minus1 = f32x2_pack(-1.0f, -1.0f);
     uint32_t w[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       uint32_t tb2[4];
-      uint32_t near = 0;  // values of this word within 2^-15 of a tie
+      float d[4], nc[4];
+      bool near = false;  // a value of this word within 2^-15 of a tie
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const uint32_t xx = xw[2 * k + u];
-        const uint64_t q2 = f32x2_mul(f32x2_pack(bf16_lo(xx), bf16_hi(xx)), rs2);
-        const uint64_t t2 = f32x2_add(q2, shift2);
-        const uint64_t d2 = f32x2_fma(f32x2_add(t2, unshift2), minus1, q2);  // q - rint(q)
-        float t0, t1, d0, d1;
+        const uint64_t x2 = f32x2_pack(bf16_lo(xx), bf16_hi(xx));
+        const uint64_t t2 = f32x2_fma(x2, rs2, shift2);       // 1.5 * 2^23 + c
+        const uint64_t nc2 = f32x2_fma(t2, minus1, shift2);   // -c, exact
+        const uint64_t d2 = f32x2_fma(x2, rs2, nc2);          // x * rs - c
+        float t0, t1;
         f32x2_unpack(t2, t0, t1);
-        f32x2_unpack(d2, d0, d1);
+        f32x2_unpack(d2, d[2 * u], d[2 * u + 1]);
+        f32x2_unpack(nc2, nc[2 * u], nc[2 * u + 1]);
         tb2[2 * u] = __float_as_uint(t0);
         tb2[2 * u + 1] = __float_as_uint(t1);
-        near |= (fabsf(d0) >= kFar ? 1u : 0u) << (2 * u);
-        near |= (fabsf(d1) >= kFar ? 1u : 0u) << (2 * u + 1);
+        near = near || fabsf(d[2 * u]) >= kFar || fabsf(d[2 * u + 1]) >= kFar;
       }
       // Values within 2^-15 of a tie (with bf16 inputs, e.g. every x = max/2
       // exactly) take the code of the IEEE quotient, decided without a
-      // divide.  Rare; patched here so that the words stay in registers.
-      if (near != 0u && active) {
+      // divide from the half-integer h = c + sign(d) / 2 they lie next to.
+      // Patched here so that the words stay in registers.
+      if (near && active) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (near & (1u << e)) {
+          if (fabsf(d[e]) >= kFar) {
             const uint32_t xx = xw[2 * k + (e >> 1)];
-            tb2[e] = static_cast<uint32_t>(tie_code((e & 1) ? bf16_hi(xx) : bf16_lo(xx), sc, rs));
+            const float h = __fsub_rn(copysignf(0.5f, d[e]), nc[e]);
+            tb2[e] = tie_code_bits((e & 1) ? bf16_hi(xx) : bf16_lo(xx), sc, h);
           }
       }
       w[k] = __byte_perm(__byte_perm(tb2[0], tb2[1], 0x0040), __byte_perm(tb2[2], tb2[3], 0x0040),

@@ -38,4 +38,23 @@ __device__ __forceinline__ int32_t tie_code(float x, float s, float rs) {
   return q < 0.0f ? -m : m;
 }
 
+// The same rule from the half-integer h itself (x / s within 2^-14 of h),
+// as the bits of code + 1.5 * 2^23, whose low byte is the code's two's
+// complement byte: e = x - h * s is exact, RN(x / s) == h when |e| is at most
+// half the spacing below |h| times s (the spacing of the float before |h|,
+// so that |h| = 0.5 needs no special case), and the code is h moved half a
+// step away from zero when RN(x / s) == h or x / s lies beyond h (e and h of
+// one sign), else half a step toward zero.
+__device__ __forceinline__ uint32_t tie_code_bits(float x, float s, float h) {
+  const float e = __fmaf_rn(-h, s, x);
+  const uint32_t hb = __float_as_uint(h);
+  const float half_gap =
+      __uint_as_float((((hb & 0x7fffffffu) - 1u) & 0x7f800000u) - (24u << 23));
+  const bool away = fabsf(e) <= __fmul_rn(half_gap, s) ||
+                    static_cast<int32_t>(__float_as_uint(e) ^ hb) >= 0;
+  const float step = __uint_as_float((hb & 0x80000000u) | 0x3f000000u);  // copysign(0.5, h)
+  const float code = __fadd_rn(h, away ? step : -step);
+  return __float_as_uint(__fadd_rn(code, 12582912.0f));
+}
+
 }  // namespace paq8
