@@ -227,6 +227,54 @@ def test_kv_store_near_ties_bit_exact(cuda_device):
     H.assert_cache_equal(g, H.OracleState(w))
 
 
+def _page_run_batches(rng, hk, d, bs, nb):
+    """Two store batches over sequences laid on randomly permuted blocks,
+    each sequence starting mid-page (as a prefill chunk after a prefix or a
+    cache population) and cut in two, so that the second batch continues
+    pages the first left partial; about 8% padding rows and a few scattered
+    single slots are mixed into both."""
+    perm = list(rng.permutation(nb))
+    a_slots, b_slots = [], []
+    for L in rng.integers(3, 5 * bs, size=10):
+        start = int(rng.integers(0, bs))
+        nblk = (start + int(L) + bs - 1) // bs
+        blocks = [perm.pop() for _ in range(nblk)]
+        seq = [blocks[p // bs] * bs + p % bs for p in range(start, start + int(L))]
+        cut = int(rng.integers(0, len(seq) + 1))
+        a_slots += seq[:cut]
+        b_slots += seq[cut:]
+    spare = [perm.pop() * bs + int(rng.integers(0, bs)) for _ in range(6)]
+    a_slots += spare[:3]
+    b_slots += spare[3:]
+    out = []
+    for sl in (a_slots, b_slots):
+        sl = np.array(sl, np.int64)
+        at = rng.integers(0, sl.shape[0] + 1, size=max(1, sl.shape[0] // 12))
+        full = np.insert(sl, np.sort(at), -1)
+        n = full.shape[0]
+        k = torch.from_numpy(rng.standard_normal((n, hk, d)) * 1.5).to(torch.bfloat16)
+        v = torch.from_numpy(rng.standard_normal((n, hk, d))).to(torch.bfloat16)
+        out.append((k, v, torch.from_numpy(full)))
+    return out
+
+
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 16), (128, 32), (256, 16), (256, 32)])
+def test_kv_store_page_runs_bit_exact(d, bs, cuda_device):
+    rng = np.random.default_rng(50 + d + bs)
+    hk, nb = 2, 128
+    (ka, va, sa), (kb, vb, sb) = _page_run_batches(rng, hk, d, bs, nb)
+    spec = inputs.Spec("page_runs", 0, hq=hk, hk=hk, d=d, bs=bs)
+    w = inputs.Workload(spec=spec, q_lens=torch.zeros(0, dtype=torch.int32),
+                        seq_lens=torch.zeros(0, dtype=torch.int32),
+                        cu_seqlens_q=torch.zeros(1, dtype=torch.int32),
+                        block_table=torch.zeros((0, 1), dtype=torch.int32), num_blocks=nb,
+                        prefix_key=ka, prefix_value=va, prefix_slots=sa,
+                        new_key=kb, new_value=vb, new_slots=sb,
+                        q=torch.zeros((0, hk, d), dtype=torch.bfloat16))
+    g = H.GpuState(w, cuda_device)  # stores batch a, then batch b
+    H.assert_cache_equal(g, H.OracleState(w))
+
+
 def _near_tie_groups(rng, count):
     """Groups of 32 bf16 values (as fp32), group max first, whose quotients
     x / s (s = fp32(amax / 127)) sit on a rounding tie k + 1/2 or close to
