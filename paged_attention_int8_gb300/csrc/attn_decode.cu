@@ -212,7 +212,20 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
     const uint32_t st = smem_base + stage * L::kBytes;
     const int key0 = (tile_lo + it) * kTile + my_mt * 16;  // first key of this warp's block
     // keys outside [kv_begin, kv_end) in this block: masked, V scales zeroed
+    // (stale bytes may sit there).  The lane's validity masks -- score rows
+    // r0, r1 and V keys 4t .. 4t+3 -- are formed once per tile, on edge
+    // tiles only, and applied without compares elsewhere.
     const bool tail = key0 + 16 > kv_end || key0 < kv_begin;
+    bool ok0 = true, ok1 = true;
+    uint2 vmask = make_uint2(0xffffffffu, 0xffffffffu);
+    if (tail) {
+      const auto in = [&](int k) { return k >= kv_begin && k < kv_end; };
+      ok0 = in(key0 + r0);
+      ok1 = in(key0 + r1);
+      const int kv = key0 + 4 * t;
+      vmask.x = (in(kv) ? 0x0000ffffu : 0u) | (in(kv + 1) ? 0xffff0000u : 0u);
+      vmask.y = (in(kv + 2) ? 0x0000ffffu : 0u) | (in(kv + 3) ? 0xffff0000u : 0u);
+    }
 
     // ---------------- S^T = K Q^T with exact codes, scaled per group
     float s[4];
@@ -246,11 +259,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      float v = s[e] * a.scale_log2;
-      if (tail) {
-        const int key = key0 + (e < 2 ? r0 : r1);
-        if (key >= kv_end || key < kv_begin) v = -INFINITY;
-      }
+      const float v = (e < 2 ? ok0 : ok1) ? s[e] * a.scale_log2 : -INFINITY;
       s[e] = v;
       mx[e & 1] = fmaxf(mx[e & 1], v);
     }
@@ -290,8 +299,9 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kMinBlocks)
     // ---------------- O^T += V'^T P^T, V' = code * scale in fp16
 #pragma unroll
     for (int gv = 0; gv < G; ++gv) {
-      const uint2 vsc =
-          v_scales4<L>(st, my_mt * 16 + 4 * t, gv, tail, key0 - my_mt * 16, kv_begin, kv_end);
+      uint2 vsc = lds64(st + L::vs_off(my_mt * 16 + 4 * t, gv));
+      vsc.x &= vmask.x;
+      vsc.y &= vmask.y;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cm = gv * 2 + half;

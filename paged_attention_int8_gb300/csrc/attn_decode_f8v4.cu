@@ -287,6 +287,11 @@ __global__ void __launch_bounds__(kThreads, F8V4Cfg<D>::kMinBlocks)
     const uint32_t st = smem_base + stage * L::kBytes;
     const int key0 = (tile_lo + it) * kTile + my_mt * 16;
     const bool tail = key0 + 16 > kv_end || key0 < kv_begin;
+    bool ok0 = true, ok1 = true;  // score rows r0, r1 inside [kv_begin, kv_end)
+    if (tail) {
+      ok0 = key0 + r0 >= kv_begin && key0 + r0 < kv_end;
+      ok1 = key0 + r1 >= kv_begin && key0 + r1 < kv_end;
+    }
 
     // ---------------- S^T = K Q^T, K exact in fp16, one accumulator
     float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -309,11 +314,7 @@ __global__ void __launch_bounds__(kThreads, F8V4Cfg<D>::kMinBlocks)
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      float v = s[e] * a.scale_log2;
-      if (tail) {
-        const int key = key0 + (e < 2 ? r0 : r1);
-        if (key >= kv_end || key < kv_begin) v = -INFINITY;
-      }
+      const float v = (e < 2 ? ok0 : ok1) ? s[e] * a.scale_log2 : -INFINITY;
       s[e] = v;
       mx[e & 1] = fmaxf(mx[e & 1], v);
     }
