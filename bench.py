@@ -95,7 +95,7 @@ def load_peaks():
 # The sources of the kernels one paged_attention call launches (their host
 # dispatch included); a recorded ncu figure holds while these are unchanged.
 ATTENTION_SOURCES = ("attention.cu", "attn_decode.cu", "attn_prefill.cu", "attn_prefill_tc.cu",
-                     "attn_common.cuh", "common.cuh", "tcgen05.cuh", "launch.h")
+                     "attn_common.cuh", "attn_f8v4.cuh", "common.cuh", "tcgen05.cuh", "launch.h")
 
 
 def kernel_sources_sha256() -> str:
@@ -296,22 +296,29 @@ def kv_store_measure(r: Runner, reps: int = 20):
             "achieved_gbs": round(nbytes / (ms * 1e-3) * 1e-9, 2)}
 
 
+MERGE_ROWS = 1 << 19  # (token, q head) rows of the merge measurement
+
+
 def merge_measure(r: Runner, reps: int = 20):
-    """merge_attn_states on the step's output (all T * Hq rows) and a second
-    state of the same shape, as when a cached prefix and the new keys are
-    attended in two passes: algorithmic bytes (two bf16 outputs and two LSEs
-    read, the merged output and LSE written) per CUDA-event time."""
+    """merge_attn_states of two attention states over MERGE_ROWS (token, q
+    head) rows of the workload's head size -- a cached-prefix pass and a
+    new-key pass of a large prefill batch, seeded synthetic values (the
+    step's own output is too small to measure bandwidth on): algorithmic
+    bytes (two bf16 outputs and two LSEs read, the merged output and LSE
+    written) per CUDA-event time."""
     d = r.out.shape[-1]
-    rows = r.out.numel() // d
-    out_b = r.out.clone()
-    lse_b = r.lse.clone().nan_to_num_(0.0) - 0.5
-    lse_a = r.lse.clone().nan_to_num_(0.0)
-    merged = torch.empty_like(r.out)
-    lse_m = torch.empty_like(r.lse)
+    rows = MERGE_ROWS
+    gen = torch.Generator(device=r.device).manual_seed(7)
+    out_a = torch.randn((rows, 1, d), generator=gen, device=r.device).to(torch.bfloat16)
+    out_b = torch.randn((rows, 1, d), generator=gen, device=r.device).to(torch.bfloat16)
+    lse_a = torch.randn((rows, 1), generator=gen, device=r.device) * 4.0
+    lse_b = torch.randn((rows, 1), generator=gen, device=r.device) * 4.0
+    merged = torch.empty_like(out_a)
+    lse_m = torch.empty_like(lse_a)
     nbytes = rows * (3 * d * 2 + 3 * 4)
 
     def call():
-        _lib.merge_attn_states(r.out, lse_a, out_b, lse_b, out=merged, lse=lse_m)
+        _lib.merge_attn_states(out_a, lse_a, out_b, lse_b, out=merged, lse=lse_m)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -346,18 +353,19 @@ def merge_measure(r: Runner, reps: int = 20):
         torch.cuda.synchronize()
         ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
         timing = "CUDA events around each call"
-    del out_b, lse_b, lse_a, merged, lse_m
+    del out_a, out_b, lse_b, lse_a, merged, lse_m
     return {"rows": rows, "bytes": nbytes, "ms": round(ms, 5),
             "achieved_gbs": round(nbytes / (ms * 1e-3) * 1e-9, 2), "timing": timing,
             "l2": "inputs larger than L2" if rows * (4 * d + 8) > L2_BYTES else "inputs fit in L2"}
 
 
-def f8v4_measure(w: inputs.Workload, device, reps: int = 20):
-    """The same decode batch stored in the fp8 / 4-bit format (e4m3 keys,
-    4-bit values with a per-key fp16 scale and zero) and attended by
-    paged_attention_f8v4: algorithmic bytes per call (D + D/2 + 4 per visible
-    (key, kv head), q, out, lse, block-table entries, metadata) per CUDA-event
-    time, and the time against the q8 call's."""
+def f8v4_measure(w: inputs.Workload, device, flops=None, reps: int = 20):
+    """The same batch stored in the fp8 / 4-bit format (e4m3 keys, 4-bit
+    values with a per-key fp16 scale and zero) and attended by
+    paged_attention_f8v4.  Decode batches: algorithmic bytes per call (D +
+    D/2 + 4 per visible (key, kv head), q, out, lse, block-table entries,
+    metadata) per CUDA-event time; prefill batches (``flops`` given): FLOPs
+    per CUDA-event time against the tensor peak."""
     s = w.spec
     kc, vc, vs, vz = inputs.empty_cache_f8v4(w.num_blocks, s.hk, s.bs, s.d, device=device,
                                              canary=False)
@@ -375,8 +383,9 @@ def f8v4_measure(w: inputs.Workload, device, reps: int = 20):
     lse = torch.empty((w.num_tokens, s.hq), dtype=torch.float32, device=device)
 
     def call():
-        _lib.paged_attention_f8v4(q, kc, vc, vs, vz, cu, seq_lens, bt, 1, w.max_seq_len,
-                                  w.softmax_scale, num_splits=ns, out=out, lse=lse, workspace=ws)
+        _lib.paged_attention_f8v4(q, kc, vc, vs, vz, cu, seq_lens, bt, w.max_query_len,
+                                  w.max_seq_len, w.softmax_scale, num_splits=ns, out=out, lse=lse,
+                                  workspace=ws)
 
     for _ in range(3):
         call()
@@ -394,12 +403,19 @@ def f8v4_measure(w: inputs.Workload, device, reps: int = 20):
     T = w.num_tokens
     nbytes = kv + T * s.hq * s.d * 4 + T * s.hq * 4 + int(((L + s.bs - 1) // s.bs).sum()) * 4 \
         + (2 * w.num_seqs + 1) * 4
-    hbm_peak, _, _ = load_peaks()
+    hbm_peak, tc_peak, _ = load_peaks()
     gbs = nbytes / (ms * 1e-3) * 1e-9
     del kc, vc, vs, vz, ws
-    return {"format": "fp8 e4m3 keys, 4-bit values with fp16 scale and zero per key",
-            "bytes": nbytes, "ms": round(ms, 5), "achieved_gbs": round(gbs, 2),
-            "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "num_splits": ns}
+    res = {"format": "fp8 e4m3 keys, 4-bit values with fp16 scale and zero per key",
+           "bytes": nbytes, "ms": round(ms, 5), "achieved_gbs": round(gbs, 2),
+           "num_splits": ns}
+    if flops is None:
+        res.update(peak=hbm_peak, frac=round(gbs / hbm_peak, 4))
+    else:
+        tf = flops / (ms * 1e-3) * 1e-12
+        res.update(flops=flops, tflops=round(tf, 2), peak=tc_peak, frac=round(tf / tc_peak, 4),
+                   kernel="generic mma.sync kernel (the tcgen05 kernel reads the q8 format)")
+    return res
 
 
 def e2e_measure(r: Runner, steps: int, warmup: int):
@@ -634,9 +650,9 @@ def run_workload(name, args, device, rank, world, headline: bool):
             store["peak"] = hbm_peak
             store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
         entry["kv_store"] = store
-    if rank == 0 and name == "decode_batch" and not args.no_kv_store:
+    if rank == 0 and name in ("decode_batch", "chunked_prefill") and not args.no_kv_store:
         # the alternative format on the same batch: fewer bytes per key
-        f8 = f8v4_measure(w, device)
+        f8 = f8v4_measure(w, device, flops=work["flops"] if unit == "TFLOP/s" else None)
         f8["vs_q8_call"] = round(f8["ms"] / attn_ms, 4)
         entry["f8v4"] = f8
     if headline and rank == 0:

@@ -289,11 +289,10 @@ pa_status pa_kv_store_f8v4(const void *key, int64_t key_token_stride,
 
 /*
  * paged_attention over the fp8 / 4-bit format: as pa_paged_attention_ex
- * (sinks, sliding window, flags), for decode rows (max_query_len == 1, at
- * most 8 q heads per kv head; otherwise PA_ERR_UNSUPPORTED).  Numerics: K is
- * exact in fp16 (every e4m3 value is an fp16 value), QK^T accumulates in
- * fp32; V' = idx * scale + zero in one fp16 FMA; softmax and accumulation in
- * fp32; output bf16.
+ * (decode and prefill rows in one batch, split-KV segments, non-causal
+ * mode, sinks, sliding window, flags).  Numerics: K is exact in fp16 (every
+ * e4m3 value is an fp16 value), QK^T accumulates in fp32; V' = idx * scale
+ * + zero in one fp16 FMA; softmax and accumulation in fp32; output bf16.
  */
 pa_status pa_paged_attention_f8v4(const void *q, const void *k_cache, const void *v_cache,
                                   const void *v_scale, const void *v_zero,

@@ -203,10 +203,6 @@ pa_status attention_args(const void *q, const void *k_cache, const void *k_scale
   if ((lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
       (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3u)))
     return fail(PA_ERR_INVALID_ARG, "lse and sinks must be 4-byte aligned");
-  if (f8v4 && (max_query_len != 1 || num_q_heads / num_kv_heads > 8))
-    return fail(PA_ERR_UNSUPPORTED,
-                "the fp8 / 4-bit format is read by the decode path: max_query_len 1, <= 8 q heads "
-                "per kv head");
   if ((flags & PA_ATTN_TEST_TIMEOUT) &&
       (max_query_len != 1 || num_q_heads / num_kv_heads > 8))
     return fail(PA_ERR_INVALID_ARG,

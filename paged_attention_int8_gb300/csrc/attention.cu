@@ -12,6 +12,8 @@
 //                      Hq/Hk > 8;
 //  * reduce_kernel  -- merges the segment triples of split rows by
 //                      log-sum-exp (the pages' reduce_segments step).
+// Over the fp8-key / 4-bit-value format the decode rows take
+// decode_f8v4_kernel and every other row the generic kernel, in that format.
 // A batch that holds only decode rows (max_query_len == 1) launches no
 // prefill kernel; both kernels exit at once for rows that are not theirs.
 #include <algorithm>
@@ -25,7 +27,7 @@ namespace paq8 {
 cudaError_t launch_decode(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int d,
                           int bs, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                           int d, int bs, cudaStream_t stream);
+                           int d, int bs, bool f8v4, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                               int d, int bs, cudaStream_t stream);
 cudaError_t launch_decode_f8v4(const AttnArgs &a, int d, int bs, cudaStream_t stream);
@@ -218,9 +220,8 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
 
   const bool use_decode = a.qpk <= 8;
   const bool use_prefill = !use_decode || L.max_query_len > 1;
-  if (L.f8v4 && use_prefill) return cudaErrorInvalidValue;  // rejected by the API first
   const int64_t pages = static_cast<int64_t>(L.num_blocks) * L.hk;
-  CUtensorMap tk, tv;
+  CUtensorMap tk = {}, tv = {};
   const int krow = L.d >= 128 ? 128 : L.d;
   // the fp8 / 4-bit decode kernel copies its pages with cp.async only
   if (!L.f8v4 &&
@@ -250,7 +251,8 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   }
   // tcgen05 prefill for multi-token sequences when the decode kernel takes the
   // single-token ones; the mma.sync kernel otherwise (D = 256, Hq/Hk > 8)
-  const bool use_tc = use_decode && prefill_tc_supported(L.d);
+  // (the fp8 / 4-bit format takes the generic kernel for multi-token rows)
+  const bool use_tc = use_decode && prefill_tc_supported(L.d) && !L.f8v4;
   const bool fork = L.side_stream_ok && use_decode && use_prefill && use_tc;
   if (fork) {
     // mixed batch: the prefill kernel on the side stream, forked from and
@@ -295,7 +297,7 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
       if (p.seg_tiles < 1) p.seg_tiles = 1;
       a.seg_tiles = p.seg_tiles;
     }
-    cudaError_t e = launch_prefill(p, tk, tv, L.d, L.bs, stream);
+    cudaError_t e = launch_prefill(p, tk, tv, L.d, L.bs, L.f8v4, stream);
     if (e != cudaSuccess) return e;
   }
   if (L.num_splits <= 1) return cudaSuccess;

@@ -17,16 +17,23 @@
 // exact integer codes (fp16) per 32-channel group, scaled by the group's K
 // scale in fp32; PV multiplies P (fp16) by V' = code * scale (fp16), read
 // from the channel-major V pages 4 keys per 32-bit load.
+// The same kernel reads the fp8-key / 4-bit-value format (F8): QK^T in one
+// accumulation over all channels (e4m3 keys are exact in fp16, no group
+// scales), V' = idx * scale + zero per key, pages copied by that format's
+// producer.
+#include <type_traits>
+
 #include "attn_common.cuh"
+#include "attn_f8v4.cuh"
 #include "launch.h"
 
 namespace paq8 {
 
 constexpr int kTile = 64;  // keys per pipeline stage
 
-template <int D, int BS>
+template <int D, int BS, bool F8>
 struct AttnCfg {
-  using L = StageLayout<D, BS, kTile>;
+  using L = std::conditional_t<F8, StageF8V4<D, BS, kTile>, StageLayout<D, BS, kTile>>;
   static constexpr int G = D / 32;
   static constexpr int kQBytes = 4 * G * 2 * 32 * 16;  // fragment-ordered q, 4 row groups
   static constexpr int kQOff = kStages * L::kBytes;
@@ -37,11 +44,11 @@ struct AttnCfg {
   static_assert(3 * kMergeFields * 32 * 4 <= kStages * L::kBytes, "merge area");
 };
 
-template <int D, int BS>
+template <int D, int BS, bool F8>
 __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant__ AttnArgs a,
                                                            const __grid_constant__ CUtensorMap tmap_k,
                                                            const __grid_constant__ CUtensorMap tmap_v) {
-  using C = AttnCfg<D, BS>;
+  using C = AttnCfg<D, BS, F8>;
   using L = typename C::L;
   constexpr int G = C::G;
   extern __shared__ uint8_t smem_raw[];
@@ -120,8 +127,12 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    produce_tiles_lsu<L, BS>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter, kv_begin,
-                             kv_end, lane);
+    if constexpr (F8)
+      produce_f8v4<L, BS, kStages>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter,
+                                   kv_begin, kv_end, lane);
+    else
+      produce_tiles_lsu<L, BS>(a, smem_base, bar_full, bar_empty, seq, h, tile_lo, n_iter,
+                               kv_begin, kv_end, lane);
     return;
   }
 
@@ -222,19 +233,26 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
       for (int nt = 0; nt < 8; ++nt) {
         const int kb16 = (nt >> 1) * 16;
         const uint2 kw = lds64(st + L::k_off(kb16 + ((nt & 1) ? kr_odd : kr_even), gq * 32 + t * 8));
-        uint32_t b0, b1, b2, b3;
-        codes4_to_half2(kw.x, b0, b1);
-        codes4_to_half2(kw.y, b2, b3);
-        float sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        mma_f16_16816(sg, qa0.x, qa0.y, qa0.z, qa0.w, b0, b1);
-        mma_f16_16816(sg, qa1.x, qa1.y, qa1.z, qa1.w, b2, b3);
-        const int off = (nt & 1) ? 2 : 0;  // odd n-tiles hold keys 4t+2, 4t+3
-        const float s0 = __half2float(__ushort_as_half(lds16(st + L::ks_off(kb16 + kc0 + off, gq))));
-        const float s1 = __half2float(__ushort_as_half(lds16(st + L::ks_off(kb16 + kc1 + off, gq))));
-        sc[nt][0] = fmaf(sg[0], s0, sc[nt][0]);
-        sc[nt][1] = fmaf(sg[1], s1, sc[nt][1]);
-        sc[nt][2] = fmaf(sg[2], s0, sc[nt][2]);
-        sc[nt][3] = fmaf(sg[3], s1, sc[nt][3]);
+        if constexpr (F8) {  // e4m3 bytes (0,1) -> k 2t, 2t+1; (2,3) -> k 2t+8, 2t+9
+          mma_f16_16816(sc[nt], qa0.x, qa0.y, qa0.z, qa0.w, e4m3x2_to_half2(kw.x),
+                        e4m3x2_to_half2(kw.x >> 16));
+          mma_f16_16816(sc[nt], qa1.x, qa1.y, qa1.z, qa1.w, e4m3x2_to_half2(kw.y),
+                        e4m3x2_to_half2(kw.y >> 16));
+        } else {
+          uint32_t b0, b1, b2, b3;
+          codes4_to_half2(kw.x, b0, b1);
+          codes4_to_half2(kw.y, b2, b3);
+          float sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          mma_f16_16816(sg, qa0.x, qa0.y, qa0.z, qa0.w, b0, b1);
+          mma_f16_16816(sg, qa1.x, qa1.y, qa1.z, qa1.w, b2, b3);
+          const int off = (nt & 1) ? 2 : 0;  // odd n-tiles hold keys 4t+2, 4t+3
+          const float s0 = __half2float(__ushort_as_half(lds16(st + L::ks_off(kb16 + kc0 + off, gq))));
+          const float s1 = __half2float(__ushort_as_half(lds16(st + L::ks_off(kb16 + kc1 + off, gq))));
+          sc[nt][0] = fmaf(sg[0], s0, sc[nt][0]);
+          sc[nt][1] = fmaf(sg[1], s1, sc[nt][1]);
+          sc[nt][2] = fmaf(sg[2], s0, sc[nt][2]);
+          sc[nt][3] = fmaf(sg[3], s1, sc[nt][3]);
+        }
       }
     }
 
@@ -288,16 +306,41 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
       const uint32_t pa1 = pack_half2(sc[2 * kk][2], sc[2 * kk][3]);
       const uint32_t pa2 = pack_half2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
       const uint32_t pa3 = pack_half2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+      if constexpr (F8) {
+        // the 4 keys 4t .. 4t+3 of this 16-key block: their scales and zeros
+        // (zeroed outside [kv_begin, kv_end): stale bytes may sit there)
+        uint2 vsc = lds64(st + L::vs_off(kk * 16 + 4 * t));
+        uint2 vzr = lds64(st + L::vz_off(kk * 16 + 4 * t));
+        if (tail) {
+          const int k = key0 + kk * 16 + 4 * t;
+          const auto in = [&](int x) { return x >= kv_begin && x < kv_end; };
+          const uint32_t mx = (in(k) ? 0x0000ffffu : 0u) | (in(k + 1) ? 0xffff0000u : 0u);
+          const uint32_t my = (in(k + 2) ? 0x0000ffffu : 0u) | (in(k + 3) ? 0xffff0000u : 0u);
+          vsc.x &= mx;
+          vzr.x &= mx;
+          vsc.y &= my;
+          vzr.y &= my;
+        }
 #pragma unroll
-      for (int gq = 0; gq < G; ++gq) {
-        const uint2 vsc = v_scales4<L>(st, kk * 16 + 4 * t, gq, tail, key0, kv_begin, kv_end);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t w = lds32(st + L::v_off(gq * 32 + jj * 8 + g, kk * 16 + 4 * t));
+        for (int c8 = 0; c8 < D / 8; ++c8) {
+          const uint32_t w = lds16(st + L::v_off(c8 * 8 + g, kk * 16 + 4 * t));
           uint32_t b0, b1;
-          codes4_to_half2(w, b0, b1);  // keys 4t, 4t+1 -> k 2t, 2t+1; 4t+2, 4t+3 -> k 2t+8, 2t+9
-          mma_f16_16816(o_acc[gq * 4 + jj], pa0, pa1, pa2, pa3, hmul2_u32(b0, vsc.x),
-                        hmul2_u32(b1, vsc.y));
+          nibbles4_to_half2(w, b0, b1);  // keys 4t, 4t+1 | 4t+2, 4t+3
+          mma_f16_16816(o_acc[c8], pa0, pa1, pa2, pa3, hfma2_u32(b0, vsc.x, vzr.x),
+                        hfma2_u32(b1, vsc.y, vzr.y));
+        }
+      } else {
+#pragma unroll
+        for (int gq = 0; gq < G; ++gq) {
+          const uint2 vsc = v_scales4<L>(st, kk * 16 + 4 * t, gq, tail, key0, kv_begin, kv_end);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t w = lds32(st + L::v_off(gq * 32 + jj * 8 + g, kk * 16 + 4 * t));
+            uint32_t b0, b1;
+            codes4_to_half2(w, b0, b1);  // keys 4t, 4t+1 -> k 2t, 2t+1; 4t+2, 4t+3 -> k 2t+8, 2t+9
+            mma_f16_16816(o_acc[gq * 4 + jj], pa0, pa1, pa2, pa3, hmul2_u32(b0, vsc.x),
+                          hmul2_u32(b1, vsc.y));
+          }
         }
       }
     }
@@ -400,27 +443,29 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   }
 }
 
-template <int D, int BS>
+template <int D, int BS, bool F8>
 static cudaError_t launch_prefill_t(const AttnArgs &args, const CUtensorMap &tk,
                                     const CUtensorMap &tv, dim3 grid, cudaStream_t stream) {
-  using C = AttnCfg<D, BS>;
+  using C = AttnCfg<D, BS, F8>;
   static DeviceOnce configured;  // the attribute is per device
   cudaError_t e = configured.get(nullptr, [](int, int *) {
-    return cudaFuncSetAttribute(prefill_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::kSmemBytes);
+    return cudaFuncSetAttribute(prefill_kernel<D, BS, F8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
-  prefill_kernel<D, BS><<<grid, kThreads, C::kSmemBytes, stream>>>(args, tk, tv);
+  prefill_kernel<D, BS, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(args, tk, tv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                           int d, int bs, cudaStream_t stream) {
+                           int d, int bs, bool f8v4, cudaStream_t stream) {
   const int64_t gx = static_cast<int64_t>(a.n_qblocks) +
                      (a.skip_single ? 0 : static_cast<int64_t>(a.num_splits - 1) * a.num_seqs);
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.hk), 1);
-#define PAQ8_PREFILL_CASE(DD, BB) \
-  if (d == DD && bs == BB) return launch_prefill_t<DD, BB>(a, tk, tv, grid, stream);
+#define PAQ8_PREFILL_CASE(DD, BB)                                                   \
+  if (d == DD && bs == BB)                                                          \
+    return f8v4 ? launch_prefill_t<DD, BB, true>(a, tk, tv, grid, stream)           \
+                : launch_prefill_t<DD, BB, false>(a, tk, tv, grid, stream);
   PAQ8_PREFILL_CASE(64, 16)
   PAQ8_PREFILL_CASE(64, 32)
   PAQ8_PREFILL_CASE(128, 16)

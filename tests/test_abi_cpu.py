@@ -256,10 +256,10 @@ def test_f8v4_entries_reject_bad_arguments(lib):
     # no v_zero
     bad = base[:2] + [base[3], base[4], None] + base[5:]
     assert lib.pa_paged_attention_f8v4(*bad) == _lib.Status.INVALID_ARG
-    # multi-token rows are not read in this format
-    multi = f8(mq=4)
-    call = multi[:2] + [multi[3], multi[4], ctypes.c_void_p(16)] + multi[5:]
-    assert lib.pa_paged_attention_f8v4(*call) == _lib.Status.UNSUPPORTED
+    # the same visibility checks as _ex: a window is causal only
+    bad = f8(window=16, flags=_lib.ATTN_NON_CAUSAL)
+    call = bad[:2] + [bad[3], bad[4], ctypes.c_void_p(16)] + bad[5:]
+    assert lib.pa_paged_attention_f8v4(*call) == _lib.Status.INVALID_ARG
     # the store: a null zero array, an odd row stride
     st = _store_args()
     store = st[:8] + [st[8], st[10], st[11], ctypes.c_void_p(16)] + st[12:]

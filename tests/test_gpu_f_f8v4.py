@@ -2,8 +2,10 @@
 values with one fp16 scale and zero per key -- against the CPU oracle: the
 store bit for bit (codes, nibbles, scales, zeros and placement, for tokens
 that share a nibble byte within one call and for tokens whose byte mate is
-already in the cache), then decode attention over that cache element by
-element, split and unsplit, with sinks and a sliding window."""
+already in the cache), then attention over that cache element by element --
+decode rows (the decode kernel of the format) and prefill chunks and rows of
+16 q heads per kv head (the generic kernel in the format), split and
+unsplit, with sinks, a sliding window and the non-causal prefix pass."""
 import math
 
 import numpy as np
@@ -27,6 +29,20 @@ SPECS = {
                        decode_lens=(1, 300)),
     "long": inputs.Spec("f8_long", 504, hq=32, hk=8, d=128, bs=32,
                         fixed_decode_lens=(3000, 2111, 17), k_bias_std=SQRT2, num_splits=16),
+    # prefill chunks (the generic kernel in this format) beside decode rows
+    "prefill": inputs.Spec("f8_prefill", 506, hq=32, hk=8, d=128, bs=16, n_prefill=3,
+                           prefill_qlen=150, prefix_lens=(0, 400), n_decode=3,
+                           decode_lens=(50, 700), k_bias_std=SQRT2),
+    "prefill_d256": inputs.Spec("f8_prefill_d256", 507, hq=16, hk=4, d=256, bs=32, n_prefill=2,
+                                prefill_qlen=70, prefix_lens=(0, 200), n_decode=2,
+                                decode_lens=(30, 300)),
+    "prefill_d64": inputs.Spec("f8_prefill_d64", 508, hq=8, hk=2, d=64, bs=16, n_prefill=2,
+                               prefill_qlen=100, prefix_lens=(0, 150), n_decode=2,
+                               decode_lens=(1, 200)),
+    # 16 q heads per kv head: every row, decode rows included, in the generic kernel
+    "wide": inputs.Spec("f8_wide", 509, hq=32, hk=2, d=128, bs=16, n_prefill=2,
+                        prefill_qlen=40, prefix_lens=(0, 300), n_decode=4,
+                        decode_lens=(20, 900)),
 }
 
 
@@ -65,7 +81,7 @@ class F8State:
         np.testing.assert_array_equal(self.vs.cpu().numpy().view(np.uint16), self.ovs)
         np.testing.assert_array_equal(self.vz.cpu().numpy().view(np.uint16), self.ovz)
 
-    def gpu(self, num_splits=0, sinks=None, window=0):
+    def gpu(self, num_splits=0, sinks=None, window=0, causal=True):
         w = self.w
         ws = torch.zeros(_lib.workspace_size(w.num_seqs, w.spec.hq, w.spec.d, num_splits),
                          dtype=torch.uint8, device=self.device)
@@ -73,18 +89,19 @@ class F8State:
         lse = torch.full((w.num_tokens, w.spec.hq), float("nan"), device=self.device)
         sk = None if sinks is None else torch.from_numpy(sinks).to(self.device)
         _lib.paged_attention_f8v4(self.q, self.kc, self.vc, self.vs, self.vz, self.cu,
-                                  self.seq_lens, self.bt, 1, w.max_seq_len, w.softmax_scale,
-                                  num_splits=num_splits, out=out, lse=lse, workspace=ws,
-                                  sinks=sk, sliding_window=window)
+                                  self.seq_lens, self.bt, w.max_query_len, w.max_seq_len,
+                                  w.softmax_scale, num_splits=num_splits, out=out, lse=lse,
+                                  workspace=ws, sinks=sk, sliding_window=window, causal=causal)
         assert _lib.check_status(ws) == 0
         return out, lse
 
-    def oracle(self, rows, sinks=None, window=0):
+    def oracle(self, rows, sinks=None, window=0, causal=True):
         w = self.w
         return oracle.paged_attention(inputs.bf16_bits(w.q), self.okc, None, self.ovc, self.ovs,
                                       w.cu_seqlens_q.numpy(), w.seq_lens.numpy(),
                                       w.block_table.numpy(), w.softmax_scale, rows=rows,
-                                      sinks=sinks, window=window, v_zero=self.ovz)
+                                      sinks=sinks, window=window, causal=causal,
+                                      v_zero=self.ovz)
 
 
 _cache = {}
@@ -113,7 +130,7 @@ def test_f8v4_store_keeps_byte_mates_from_earlier_calls(cuda_device):
 
 
 @pytest.mark.parametrize("name", sorted(SPECS))
-def test_f8v4_decode_attention_matches_oracle(name, cuda_device):
+def test_f8v4_attention_matches_oracle(name, cuda_device):
     g = _state(name, cuda_device)
     rows = H.owned_rows(g.w)
     ref_out, ref_lse = g.oracle(rows)
@@ -133,10 +150,14 @@ def test_f8v4_sinks_and_window(window, sink, cuda_device):
         H.compare(out, lse, ref_out, ref_lse, rows, label=f"f8v4 window={window} sink={sink}")
 
 
-def test_f8v4_rejects_multi_token_rows(cuda_device):
-    g = _state("decode", cuda_device)
-    w = g.w
-    with pytest.raises(_lib.PagedAttentionError) as e:
-        _lib.paged_attention_f8v4(g.q, g.kc, g.vc, g.vs, g.vz, g.cu, g.seq_lens, g.bt, 2,
-                                  w.max_seq_len)
-    assert e.value.status == _lib.Status.UNSUPPORTED
+@pytest.mark.parametrize("window,sink,causal", [(60, 1.0, True), (0, None, False),
+                                                (0, -1.0, False), (500, None, True)])
+def test_f8v4_prefill_options(window, sink, causal, cuda_device):
+    g = _state("prefill", cuda_device)
+    rows = H.owned_rows(g.w)
+    sinks = None if sink is None else np.full(g.w.spec.hq, sink, np.float32)
+    ref_out, ref_lse = g.oracle(rows, sinks=sinks, window=window, causal=causal)
+    for ns in (1, 4):
+        out, lse = g.gpu(num_splits=ns, sinks=sinks, window=window, causal=causal)
+        H.compare(out, lse, ref_out, ref_lse, rows,
+                  label=f"f8v4 prefill window={window} sink={sink} causal={causal} splits={ns}")
