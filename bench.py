@@ -413,8 +413,7 @@ def f8v4_measure(w: inputs.Workload, device, flops=None, reps: int = 20):
         res.update(peak=hbm_peak, frac=round(gbs / hbm_peak, 4))
     else:
         tf = flops / (ms * 1e-3) * 1e-12
-        res.update(flops=flops, tflops=round(tf, 2), peak=tc_peak, frac=round(tf / tc_peak, 4),
-                   kernel="generic mma.sync kernel (the tcgen05 kernel reads the q8 format)")
+        res.update(flops=flops, tflops=round(tf, 2), peak=tc_peak, frac=round(tf / tc_peak, 4))
     return res
 
 

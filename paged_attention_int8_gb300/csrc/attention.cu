@@ -12,8 +12,8 @@
 //                      Hq/Hk > 8;
 //  * reduce_kernel  -- merges the segment triples of split rows by
 //                      log-sum-exp (the pages' reduce_segments step).
-// Over the fp8-key / 4-bit-value format the decode rows take
-// decode_f8v4_kernel and every other row the generic kernel, in that format.
+// Over the fp8-key / 4-bit-value format the same dispatch runs the kernels'
+// instantiations for that format (decode_f8v4_kernel for the decode rows).
 // A batch that holds only decode rows (max_query_len == 1) launches no
 // prefill kernel; both kernels exit at once for rows that are not theirs.
 #include <algorithm>
@@ -29,7 +29,7 @@ cudaError_t launch_decode(const AttnArgs &a, const CUtensorMap &tk, const CUtens
 cudaError_t launch_prefill(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                            int d, int bs, bool f8v4, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                              int d, int bs, cudaStream_t stream);
+                              int d, int bs, bool f8v4, cudaStream_t stream);
 cudaError_t launch_decode_f8v4(const AttnArgs &a, int d, int bs, cudaStream_t stream);
 bool prefill_tc_supported(int d);
 int prefill_tc_rows();
@@ -223,12 +223,12 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   const int64_t pages = static_cast<int64_t>(L.num_blocks) * L.hk;
   CUtensorMap tk = {}, tv = {};
   const int krow = L.d >= 128 ? 128 : L.d;
-  // the fp8 / 4-bit decode kernel copies its pages with cp.async only
-  if (!L.f8v4 &&
-      (!encode_map(&tk, L.k_cache, pages * L.bs, L.d, krow, L.bs,
-                   krow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
-       !encode_map(&tv, L.v_cache, pages * L.d, L.bs, L.bs, L.d,
-                   L.bs == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE)))
+  // K pages have one [bs][D] byte shape in both formats; the fp8 / 4-bit
+  // format's V pages are copied whole (bulk copies or cp.async), with no map
+  if (!encode_map(&tk, L.k_cache, pages * L.bs, L.d, krow, L.bs,
+                  krow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
+      (!L.f8v4 && !encode_map(&tv, L.v_cache, pages * L.d, L.bs, L.bs, L.d,
+                              L.bs == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE)))
     return cudaErrorInvalidValue;
 
   // keys a single-token row sees at most: the hint, or the window plus the
@@ -251,8 +251,10 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
   }
   // tcgen05 prefill for multi-token sequences when the decode kernel takes the
   // single-token ones; the mma.sync kernel otherwise (D = 256, Hq/Hk > 8)
-  // (the fp8 / 4-bit format takes the generic kernel for multi-token rows)
-  const bool use_tc = use_decode && prefill_tc_supported(L.d) && !L.f8v4;
+  const bool use_tc = use_decode && prefill_tc_supported(L.d);
+  auto decode = [&](cudaStream_t s) {
+    return L.f8v4 ? launch_decode_f8v4(a, L.d, L.bs, s) : launch_decode(a, tk, tv, L.d, L.bs, s);
+  };
   const bool fork = L.side_stream_ok && use_decode && use_prefill && use_tc;
   if (fork) {
     // mixed batch: the prefill kernel on the side stream, forked from and
@@ -266,15 +268,12 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     p.block_q = prefill_tc_rows() / a.qpk;
     p.n_qblocks = L.num_tokens / p.block_q + L.num_seqs;
     p.skip_single = 1;
-    if ((e = launch_prefill_tc(p, tk, tv, L.d, L.bs, ss->s)) != cudaSuccess) return e;
-    if ((e = launch_decode(a, tk, tv, L.d, L.bs, stream)) != cudaSuccess) return e;
+    if ((e = launch_prefill_tc(p, tk, tv, L.d, L.bs, L.f8v4, ss->s)) != cudaSuccess) return e;
+    if ((e = decode(stream)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(stream, ss->join, 0)) != cudaSuccess) return e;
-  } else if (use_decode && L.f8v4) {
-    cudaError_t e = launch_decode_f8v4(a, L.d, L.bs, stream);
-    if (e != cudaSuccess) return e;
   } else if (use_decode) {
-    cudaError_t e = launch_decode(a, tk, tv, L.d, L.bs, stream);
+    cudaError_t e = decode(stream);
     if (e != cudaSuccess) return e;
   }
   if (use_prefill && use_tc) {
@@ -283,7 +282,7 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
       p.block_q = prefill_tc_rows() / a.qpk;
       p.n_qblocks = L.num_tokens / p.block_q + L.num_seqs;
       p.skip_single = 1;
-      cudaError_t e = launch_prefill_tc(p, tk, tv, L.d, L.bs, stream);
+      cudaError_t e = launch_prefill_tc(p, tk, tv, L.d, L.bs, L.f8v4, stream);
       if (e != cudaSuccess) return e;
     }
   } else if (use_prefill) {

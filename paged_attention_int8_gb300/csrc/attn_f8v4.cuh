@@ -119,6 +119,74 @@ __device__ __forceinline__ void produce_f8v4(const AttnArgs &a, uint32_t smem_ba
   }
 }
 
+// The producer of the tcgen05 prefill kernel in this format: the same walk
+// as produce_tiles, per page one 2-D TMA box for the K rows (the q8 K map:
+// the pages have the same [BS][D] byte shape) and bulk copies of the V
+// nibble page and of the scales and zeros, all completing on the stage's
+// full barrier (D <= 128: one K box per page).
+template <class L, int BS, int NST>
+__device__ __forceinline__ void produce_tiles_f8v4_tma(const AttnArgs &a, const CUtensorMap *tmap_k,
+                                                       uint32_t smem_base, uint32_t bar_full,
+                                                       uint32_t bar_empty, int seq, int h,
+                                                       int tile_lo, int n_iter, int kv_begin,
+                                                       int kv_end, int lane) {
+  constexpr int D = L::kD;
+  static_assert(D <= 128, "one K box per page");
+  constexpr uint32_t kKPage = BS * L::kRowBytes;
+  constexpr uint32_t kVPage = D * BS / 2;
+  constexpr uint32_t kPageTx = BS * D + kVPage + 4 * BS;
+  const int n_pages = (kv_end + BS - 1) / BS;
+  const int32_t *bt_row = a.block_table + static_cast<int64_t>(seq) * a.bt_stride;
+  const uint8_t *vc = reinterpret_cast<const uint8_t *>(a.v_cache);
+  int page_base = -(1 << 30);
+  int my_blk = -1;
+  for (int it = 0; it < n_iter; ++it) {
+    const int stage = it % NST;
+    if (it >= NST) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(bar_empty + 8 * stage, ((it / NST) - 1) & 1, a.wait_limit_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
+        return;
+      }
+    }
+    const int lp0 = (tile_lo + it) * L::kPages;
+    if (lp0 - page_base >= 32) {
+      page_base = lp0;
+      const int lp = page_base + lane;
+      my_blk = -1;
+      if (lp < n_pages && (lp + 1) * BS > kv_begin) {
+        const int b = lp < a.bt_stride ? bt_row[lp] : -1;
+        if (b >= 0 && b < a.num_blocks) my_blk = b;
+        else flag_status(a.status, PA_DEV_BAD_BLOCK);
+      }
+    }
+    int blk[L::kPages];
+    int nvalid = 0;
+#pragma unroll
+    for (int p = 0; p < L::kPages; ++p) {
+      blk[p] = __shfl_sync(0xffffffffu, my_blk, lp0 + p - page_base);
+      nvalid += blk[p] >= 0;
+    }
+    if (lane == 0) {
+      const uint32_t full = bar_full + 8 * stage;
+      const uint32_t st = smem_base + stage * L::kBytes;
+      mbar_arrive_expect_tx(full, nvalid * kPageTx);
+#pragma unroll
+      for (int p = 0; p < L::kPages; ++p) {
+        if (blk[p] < 0) continue;
+        const int64_t page = static_cast<int64_t>(blk[p]) * a.hk + h;
+        tma_load_2d(st + p * kKPage, tmap_k, 0, static_cast<int32_t>(page * BS), full);
+        bulk_load(st + L::kVOff + p * kVPage, vc + page * kVPage, kVPage, full);
+        bulk_load(st + L::kVsOff + p * (BS * 2), a.v_scale + page * BS, BS * 2, full);
+        bulk_load(st + L::kVzOff + p * (BS * 2), a.v_zero + page * BS, BS * 2, full);
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // Two e4m3 values (byte 0 -> low half) -> fp16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t v16) {
   uint32_t d;

@@ -54,20 +54,29 @@
 // execute in issue order, so the single S/P buffer is never overwritten
 // early; the commit of QK(j) also implies PV(j-1) is done, so the softmax may
 // rescale O as soon as S(j) is ready.
+//
+// The same kernel reads the fp8-key / 4-bit-value format (F8): the K
+// dequant warps turn e4m3 keys into fp16 exactly (one part, so QK^T is one
+// MMA pass with no K_lo), the V dequant warps form V' = idx * scale + zero
+// per key, and the producer stages the K rows by TMA and the nibble pages,
+// scales and zeros by bulk copies.
+#include <type_traits>
+
 #include "attn_common.cuh"
+#include "attn_f8v4.cuh"
 #include "tcgen05.cuh"
 #include "launch.h"
 
 namespace paq8 {
 
-template <int D, int BS>
+template <int D, int BS, bool F8>
 struct TcCfg {
   static constexpr int kTile = 64;
   static constexpr int kHalves = 2;
   static constexpr int kRows = 128 * kHalves;
   static constexpr int kSt = 4;  // int8 staging stages (TMA)
   static constexpr int kWarps = 16;
-  using L = StageLayout<D, BS, kTile>;
+  using L = std::conditional_t<F8, StageF8V4<D, BS, kTile>, StageLayout<D, BS, kTile>>;
   static constexpr int kKBytes = kTile * D * 2;  // one of K_hi, K_lo: [D/64][64 keys][128 B]
   static constexpr int kKSlot = 2 * kKBytes;     // K ring slot: hi then lo
   static constexpr int kVBytes = D * kTile * 2;  // V' ring slot: [D rows][64 keys]
@@ -101,11 +110,11 @@ enum : int {
   kNumBars = 23
 };
 
-template <int D, int BS>
+template <int D, int BS, bool F8>
 __global__ void __launch_bounds__(512, 1)
     prefill_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
-  using C = TcCfg<D, BS>;
+  using C = TcCfg<D, BS, F8>;
   using L = typename C::L;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -183,10 +192,15 @@ __global__ void __launch_bounds__(512, 1)
     // ============================================================ producer
     if (lane == 0) {
       prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
+      if constexpr (!F8) prefetch_tensormap(&tmap_v);
     }
-    produce_tiles<L, BS, C::kSt>(a, &tmap_k, &tmap_v, smem_base, bar(kBarStFull),
-                                 bar(kBarStEmpty), seq, h, t0, nt, kv_begin, kv_end, lane);
+    if constexpr (F8)
+      produce_tiles_f8v4_tma<L, BS, C::kSt>(a, &tmap_k, smem_base, bar(kBarStFull),
+                                            bar(kBarStEmpty), seq, h, t0, nt, kv_begin, kv_end,
+                                            lane);
+    else
+      produce_tiles<L, BS, C::kSt>(a, &tmap_k, &tmap_v, smem_base, bar(kBarStFull),
+                                   bar(kBarStEmpty), seq, h, t0, nt, kv_begin, kv_end, lane);
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     // The whole warp runs this loop (uniform values, no divergence); the
@@ -215,7 +229,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t k_desc = tc::desc_sw128(smem_base + C::kKOff + (j & 1) * C::kKSlot);
       const uint32_t base = tmem + hf * C::kHalfCols;
 #pragma unroll
-      for (int part = 0; part < 2; ++part)
+      for (int part = 0; part < (F8 ? 1 : 2); ++part)  // F8: exact keys, no K_lo part
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = part * C::kKBytes + (ks >> 2) * (64 * 128) + (ks & 3) * 32;
@@ -266,6 +280,23 @@ __global__ void __launch_bounds__(512, 1)
         const int r = t & 63;
         const int c0 = (t >> 6) * (D / 2);
         const bool dead = tail && (key0 + r >= kv_end || key0 + r < kv_begin);
+        if constexpr (F8) {
+          // e4m3 -> fp16 exactly; a row outside the visible keys becomes zeros
+#pragma unroll
+          for (int c = c0; c < c0 + D / 2; c += 16) {
+            const uint4 codes = dead ? make_uint4(0u, 0u, 0u, 0u) : lds128(st + L::k_off(r, c));
+            const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+            uint32_t hw[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              hw[2 * i] = e4m3x2_to_half2(cw[i]);
+              hw[2 * i + 1] = e4m3x2_to_half2(cw[i] >> 16);
+            }
+            const int c16 = c / 8;
+            sts128(kdst + tc::sw128_chunk(r, c16, 64), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+            sts128(kdst + tc::sw128_chunk(r, c16 + 1, 64), make_uint4(hw[4], hw[5], hw[6], hw[7]));
+          }
+        } else {
 #pragma unroll
         for (int c = c0; c < c0 + D / 2; c += 16) {
           const uint4 codes = lds128(st + L::k_off(r, c));
@@ -295,6 +326,7 @@ __global__ void __launch_bounds__(512, 1)
           sts128(kdst + C::kKBytes + tc::sw128_chunk(r, c16 + 1, 64),
                  make_uint4(lw[4], lw[5], lw[6], lw[7]));
         }
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
@@ -315,6 +347,43 @@ __global__ void __launch_bounds__(512, 1)
         } else {
           ch[0] = t;
         }
+        if constexpr (F8) {
+#pragma unroll
+          for (int key = 0; key < C::kTile; key += 16) {  // 16 keys: 8 bytes per channel row
+            // the keys' scales and zeros, fp16 pairs (keys 2i, 2i+1); zero
+            // outside the visible keys (stale bytes may sit there)
+            const uint4 s01 = lds128(st + L::vs_off(key)), s23 = lds128(st + L::vs_off(key + 8));
+            const uint4 z01 = lds128(st + L::vz_off(key)), z23 = lds128(st + L::vz_off(key + 8));
+            uint32_t sc[8] = {s01.x, s01.y, s01.z, s01.w, s23.x, s23.y, s23.z, s23.w};
+            uint32_t zr[8] = {z01.x, z01.y, z01.z, z01.w, z23.x, z23.y, z23.z, z23.w};
+            if (tail) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int k0 = key0 + key + 2 * i;
+                const uint32_t m = (k0 >= kv_end || k0 < kv_begin ? 0u : 0x0000ffffu) |
+                                   (k0 + 1 >= kv_end || k0 + 1 < kv_begin ? 0u : 0xffff0000u);
+                sc[i] &= m;
+                zr[i] &= m;
+              }
+            }
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+              const uint2 nb = lds64(st + L::v_off(ch[rr], key));  // keys key .. key+15
+              const uint32_t nw[4] = {nb.x, nb.x >> 16, nb.y, nb.y >> 16};
+              uint32_t o[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t lo, hi;
+                nibbles4_to_half2(nw[i], lo, hi);  // keys 4i, 4i+1 | 4i+2, 4i+3
+                o[2 * i] = hfma2_u32(lo, sc[2 * i], zr[2 * i]);
+                o[2 * i + 1] = hfma2_u32(hi, sc[2 * i + 1], zr[2 * i + 1]);
+              }
+              sts128(vrow + tc::sw128_chunk(ch[rr], key / 8, D), make_uint4(o[0], o[1], o[2], o[3]));
+              sts128(vrow + tc::sw128_chunk(ch[rr], key / 8 + 1, D),
+                     make_uint4(o[4], o[5], o[6], o[7]));
+            }
+          }
+        } else {
         const int g = ch[0] / 32;
 #pragma unroll
         for (int key = 0; key < C::kTile; key += 16) {  // 16 keys: one 16-byte load
@@ -345,6 +414,7 @@ __global__ void __launch_bounds__(512, 1)
             sts128(vrow + tc::sw128_chunk(ch[rr], key / 8 + 1, D),
                    make_uint4(o[4], o[5], o[6], o[7]));
           }
+        }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -541,18 +611,18 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int D, int BS>
+template <int D, int BS, bool F8>
 static cudaError_t launch_prefill_tc_t(const AttnArgs &a, const CUtensorMap &tk,
                                        const CUtensorMap &tv, cudaStream_t stream) {
-  using C = TcCfg<D, BS>;
+  using C = TcCfg<D, BS, F8>;
   static DeviceOnce configured;
   cudaError_t e = configured.get(nullptr, [](int, int *) {
-    return cudaFuncSetAttribute(prefill_tc_kernel<D, BS>,
+    return cudaFuncSetAttribute(prefill_tc_kernel<D, BS, F8>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.n_qblocks), static_cast<unsigned>(a.hk), 1);
-  prefill_tc_kernel<D, BS><<<grid, C::kWarps * 32, C::kSmem, stream>>>(a, tk, tv);
+  prefill_tc_kernel<D, BS, F8><<<grid, C::kWarps * 32, C::kSmem, stream>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
@@ -562,9 +632,11 @@ bool prefill_tc_supported(int d) { return d == 64 || d == 128; }
 int prefill_tc_rows() { return 256; }
 
 cudaError_t launch_prefill_tc(const AttnArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                              int d, int bs, cudaStream_t stream) {
-#define PAQ8_TC_CASE(DD, BB) \
-  if (d == DD && bs == BB) return launch_prefill_tc_t<DD, BB>(a, tk, tv, stream);
+                              int d, int bs, bool f8v4, cudaStream_t stream) {
+#define PAQ8_TC_CASE(DD, BB)                                               \
+  if (d == DD && bs == BB)                                                 \
+    return f8v4 ? launch_prefill_tc_t<DD, BB, true>(a, tk, tv, stream)     \
+                : launch_prefill_tc_t<DD, BB, false>(a, tk, tv, stream);
   PAQ8_TC_CASE(64, 16)
   PAQ8_TC_CASE(64, 32)
   PAQ8_TC_CASE(128, 16)
