@@ -374,6 +374,27 @@ def f8v4_measure(w: inputs.Workload, device, flops=None, reps: int = 20):
     for a in range(0, k.shape[0], chunk):
         _lib.kv_store_f8v4(k[a:a + chunk].to(device), v[a:a + chunk].to(device),
                            sl[a:a + chunk].to(device), kc, vc, vs, vz)
+    # the store alone on the population batch (the prefix rows, stored again:
+    # idempotent): bf16 K/V read, codes, nibbles, scales and zeros written
+    pk, pv, ps = (w.prefix_key.to(device), w.prefix_value.to(device),
+                  w.prefix_slots.to(device))
+    n = int(ps.shape[0])
+    store = None
+    if n:
+        for _ in range(3):
+            _lib.kv_store_f8v4(pk, pv, ps, kc, vc, vs, vz)
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for a, b in sev:
+            a.record()
+            _lib.kv_store_f8v4(pk, pv, ps, kc, vc, vs, vz)
+            b.record()
+        torch.cuda.synchronize()
+        sms = statistics.mean(a.elapsed_time(b) for a, b in sev)
+        sbytes = n * s.hk * (4 * s.d + s.d + s.d // 2 + 4) + 8 * n
+        store = {"tokens": n, "bytes": sbytes, "ms": round(sms, 5),
+                 "achieved_gbs": round(sbytes / (sms * 1e-3) * 1e-9, 2)}
+    del pk, pv, ps
     q, cu = w.q.to(device), w.cu_seqlens_q.to(device)
     seq_lens, bt = w.seq_lens.to(device), w.block_table.to(device)
     ns = _lib.auto_num_splits(w.num_seqs, s.hk, w.max_query_len, w.max_seq_len)
@@ -406,9 +427,12 @@ def f8v4_measure(w: inputs.Workload, device, flops=None, reps: int = 20):
     hbm_peak, tc_peak, _ = load_peaks()
     gbs = nbytes / (ms * 1e-3) * 1e-9
     del kc, vc, vs, vz, ws
+    if store is not None:
+        store["peak"] = hbm_peak
+        store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
     res = {"format": "fp8 e4m3 keys, 4-bit values with fp16 scale and zero per key",
            "bytes": nbytes, "ms": round(ms, 5), "achieved_gbs": round(gbs, 2),
-           "num_splits": ns}
+           "num_splits": ns, "kv_store_f8v4": store}
     if flops is None:
         res.update(peak=hbm_peak, frac=round(gbs / hbm_peak, 4))
     else:
