@@ -26,12 +26,88 @@
 namespace paq8 {
 
 constexpr int kF8v4Warps = 8;
+constexpr int kNibStride = 34;  // nibble words per row of the staging area: 32 lanes + 2 outside mates
 
 // two fp32 -> e4m3x2 (x0 in byte 0), round to nearest even, saturating
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float x0, float x1) {
   uint16_t d;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(x1), "f"(x0));
   return d;
+}
+
+// The 4-bit code of x in a row with minimum lo and step s (rs = 1/s):
+// round_half_away((x - lo) / s) of the IEEE quotient (the product with 1/s,
+// exact near ties), clamped to [0, 15].
+// (the rare near-tie decision is a call, so that the unrolled code of a row
+// stays small)
+__device__ __noinline__ int32_t v4_tie(float v, float s, float rs) { return tie_code(v, s, rs); }
+
+__device__ __forceinline__ uint32_t v4_code(float x, float lo, float s, float rs) {
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kFar = 0.5f - 0x1p-15f;
+  const float v = __fsub_rn(x, lo);
+  const float q = __fmul_rn(v, rs);
+  const float t = __fadd_rn(q, kShift);
+  int32_t code = static_cast<int32_t>(__float_as_uint(t) & 0xffu);
+  if (fabsf(__fsub_rn(q, __fsub_rn(t, kShift))) >= kFar) code = v4_tie(v, s, rs);
+  return static_cast<uint32_t>(min(max(code, 0), 15));
+}
+
+// The step of a row from its extremes: max((hi - lo) / 15, 1e-8).
+__device__ __forceinline__ float v4_step(float lo, float hi) {
+  const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  return s < 1e-8f ? 1e-8f : s;
+}
+
+// The nibbles of value row `row` (one token, one kv head), computed by the
+// whole warp (lane l: channels l * D/32 ...) and written as D / 8 words to
+// col[0], col[stride], ... (shared memory): the nibbles of a token just
+// outside the warp's 32 whose byte mate is a lane of this warp.  The same
+// arithmetic as a lane's own row, so the same codes.
+template <int D>
+__device__ __forceinline__ void v4_row_by_warp(const uint16_t *__restrict__ row, int lane,
+                                               uint32_t *col, int stride) {
+  constexpr int C = D / 32;  // channels per lane
+  float x[C];
+  if constexpr (C == 2) {
+    const uint32_t a = *reinterpret_cast<const uint32_t *>(row + lane * C);
+    x[0] = bf16_lo(a);
+    x[1] = bf16_hi(a);
+  } else if constexpr (C == 4) {
+    const uint2 a = *reinterpret_cast<const uint2 *>(row + lane * C);
+    x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+  } else {
+    const uint4 a = *reinterpret_cast<const uint4 *>(row + lane * C);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_lo(w[i]);
+      x[2 * i + 1] = bf16_hi(w[i]);
+    }
+  }
+  float lo = x[0], hi = x[0];
+#pragma unroll
+  for (int i = 1; i < C; ++i) {
+    lo = fminf(lo, x[i]);
+    hi = fmaxf(hi, x[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  const float s = v4_step(lo, hi);
+  const float rs = __frcp_rn(s);
+  uint32_t chunk = 0u;  // 4C bits: this lane's channels
+#pragma unroll
+  for (int i = 0; i < C; ++i) chunk |= v4_code(x[i], lo, s, rs) << (4 * i);
+  // lane l's chunk is the (l % (8 / C))-th C/2-byte piece of word l / (8 / C)
+  constexpr int kLanesPerWord = 8 / C;
+  uint8_t *dst = reinterpret_cast<uint8_t *>(col + (lane / kLanesPerWord) * stride) +
+                 (lane % kLanesPerWord) * (C / 2);
+  if constexpr (C == 2) *dst = static_cast<uint8_t>(chunk);
+  else if constexpr (C == 4) *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(chunk);
+  else *reinterpret_cast<uint32_t *>(dst) = chunk;
 }
 
 template <int D>
@@ -42,6 +118,7 @@ __global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
     uint16_t *__restrict__ v_scale, uint16_t *__restrict__ v_zero, int64_t num_slots,
     int32_t block_size, uint32_t *status) {
   constexpr int W = D / 8;  // nibble words of a row (8 channels each)
+  __shared__ uint32_t nib_s[kF8v4Warps][W][kNibStride];
   const int lane = threadIdx.x & 31;
   const int n_tblocks = (num_tokens + 31) / 32;
   const int64_t units = static_cast<int64_t>(n_tblocks) * hk;
@@ -79,10 +156,11 @@ __global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
       }
     }
 
-    // ---- values: 4-bit codes with the row's scale and zero
-    uint32_t nib[W];
-#pragma unroll
-    for (int i = 0; i < W; ++i) nib[i] = 0u;
+    // ---- values: 4-bit codes with the row's scale and zero.  The nibble
+    // words go through shared memory (word i of lane l at nib[i][l]), so that
+    // the loops below stay rolled (small code) and a byte mate's words are a
+    // plain load.
+    uint32_t(*nib)[kNibStride] = nib_s[threadIdx.x >> 5];
     if (active) {
       const uint16_t *vs = value + n * value_stride + static_cast<int64_t>(h) * D;
       float lo = INFINITY, hi = -INFINITY;
@@ -96,29 +174,17 @@ __global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
           hi = fmax3(hi, bf16_lo(w[i]), bf16_hi(w[i]));
         }
       }
-      float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-      if (s < 1e-8f) s = 1e-8f;
+      const float s = v4_step(lo, hi);
       const float rs = __frcp_rn(s);
-      constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-      constexpr float kFar = 0.5f - 0x1p-15f;
-#pragma unroll
+#pragma unroll 2
       for (int c = 0; c < D; c += 8) {
         const uint4 a = *reinterpret_cast<const uint4 *>(vs + c);
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
         uint32_t word = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float x = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
-          // (x - lo) / s as in kv_store: the product with 1/s, exact near ties
-          const float v = __fsub_rn(x, lo);
-          const float q = __fmul_rn(v, rs);
-          const float t = __fadd_rn(q, kShift);
-          int32_t code = static_cast<int32_t>(__float_as_uint(t) & 0xffu);
-          if (fabsf(__fsub_rn(q, __fsub_rn(t, kShift))) >= kFar) code = tie_code(v, s, rs);
-          code = min(max(code, 0), 15);
-          word |= static_cast<uint32_t>(code) << (4 * i);
-        }
-        nib[c / 8] = word;
+        for (int i = 0; i < 8; ++i)
+          word |= v4_code((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]), lo, s, rs) << (4 * i);
+        nib[c / 8][lane] = word;
       }
       v_scale[page * block_size + off] = __half_as_ushort(__float2half_rn(s));
       v_zero[page * block_size + off] = __half_as_ushort(__float2half_rn(lo));
@@ -127,40 +193,64 @@ __global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
     // ---- nibble bytes: pair the two tokens of a byte when both are here
     const uint32_t pair_mask = __match_any_sync(0xffffffffu, active ? (slot >> 1) : -1 - lane);
     const bool paired = __popc(pair_mask) == 2;
-    const int mate = paired ? __ffs(pair_mask & ~(1u << lane)) - 1 : lane;
-    uint32_t mate_nib[W];
+    int mate = paired ? __ffs(pair_mask & ~(1u << lane)) - 1 : lane;
+    // A stretch of consecutive slots that crosses the warp's first or last
+    // token (a chunk starting mid-pair) leaves lane 0 or 31 without its mate
+    // in the warp, while the mate is the token just outside: the warp then
+    // computes that token's nibbles into column 32 + side, and the lane
+    // writes the whole byte -- as does the warp that owns the mate, with the
+    // same value.
+    bool outer = false;
 #pragma unroll
-    for (int i = 0; i < W; ++i) mate_nib[i] = __shfl_sync(0xffffffffu, nib[i], mate);
-    if (!active) continue;
-    uint8_t *vrow = v_cache + page * D * (block_size / 2) + off / 2;  // channel 0's byte
-    // (loops fully unrolled: the nibble words stay in registers)
-    if (paired) {
-      if (off & 1) continue;  // the even-offset token writes the byte
-#pragma unroll
-      for (int i = 0; i < W; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t lo4 = (nib[i] >> (4 * j)) & 0xfu;
-          const uint32_t hi4 = (mate_nib[i] >> (4 * j)) & 0xfu;
-          vrow[static_cast<int64_t>(8 * i + j) * (block_size / 2)] =
-              static_cast<uint8_t>(lo4 | (hi4 << 4));
-        }
-    } else {
-#pragma unroll
-      for (int i = 0; i < W; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t v4 = (nib[i] >> (4 * j)) & 0xfu;
-          uint8_t *byte = vrow + static_cast<int64_t>(8 * i + j) * (block_size / 2);
-          unsigned int *word = reinterpret_cast<unsigned int *>(
-              reinterpret_cast<uintptr_t>(byte) & ~static_cast<uintptr_t>(3));
-          const uint32_t shift =
-              8u * static_cast<uint32_t>(reinterpret_cast<uintptr_t>(byte) & 3u) +
-              4u * static_cast<uint32_t>(off & 1);
-          atomicAnd(word, ~(0xfu << shift));
-          atomicOr(word, v4 << shift);
-        }
+    for (int side = 0; side < 2; ++side) {
+      const int src = side == 0 ? 0 : 31;
+      const int64_t nm = n + (side == 0 ? -1 : 1);  // the mate token (lane src)
+      bool want = false;
+      if (lane == src && active && !paired && ((off & 1) != 0) == (side == 0) && nm >= 0 &&
+          nm < num_tokens)
+        want = slot_mapping[nm] == (side == 0 ? slot - 1 : slot + 1);
+      if (!__shfl_sync(0xffffffffu, want, src)) continue;  // warp-uniform
+      const int64_t row_m = __shfl_sync(0xffffffffu, nm, src);
+      v4_row_by_warp<D>(value + row_m * value_stride + static_cast<int64_t>(h) * D, lane,
+                        &nib[0][32 + side], kNibStride);
+      if (lane == src) {
+        outer = true;
+        mate = 32 + side;
+      }
     }
+    __syncwarp();  // every lane's words (and the outer columns) are in place
+    if (active && (outer || paired)) {
+      // the even-offset token of an in-warp pair writes the byte; an edge
+      // lane writes it with the outside mate's nibbles
+      if (outer || !(off & 1)) {
+        const bool odd = off & 1;  // the low nibble is the even-offset token's
+        uint8_t *vrow = v_cache + page * D * (block_size / 2) + off / 2;  // channel 0's byte
+#pragma unroll 1
+        for (int i = 0; i < W; ++i) {
+          const uint32_t own = nib[i][lane], other = nib[i][mate];
+          const uint32_t lo_w = odd ? other : own, hi_w = odd ? own : other;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            vrow[static_cast<int64_t>(8 * i + j) * (block_size / 2)] = static_cast<uint8_t>(
+                ((lo_w >> (4 * j)) & 0xfu) | (((hi_w >> (4 * j)) & 0xfu) << 4));
+        }
+      }
+    } else if (active) {
+      // the byte mate is not in this call: update this token's nibbles alone
+      uint8_t *vrow = v_cache + page * D * (block_size / 2) + off / 2;
+#pragma unroll 1
+      for (int c = 0; c < D; ++c) {
+        const uint32_t v4 = (nib[c / 8][lane] >> (4 * (c % 8))) & 0xfu;
+        uint8_t *byte = vrow + static_cast<int64_t>(c) * (block_size / 2);
+        unsigned int *word = reinterpret_cast<unsigned int *>(
+            reinterpret_cast<uintptr_t>(byte) & ~static_cast<uintptr_t>(3));
+        const uint32_t shift = 8u * static_cast<uint32_t>(reinterpret_cast<uintptr_t>(byte) & 3u) +
+                               4u * static_cast<uint32_t>(off & 1);
+        atomicAnd(word, ~(0xfu << shift));
+        atomicOr(word, v4 << shift);
+      }
+    }
+    __syncwarp();  // the words are rewritten for the warp's next unit
   }
 }
 
