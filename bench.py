@@ -296,6 +296,55 @@ def kv_store_measure(r: Runner, reps: int = 20):
             "achieved_gbs": round(nbytes / (ms * 1e-3) * 1e-9, 2)}
 
 
+def norm_rope_measure(r: Runner, reps: int = 20):
+    """kv_store_norm_rope alone on the workload's prefix rows (the cache
+    population batch, stored again): each key row through a weighted RMSNorm
+    and a full rotary embedding (positions = the tokens' places in their
+    sequences, the usual rotary frequencies) before q8, values as kv_store.
+    Algorithmic bytes: bf16 K/V read, codes and scales written, slots and
+    positions read, each token's cos/sin row and the norm weight once."""
+    w = r.w
+    s = w.spec
+    n = int(w.prefix_slots.shape[0])
+    if n == 0:
+        return None
+    L = w.seq_lens.to(torch.int64)
+    ctx = L - w.q_lens.to(torch.int64)
+    pos = torch.cat([torch.arange(int(c), dtype=torch.int64) for c in ctx.tolist()])
+    max_pos = int(ctx.max().item()) if ctx.numel() else 1
+    pairs = s.d // 2
+    inv_freq = 10000.0 ** (-torch.arange(pairs, dtype=torch.float64) / pairs)
+    ang = torch.arange(max(max_pos, 1), dtype=torch.float64)[:, None] * inv_freq[None, :]
+    table = torch.stack([ang.cos(), ang.sin()], -1).to(torch.float32).to(r.device)
+    wt = (torch.rand(s.d, generator=torch.Generator().manual_seed(5)) + 0.5).to(
+        torch.bfloat16).to(r.device)
+    k, v, sl = (w.prefix_key.to(r.device), w.prefix_value.to(r.device),
+                w.prefix_slots.to(r.device))
+    pos = pos.to(r.device)
+
+    def call():
+        _lib.kv_store_norm_rope(k, v, sl, r.kc, r.ks, r.vc, r.vs, positions=pos, norm_weight=wt,
+                                rope=table, status=r.status)
+
+    for _ in range(3):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    assert _lib.check_status(r.status) == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    G = s.d // 32
+    nbytes = n * (s.hk * (4 * s.d + 2 * (s.d + 2 * G)) + 4 * s.d + 16) + 2 * s.d
+    del k, v, sl, pos, table, wt
+    return {"tokens": n, "bytes": nbytes, "ms": round(ms, 5),
+            "achieved_gbs": round(nbytes / (ms * 1e-3) * 1e-9, 2),
+            "rotary_dim": s.d, "norm": True}
+
+
 MERGE_ROWS = 1 << 19  # (token, q head) rows of the merge measurement
 
 
@@ -673,6 +722,14 @@ def run_workload(name, args, device, rank, world, headline: bool):
             store["peak"] = hbm_peak
             store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
         entry["kv_store"] = store
+    if rank == 0 and name == "decode_batch" and not args.no_kv_store:
+        # the fused norm + rotation store on the same population batch
+        nr = norm_rope_measure(r)
+        if nr is not None:
+            hbm_peak_nr, _, _ = load_peaks()
+            nr["peak"] = hbm_peak_nr
+            nr["frac"] = round(nr["achieved_gbs"] / hbm_peak_nr, 4)
+        entry["kv_store_norm_rope"] = nr
     if rank == 0 and name in ("decode_batch", "chunked_prefill") and not args.no_kv_store:
         # the alternative format on the same batch: fewer bytes per key
         f8 = f8v4_measure(w, device, flops=work["flops"] if unit == "TFLOP/s" else None)
