@@ -345,6 +345,62 @@ def norm_rope_measure(r: Runner, reps: int = 20):
             "rotary_dim": s.d, "norm": True}
 
 
+def options_measure(r: Runner, unit: str, reps: int = 20, window: int = 1024):
+    """The attention options on the workload's own batch, timed with CUDA
+    events: for a decode batch a sliding window of `window` keys with a sink
+    logit per q head (algorithmic bytes: the visible keys' K/V codes and
+    scales, q, out, lse, the visible pages' block-table entries, the sinks);
+    for a prefill batch the non-causal prefix pass, every query over all of
+    its sequence's keys (FLOPs: 4 D per (row, key) pair)."""
+    w = r.w
+    s = w.spec
+    G = s.d // 32
+    L = w.seq_lens.to(torch.int64)
+    ql = w.q_lens.to(torch.int64)
+    T = w.num_tokens
+    out = torch.empty_like(r.q)
+    lse = torch.empty((T, s.hq), dtype=torch.float32, device=r.device)
+    ws = torch.zeros_like(r.ws)
+    ns = r.ns_eff
+    if unit == "TFLOP/s":
+        kw = dict(causal=False)
+        flops = 4 * s.d * s.hq * int((ql * L).sum())
+    else:
+        sinks = (torch.rand(s.hq, generator=torch.Generator().manual_seed(9)) * 4.0 - 1.0).to(
+            r.device)
+        kw = dict(sinks=sinks, sliding_window=window)
+        ns = 0  # the library's automatic split count, sized for the window
+        vis = torch.clamp(L, max=window)
+        nbytes = (int(vis.sum()) * s.hk * 2 * (s.d + 2 * G) + T * s.hq * (4 * s.d + 4)
+                  + int(((vis + s.bs - 1) // s.bs + 1).sum()) * 4 + (2 * w.num_seqs + 1) * 4
+                  + s.hq * 4)
+
+    def call():
+        _lib.paged_attention(r.q, r.kc, r.ks, r.vc, r.vs, r.cu, r.seq_lens, r.bt, w.max_query_len,
+                             w.max_seq_len, w.softmax_scale, num_splits=ns, out=out,
+                             lse=lse, workspace=ws, **kw)
+
+    for _ in range(3):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    assert _lib.check_status(ws) == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    hbm_peak, tc_peak, _ = load_peaks()
+    if unit == "TFLOP/s":
+        tf = flops / (ms * 1e-3) * 1e-12
+        return {"option": "non-causal prefix pass", "flops": flops, "ms": round(ms, 5),
+                "tflops": round(tf, 2), "peak": tc_peak, "frac": round(tf / tc_peak, 4)}
+    gbs = nbytes / (ms * 1e-3) * 1e-9
+    return {"option": f"sliding window {window} + sinks", "bytes": nbytes, "ms": round(ms, 5),
+            "achieved_gbs": round(gbs, 2), "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4)}
+
+
 MERGE_ROWS = 1 << 19  # (token, q head) rows of the merge measurement
 
 
@@ -722,6 +778,8 @@ def run_workload(name, args, device, rank, world, headline: bool):
             store["peak"] = hbm_peak
             store["frac"] = round(store["achieved_gbs"] / hbm_peak, 4)
         entry["kv_store"] = store
+    if rank == 0 and name in ("decode_batch", "chunked_prefill") and not args.no_kv_store:
+        entry["options"] = options_measure(r, unit)
     if rank == 0 and name == "decode_batch" and not args.no_kv_store:
         # the fused norm + rotation store on the same population batch
         nr = norm_rope_measure(r)
