@@ -156,19 +156,13 @@ int32_t auto_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_quer
   return ns < 1 ? 1 : (ns > kMaxSplits ? kMaxSplits : ns);
 }
 
-// A high-priority side stream per device (and fork / join events) on which
-// the tcgen05 prefill kernel runs beside the decode kernel of a mixed batch:
-// one is bound by the tensor cores, the other by HBM.  Created once; calls
-// from several host threads share it (correct, but their prefill kernels
-// then queue behind one another).
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
+// The side stream (launch.h) on which the tcgen05 prefill kernel runs beside
+// the decode kernel of a mixed batch (one is bound by the tensor cores, the
+// other by HBM), and the fused store's values beside its keys.
 static std::mutex g_side_mu;
 static SideStream g_side[64];
 
-static cudaError_t side_stream(SideStream **out) {
+cudaError_t side_stream(SideStream **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -35,19 +35,6 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// copies into shared memory that complete asynchronously (per thread)
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 constexpr int kStoreWarps = 8;
 constexpr int kStoreStages = 3;
 constexpr int kStoreStageBytes = 32 * 64 + 32 * 8;  // 32 rows of 32 bf16, then 32 slots
@@ -303,7 +290,8 @@ __global__ void __launch_bounds__(32 * kStoreWarps, 4) kv_store_kernel(
 
 // token-block slots of the grid
 template <int D, int BS>
-static cudaError_t store_grid_x(int n_tblocks, unsigned grid_y, unsigned *grid_x) {
+static cudaError_t store_grid_x(int n_tblocks, unsigned grid_y, int32_t blocks_per_sm,
+                                unsigned *grid_x) {
   // blocks of the kernel resident at once on the current device
   static DeviceOnce resident_blocks;
   int res = 0;
@@ -321,13 +309,22 @@ static cudaError_t store_grid_x(int n_tblocks, unsigned grid_y, unsigned *grid_x
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
+  static DeviceOnce sm_count;
+  int sms = 0;
+  e = sm_count.get(&sms, [](int dev, int *v) {
+    return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (e != cudaSuccess) return e;
+  if (blocks_per_sm > 0 && sms > 0 && static_cast<int64_t>(sms) * blocks_per_sm < res)
+    res = sms * blocks_per_sm;
   const unsigned resident = static_cast<unsigned>(res);
   // up to 16 waves: one block per token block (every block starts at once
   // with its own loads); beyond that, one resident set of blocks that walks
   // the token blocks with its loads two steps ahead
   const unsigned want = (resident + grid_y - 1) / grid_y;
   const unsigned n = static_cast<unsigned>(n_tblocks);
-  *grid_x = n <= 16 * want ? n : want;
+  // (a capped grid stays persistent: it shares the SMs with other work)
+  *grid_x = blocks_per_sm == 0 && n <= 16 * want ? n : (n < want ? n : want);
   return cudaSuccess;
 }
 
@@ -337,7 +334,8 @@ static cudaError_t launch_store(const uint16_t *key, int64_t key_stride, const u
                                 uint16_t *k_scale, int8_t *v_cache, uint16_t *v_scale,
                                 int32_t num_blocks, int32_t block_size, uint32_t *status,
                                 int32_t values_only, const int64_t *positions,
-                                int32_t max_position, cudaStream_t stream) {
+                                int32_t max_position, cudaStream_t stream,
+                                int32_t blocks_per_sm) {
   const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
   const dim3 block(32 * kStoreWarps);
   const int n_tblocks = (num_tokens + 31) / 32;
@@ -346,7 +344,7 @@ static cudaError_t launch_store(const uint16_t *key, int64_t key_stride, const u
   unsigned grid_x = 0;
 #define PAQ8_STORE_CASE(DD, BB)                                                               \
   if (d == DD && block_size == BB) {                                                          \
-    if (cudaError_t e = store_grid_x<DD, BB>(n_tblocks, grid_y, &grid_x); e != cudaSuccess)  \
+    if (cudaError_t e = store_grid_x<DD, BB>(n_tblocks, grid_y, blocks_per_sm, &grid_x); e != cudaSuccess)  \
       return e;                                                                               \
     kv_store_kernel<DD, BB><<<dim3(grid_x, grid_y), block, kStoreSmem, stream>>>(              \
         key, key_stride, value, value_stride, slot_mapping, num_tokens, hk, k_cache, k_scale, \
@@ -371,21 +369,19 @@ cudaError_t launch_kv_store(const uint16_t *key, int64_t key_stride, const uint1
                             cudaStream_t stream) {
   return launch_store(key, key_stride, value, value_stride, slot_mapping, num_tokens, hk, d,
                       k_cache, k_scale, v_cache, v_scale, num_blocks, block_size, status, 0,
-                      nullptr, 0, stream);
+                      nullptr, 0, stream, 0);
 }
 
-// The values of a store whose keys another kernel writes (the fused norm and
-// rotation store): the same kernel, value warps only; with `positions`, a
-// token whose position is outside [0, max_position) is skipped.
+// The values of the fused norm and rotation store (launch.h).
 cudaError_t launch_kv_store_values(const uint16_t *value, int64_t value_stride,
                                    const int64_t *slot_mapping, int32_t num_tokens, int32_t hk,
                                    int32_t d, int8_t *v_cache, uint16_t *v_scale,
                                    int32_t num_blocks, int32_t block_size, uint32_t *status,
                                    const int64_t *positions, int32_t max_position,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, int32_t blocks_per_sm) {
   return launch_store(value, value_stride, value, value_stride, slot_mapping, num_tokens, hk, d,
                       nullptr, nullptr, v_cache, v_scale, num_blocks, block_size, status, 1,
-                      positions, max_position, stream);
+                      positions, max_position, stream, blocks_per_sm);
 }
 
 }  // namespace paq8

@@ -5,20 +5,29 @@
 // from the fp32 rotated values) applied to the q8 cache format.  The values
 // are stored as kv_store stores them (kv_store.cu, values-only mode).
 //
-// Keys: one warp per (token, kv head); lane l holds channels l, l + 32, ...
-// (register j = channel l + 32 j), which is also the q8 group layout: group j
-// is register j across the 32 lanes.
+// Keys: one warp per unit = (token, run of its kv heads): all heads of a
+// token when they fit 2 KB of bf16 (fewer per unit otherwise), and one head
+// per unit for a batch too small to fill the GPU that way; one block per 8
+// units, so that the block scheduler balances the work.  Lane l holds
+// channels l, l + 32, ... (register j = channel l + 32 j), which is also the
+// q8 group layout: group j is register j across the 32 lanes.  The unit's
+// slot, position and cos / sin values are read once for all of its heads,
+// the next head's row is in flight while one is worked.
 //  * norm: each lane squares its first channel and adds the next ones with
 //    fused multiply-adds (the page's lane sums), the 32 lane sums are added
 //    by an xor butterfly (16, 8, 4, 2, 1); inv = 1 / sqrt(total / D + eps)
-//    with the square root and the division each rounded once in fp32;
-//    y = bf16((x * inv) * w);
-//  * rotation: the row goes through shared memory so that every lane reads
-//    its pair partner (p with p + rot / 2, or 2p with 2p + 1); lead =
-//    fma(cos, y_lead, (-sin) * y_trail), trail = fma(sin, y_lead, cos *
-//    y_trail), fp32;
-//  * q8: the group max by a warp max-reduction, the code of each lane's value
-//    as in kv_store (the product with 1/s, exact near rounding ties).
+//    with the square root and the reciprocal each rounded once in fp32
+//    (total / D is exact scaling by a power of two); y = bf16((x * inv) * w),
+//    two channels at a time in packed fp32 arithmetic;
+//  * rotation: lead = fma(cos, y_lead, (-sin) * y_trail), trail = fma(sin,
+//    y_lead, cos * y_trail), fp32.  With split-half pairs over the whole row
+//    the partner of register j is register j +- J/2 of the same lane; with
+//    interleaved pairs it is lane l ^ 1 (one shuffle); other split-half
+//    rotary dims go through shared memory;
+//  * q8: the J group maxima by a reduce-scatter over the lanes (lane l ends
+//    with group l / (32 / J)), one scale and reciprocal per lane, broadcast
+//    back; the code of each value as in kv_store (the product with 1/s,
+//    exact near rounding ties).
 // Every floating-point step uses an explicitly rounded intrinsic, so that no
 // contraction changes a bit: the codes are those of the CPU oracle.
 #include "common.cuh"
@@ -28,150 +37,371 @@
 namespace paq8 {
 
 constexpr int kRopeWarps = 8;
+constexpr int kRopeMaxBytes = 2048;          // bf16 keys of one unit, at most
+constexpr int64_t kRopeWideUnits = 16384;    // fewer wide units: one head per unit
+constexpr int32_t kRopeOverlapTokens = 4096;  // fewer tokens: keys, then values
 
-template <int D>
-__global__ void __launch_bounds__(32 * kRopeWarps) kv_store_norm_rope_kernel(
-    const uint16_t *__restrict__ key, int64_t key_stride, const int64_t *__restrict__ slot_mapping,
-    const int64_t *__restrict__ positions, int32_t num_tokens, int32_t hk,
-    const uint16_t *__restrict__ norm_weight, float eps, const float *__restrict__ rope,
-    int32_t max_position, int32_t rot, int32_t interleaved, int8_t *__restrict__ k_cache,
-    uint16_t *__restrict__ k_scale, int64_t num_slots, int32_t block_size, uint32_t *status) {
-  constexpr int J = D / 32;  // channels per lane, and q8 groups per row
-  __shared__ float rowbuf[kRopeWarps][D];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  float *row_s = rowbuf[warp];
-  const int64_t units = static_cast<int64_t>(num_tokens) * hk;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kRopeWarps;
-  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kRopeWarps + warp; u < units; u += stride) {
-    const int64_t n = u / hk;
-    const int h = static_cast<int>(u % hk);
-    const int64_t slot = slot_mapping[n];
-    if (slot < 0) continue;  // padding row
-    if (slot >= num_slots) {
-      if (h == 0 && lane == 0) flag_status(status, PA_DEV_BAD_SLOT);
-      continue;
+enum RopeMode : int {
+  kRopeNone = 0,         // norm only
+  kRopeHalfFull = 1,     // split-half pairs (p, p + D/2) over the whole row
+  kRopeInterleaved = 2,  // pairs (2p, 2p + 1), any rotary dim
+  kRopeHalfPart = 3,     // split-half pairs (p, p + rot/2), rot < D
+};
+
+// Max of each of the J values m[j] over the 32 lanes, reduce-scattered:
+// returns the max of group (lane >> (5 - log2 J)), i.e. lanes
+// g * 32/J .. (g+1) * 32/J - 1 hold group g's.  At each of the first log2 J
+// steps a lane keeps half of its groups and sends the other half to its
+// partner; the remaining steps are a plain butterfly.
+template <int J>
+__device__ __forceinline__ float group_max_scatter(float (&m)[J], int lane) {
+#pragma unroll
+  for (int width = J, bit = 16; width > 1; width >>= 1, bit >>= 1) {
+    const bool hi = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < width / 2; ++i) {
+      const float send = hi ? m[i] : m[i + width / 2];
+      const float keep = hi ? m[i + width / 2] : m[i];
+      m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, bit));
     }
-    int64_t pos = 0;
-    if (rope) {
-      pos = positions[n];
-      if (pos < 0 || pos >= max_position) {
-        if (h == 0 && lane == 0) flag_status(status, PA_DEV_BAD_POS);
-        continue;
+  }
+  float r = m[0];
+#pragma unroll
+  for (int bit = 16 / J; bit > 0; bit >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, bit));
+  return r;
+}
+
+// The rotation constants of one unit (token) for this lane.
+template <int J>
+struct TokenRope {
+  float2 cs[J];  // cos, sin of the pair of register j (split-half: j < J/2)
+  uint64_t cos2[J / 4 > 0 ? J / 4 : 1], sin2[J / 4 > 0 ? J / 4 : 1], nsin2[J / 4 > 0 ? J / 4 : 1];
+  const float *row;  // the token's [rot / 2][2] table row
+};
+
+template <int D, int MODE>
+__device__ __forceinline__ void token_rope(TokenRope<D / 32> &tr, const float *rope, int64_t pos,
+                                           int rot, int lane) {
+  constexpr int J = D / 32;
+  if constexpr (MODE != kRopeNone) {
+    tr.row = rope + pos * rot;
+    if constexpr (MODE == kRopeHalfFull) {
+#pragma unroll
+      for (int j = 0; j < J / 2; ++j)
+        tr.cs[j] = *reinterpret_cast<const float2 *>(tr.row + 2 * (lane + 32 * j));
+#pragma unroll
+      for (int i = 0; i < J / 4; ++i) {
+        tr.cos2[i] = f32x2_pack(tr.cs[2 * i].x, tr.cs[2 * i + 1].x);
+        tr.sin2[i] = f32x2_pack(tr.cs[2 * i].y, tr.cs[2 * i + 1].y);
+        tr.nsin2[i] = f32x2_pack(-tr.cs[2 * i].y, -tr.cs[2 * i + 1].y);
       }
-    }
-    const uint16_t *src = key + n * key_stride + static_cast<int64_t>(h) * D;
-    float y[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) y[j] = __uint_as_float(static_cast<uint32_t>(src[lane + 32 * j]) << 16);
-
-    // ---- weighted RMSNorm, output rounded to bf16
-    if (norm_weight) {
-      float acc = __fmul_rn(y[0], y[0]);
-#pragma unroll
-      for (int j = 1; j < J; ++j) acc = __fmaf_rn(y[j], y[j], acc);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-      const float inv =
-          __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, static_cast<float>(D)), eps)));
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const float w = __uint_as_float(static_cast<uint32_t>(norm_weight[lane + 32 * j]) << 16);
-        const float t = __fmul_rn(__fmul_rn(y[j], inv), w);
-        y[j] = __bfloat162float(__float2bfloat16_rn(t));
-      }
-    }
-
-    // ---- rotation of the first `rot` channels (pairs through shared memory)
-    if (rope) {
-#pragma unroll
-      for (int j = 0; j < J; ++j) row_s[lane + 32 * j] = y[j];
-      __syncwarp();
-      const float *cs_row = rope + pos * rot;  // [rot / 2][2]: cos, sin
-      const int pairs = rot >> 1;
-      float out[J];
+    } else if constexpr (MODE == kRopeInterleaved) {
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int c = lane + 32 * j;
-        out[j] = y[j];
-        if (c < rot) {
-          const bool lead = interleaved ? (c & 1) == 0 : c < pairs;
-          const int partner = interleaved ? (c ^ 1) : (lead ? c + pairs : c - pairs);
-          const int p = interleaved ? (c >> 1) : (lead ? c : c - pairs);
-          const float2 cs = *reinterpret_cast<const float2 *>(cs_row + 2 * p);
-          const float other = row_s[partner];
-          // lead:  fma(cos, y_lead, (-sin) * y_trail)
-          // trail: fma(sin, y_lead, cos * y_trail)
-          out[j] = lead ? __fmaf_rn(cs.x, y[j], __fmul_rn(-cs.y, other))
-                        : __fmaf_rn(cs.y, other, __fmul_rn(cs.x, y[j]));
-        }
+        tr.cs[j] = c < rot ? *reinterpret_cast<const float2 *>(tr.row + 2 * (c >> 1))
+                           : make_float2(1.0f, 0.0f);
       }
-      __syncwarp();  // row_s is rewritten for the warp's next unit
-#pragma unroll
-      for (int j = 0; j < J; ++j) y[j] = out[j];
-    }
-
-    // ---- q8 of each group j (register j across the lanes)
-    const int64_t blk = slot / block_size, off = slot % block_size;
-    const int64_t krow = (blk * hk + h) * block_size + off;
-    constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-    constexpr float kFar = 0.5f - 0x1p-15f;
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      float amax = fabsf(y[j]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float sc = group_scale(amax);
-      const float rs = __frcp_rn(sc);
-      const float q = __fmul_rn(y[j], rs);
-      const float t = __fadd_rn(q, kShift);
-      int32_t code = static_cast<int32_t>(__float_as_uint(t) & 0xffu);
-      // within 2^-15 of a rounding tie: the IEEE quotient's code, exactly
-      if (fabsf(__fsub_rn(q, __fsub_rn(t, kShift))) >= kFar) code = tie_code(y[j], sc, rs);
-      k_cache[krow * D + 32 * j + lane] = static_cast<int8_t>(code);
-      if (lane == 0) k_scale[krow * J + j] = __half_as_ushort(__float2half_rn(sc));
     }
   }
 }
 
-cudaError_t launch_kv_store_values(const uint16_t *value, int64_t value_stride,
-                                   const int64_t *slot_mapping, int32_t num_tokens, int32_t hk,
-                                   int32_t d, int8_t *v_cache, uint16_t *v_scale,
-                                   int32_t num_blocks, int32_t block_size, uint32_t *status,
-                                   const int64_t *positions, int32_t max_position,
-                                   cudaStream_t stream);
+// Whether the unit's token is stored; flags a bad slot or position once per
+// token (by the unit holding head 0).
+__device__ __forceinline__ bool token_ok(int64_t slot, int64_t pos, bool has_rope, int h0,
+                                         int lane, int64_t num_slots, int32_t max_position,
+                                         uint32_t *status) {
+  if (slot < 0) return false;  // padding row
+  if (slot >= num_slots) {
+    if (h0 == 0 && lane == 0) flag_status(status, PA_DEV_BAD_SLOT);
+    return false;
+  }
+  if (has_rope && (pos < 0 || pos >= max_position)) {
+    if (h0 == 0 && lane == 0) flag_status(status, PA_DEV_BAD_POS);
+    return false;
+  }
+  return true;
+}
 
-template <int D>
+// Norm, rotation and q8 of one key row y (register j = channel lane + 32 j),
+// stored at cache row krow.
+template <int D, int MODE>
+__device__ __forceinline__ void norm_rope_row(float (&y)[D / 32], const uint64_t (&wt2)[D / 64],
+                                              bool norm, float eps, const TokenRope<D / 32> &tr,
+                                              int rot, float *row_s, int lane,
+                                              int8_t *__restrict__ k_cache,
+                                              uint16_t *__restrict__ k_scale, int64_t krow) {
+  constexpr int J = D / 32;
+  constexpr int kLanesPerGroup = 32 / J;
+  // ---- weighted RMSNorm, output rounded to bf16
+  if (norm) {
+    float acc = __fmul_rn(y[0], y[0]);
+#pragma unroll
+    for (int j = 1; j < J; ++j) acc = __fmaf_rn(y[j], y[j], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    const float inv =
+        __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(acc, 1.0f / static_cast<float>(D)), eps)));
+    const uint64_t inv2 = f32x2_pack(inv, inv);
+#pragma unroll
+    for (int i = 0; i < J / 2; ++i) {  // two channels at a time
+      const uint64_t t2 = f32x2_mul(f32x2_mul(f32x2_pack(y[2 * i], y[2 * i + 1]), inv2), wt2[i]);
+      float t0, t1;
+      f32x2_unpack(t2, t0, t1);
+      const __nv_bfloat162 r = __floats2bfloat162_rn(t0, t1);
+      const uint32_t rb = *reinterpret_cast<const uint32_t *>(&r);
+      y[2 * i] = bf16_lo(rb);
+      y[2 * i + 1] = bf16_hi(rb);
+    }
+  }
+
+  // ---- rotation
+  if constexpr (MODE == kRopeHalfFull) {
+    if constexpr (J == 2) {
+      const float lead = y[0], trail = y[1];
+      y[0] = __fmaf_rn(tr.cs[0].x, lead, __fmul_rn(-tr.cs[0].y, trail));
+      y[1] = __fmaf_rn(tr.cs[0].y, lead, __fmul_rn(tr.cs[0].x, trail));
+    } else {
+#pragma unroll
+      for (int i = 0; i < J / 4; ++i) {  // leads 2i, 2i+1 with trails 2i + J/2, 2i+1 + J/2
+        const uint64_t lead = f32x2_pack(y[2 * i], y[2 * i + 1]);
+        const uint64_t trail = f32x2_pack(y[2 * i + J / 2], y[2 * i + 1 + J / 2]);
+        const uint64_t ol = f32x2_fma(tr.cos2[i], lead, f32x2_mul(tr.nsin2[i], trail));
+        const uint64_t ot = f32x2_fma(tr.sin2[i], lead, f32x2_mul(tr.cos2[i], trail));
+        f32x2_unpack(ol, y[2 * i], y[2 * i + 1]);
+        f32x2_unpack(ot, y[2 * i + J / 2], y[2 * i + 1 + J / 2]);
+      }
+    }
+  } else if constexpr (MODE == kRopeInterleaved) {
+    const bool is_lead = (lane & 1) == 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float other = __shfl_xor_sync(0xffffffffu, y[j], 1);
+      if (lane + 32 * j < rot)
+        y[j] = is_lead ? __fmaf_rn(tr.cs[j].x, y[j], __fmul_rn(-tr.cs[j].y, other))
+                       : __fmaf_rn(tr.cs[j].y, other, __fmul_rn(tr.cs[j].x, y[j]));
+    }
+  } else if constexpr (MODE == kRopeHalfPart) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) row_s[lane + 32 * j] = y[j];
+    __syncwarp();
+    const int pairs = rot >> 1;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int c = lane + 32 * j;
+      if (c < rot) {
+        const bool is_lead = c < pairs;
+        const int p = is_lead ? c : c - pairs;
+        const float2 c2 = *reinterpret_cast<const float2 *>(tr.row + 2 * p);
+        const float other = row_s[is_lead ? c + pairs : c - pairs];
+        y[j] = is_lead ? __fmaf_rn(c2.x, y[j], __fmul_rn(-c2.y, other))
+                       : __fmaf_rn(c2.y, other, __fmul_rn(c2.x, y[j]));
+      }
+    }
+    __syncwarp();  // row_s is rewritten for the next row
+  }
+
+  // ---- q8 of each group j (register j across the lanes)
+  float m[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) m[j] = fabsf(y[j]);
+  const float my_sc = group_scale(group_max_scatter<J>(m, lane));
+  const float my_rs = __frcp_rn(my_sc);
+  // c = the integer nearest to q = y * (1/s), taken exactly from one fused
+  // multiply-add of 1.5 * 2^23 (its low byte is the code); d = q - c from a
+  // second one.  Where |d| < 1/2 - 2^-15 the IEEE quotient y / s rounds to c
+  // as well (they differ by under 1.6e-5 for |y / s| <= 127.00002); values
+  // closer to a tie are decided exactly below.
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kFar = 0.5f - 0x1p-15f;
+  const uint64_t shift2 = f32x2_pack(kShift, kShift);
+  const uint64_t minus1 = f32x2_pack(-1.0f, -1.0f);
+  uint32_t tb[J];
+  float d[J], nc[J];
+  bool near = false;
+#pragma unroll
+  for (int i = 0; i < J / 2; ++i) {
+    const uint64_t rs2 = f32x2_pack(__shfl_sync(0xffffffffu, my_rs, 2 * i * kLanesPerGroup),
+                                    __shfl_sync(0xffffffffu, my_rs, (2 * i + 1) * kLanesPerGroup));
+    const uint64_t y2 = f32x2_pack(y[2 * i], y[2 * i + 1]);
+    const uint64_t t2 = f32x2_fma(y2, rs2, shift2);      // 1.5 * 2^23 + c
+    const uint64_t nc2 = f32x2_fma(t2, minus1, shift2);  // -c, exact
+    const uint64_t d2 = f32x2_fma(y2, rs2, nc2);         // y * rs - c
+    float t0, t1;
+    f32x2_unpack(t2, t0, t1);
+    tb[2 * i] = __float_as_uint(t0);
+    tb[2 * i + 1] = __float_as_uint(t1);
+    f32x2_unpack(d2, d[2 * i], d[2 * i + 1]);
+    f32x2_unpack(nc2, nc[2 * i], nc[2 * i + 1]);
+    near = near || fabsf(d[2 * i]) >= kFar || fabsf(d[2 * i + 1]) >= kFar;
+  }
+  // Values within 2^-15 of a tie take the code of the IEEE quotient, decided
+  // without a divide from the half-integer h = c + sign(d) / 2 they lie next
+  // to (rare: the whole warp takes this branch together).
+  if (__any_sync(0xffffffffu, near)) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float sc = __shfl_sync(0xffffffffu, my_sc, j * kLanesPerGroup);
+      if (fabsf(d[j]) >= kFar) {
+        const float hh = __fsub_rn(copysignf(0.5f, d[j]), nc[j]);
+        tb[j] = tie_code_bits(y[j], sc, hh);
+      }
+    }
+  }
+  int8_t *dst = k_cache + krow * D + lane;
+#pragma unroll
+  for (int j = 0; j < J; ++j) dst[32 * j] = static_cast<int8_t>(tb[j] & 0xffu);
+  // each group's first lane stores its scale
+  if (lane % kLanesPerGroup == 0)
+    k_scale[krow * J + lane / kLanesPerGroup] = __half_as_ushort(__float2half_rn(my_sc));
+}
+
+// grid: one warp per unit (ceil(units / kRopeWarps) blocks, capped; the
+// warps then stride on); block: 32 x kRopeWarps; dynamic shared memory:
+// kRopeHalfPart, [kRopeWarps][D] fp32.
+template <int D, int BS, int MODE>
+__global__ void __launch_bounds__(32 * kRopeWarps) kv_store_norm_rope_kernel(
+    const uint16_t *__restrict__ key, int64_t key_stride, const int64_t *__restrict__ slot_mapping,
+    const int64_t *__restrict__ positions, int32_t num_tokens, int32_t hk, int32_t head_split,
+    const uint16_t *__restrict__ norm_weight, float eps, const float *__restrict__ rope,
+    int32_t max_position, int32_t rot, int8_t *__restrict__ k_cache,
+    uint16_t *__restrict__ k_scale, int64_t num_slots, uint32_t *status) {
+  constexpr int J = D / 32;  // channels per lane, and q8 groups per row
+  extern __shared__ __align__(16) float rope_rows[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  float *row_s = rope_rows + warp * D;
+  const bool norm = norm_weight != nullptr;
+  constexpr bool kHasRope = MODE != kRopeNone;
+
+  uint64_t wt2[J / 2];  // norm weights of channel pairs (2i, 2i + 1) of the lane
+  if (norm) {
+#pragma unroll
+    for (int i = 0; i < J / 2; ++i)
+      wt2[i] = f32x2_pack(bf16_lo(norm_weight[lane + 64 * i]),
+                          bf16_lo(norm_weight[lane + 64 * i + 32]));
+  }
+  const int heads_per = (hk + head_split - 1) / head_split;
+  const int64_t units = static_cast<int64_t>(num_tokens) * head_split;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kRopeWarps;
+  TokenRope<J> tr;
+#pragma unroll 1
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kRopeWarps + warp; u < units; u += stride) {
+    // token and first head of unit u
+    int64_t n = u;
+    int h0 = 0;
+    if (head_split > 1) {
+      n = u / head_split;
+      h0 = static_cast<int>(u - n * head_split) * heads_per;
+    }
+    const int h1 = min(h0 + heads_per, hk);
+    const int64_t slot = slot_mapping[n];
+    const int64_t pos = kHasRope && slot >= 0 && slot < num_slots ? positions[n] : 0;
+    if (h0 >= h1 || !token_ok(slot, pos, kHasRope, h0, lane, num_slots, max_position, status))
+      continue;
+    token_rope<D, MODE>(tr, rope, pos, rot, lane);
+    const uint64_t us = static_cast<uint64_t>(slot);
+    const int64_t blk = static_cast<int64_t>(us / BS), off = static_cast<int64_t>(us % BS);
+    const uint16_t *src = key + n * key_stride + lane;
+    uint16_t nxt[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) nxt[j] = src[static_cast<int64_t>(h0) * D + 32 * j];
+#pragma unroll 1
+    for (int h = h0; h < h1; ++h) {
+      float y[J];
+#pragma unroll
+      for (int j = 0; j < J; ++j) y[j] = bf16_lo(nxt[j]);
+      if (h + 1 < h1) {  // the next head's row, in flight while this one is worked
+#pragma unroll
+        for (int j = 0; j < J; ++j) nxt[j] = src[static_cast<int64_t>(h + 1) * D + 32 * j];
+      }
+      norm_rope_row<D, MODE>(y, wt2, norm, eps, tr, rot, row_s, lane, k_cache, k_scale,
+                             (blk * hk + h) * BS + off);
+    }
+  }
+}
+
+template <int D, int BS, int MODE>
 static cudaError_t launch_keys(const KvNormRope &p, cudaStream_t stream) {
-  static DeviceOnce sm_count;
-  int sms = 0;
-  cudaError_t e = sm_count.get(&sms, [](int dev, int *v) {
-    return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+  constexpr int smem = MODE == kRopeHalfPart ? kRopeWarps * D * 4 : 0;
+  // the shared-memory carveout of the values kernel, so that the blocks of
+  // both can be resident on one SM together
+  static DeviceOnce carveout;
+  int unused = 0;
+  cudaError_t e = carveout.get(&unused, [](int, int *v) {
+    *v = 0;
+    return cudaFuncSetAttribute(kv_store_norm_rope_kernel<D, BS, MODE>,
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
   });
   if (e != cudaSuccess) return e;
-  const int64_t units = static_cast<int64_t>(p.num_tokens) * p.hk;
+  // units of a token's heads (as many as fit kRopeMaxBytes) when that makes
+  // enough units to fill the GPU; otherwise one head per unit
+  constexpr int kMaxHeads = kRopeMaxBytes / (2 * D);
+  const int wide_split = (p.hk + kMaxHeads - 1) / kMaxHeads;
+  const int64_t wide_units = static_cast<int64_t>(p.num_tokens) * wide_split;
+  const int head_split = wide_units >= kRopeWideUnits ? wide_split : p.hk;
+  const int64_t units = static_cast<int64_t>(p.num_tokens) * head_split;
   const int64_t want = (units + kRopeWarps - 1) / kRopeWarps;
-  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;  // 8 blocks of 256 per SM
-  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  kv_store_norm_rope_kernel<D><<<grid, 32 * kRopeWarps, 0, stream>>>(
-      p.key, p.key_stride, p.slot_mapping, p.positions, p.num_tokens, p.hk, p.norm_weight, p.eps,
-      p.rope, p.max_position, p.rotary_dim, p.interleaved ? 1 : 0, p.k_cache, p.k_scale,
-      static_cast<int64_t>(p.num_blocks) * p.block_size, p.block_size, p.status);
+  const unsigned grid = static_cast<unsigned>(want < (1 << 30) ? want : (1 << 30));
+  kv_store_norm_rope_kernel<D, BS, MODE><<<grid, 32 * kRopeWarps, smem, stream>>>(
+      p.key, p.key_stride, p.slot_mapping, p.positions, p.num_tokens, p.hk, head_split,
+      p.norm_weight, p.eps, p.rope, p.max_position, p.rotary_dim, p.k_cache, p.k_scale,
+      static_cast<int64_t>(p.num_blocks) * p.block_size, p.status);
   return cudaGetLastError();
 }
 
+template <int D, int BS>
+static cudaError_t launch_keys_mode(const KvNormRope &p, cudaStream_t stream) {
+  if (!p.rope) return launch_keys<D, BS, kRopeNone>(p, stream);
+  if (p.interleaved) return launch_keys<D, BS, kRopeInterleaved>(p, stream);
+  if (p.rotary_dim == D) return launch_keys<D, BS, kRopeHalfFull>(p, stream);
+  return launch_keys<D, BS, kRopeHalfPart>(p, stream);
+}
+
+static cudaError_t launch_keys_any(const KvNormRope &p, cudaStream_t stream) {
+#define PAQ8_ROPE_CASE(DD, BB) \
+  if (p.d == DD && p.block_size == BB) return launch_keys_mode<DD, BB>(p, stream);
+  PAQ8_ROPE_CASE(64, 16)
+  PAQ8_ROPE_CASE(64, 32)
+  PAQ8_ROPE_CASE(128, 16)
+  PAQ8_ROPE_CASE(128, 32)
+  PAQ8_ROPE_CASE(256, 16)
+  PAQ8_ROPE_CASE(256, 32)
+#undef PAQ8_ROPE_CASE
+  return cudaErrorInvalidValue;
+}
+
+// The values (kv_store's kernel, light on instructions and bound by memory)
+// run on the high-priority side stream beside the keys (bound by
+// instruction issue), one block per SM, so that the two overlap: their
+// blocks are resident together and the keys' many short blocks take what the
+// values leave.  A small batch (or a side stream that cannot be had) runs
+// the two one after the other on `stream`.
 cudaError_t launch_kv_store_norm_rope(const KvNormRope &p, cudaStream_t stream) {
-  cudaError_t e = cudaErrorInvalidValue;
-  switch (p.d) {
-    case 64: e = launch_keys<64>(p, stream); break;
-    case 128: e = launch_keys<128>(p, stream); break;
-    case 256: e = launch_keys<256>(p, stream); break;
-    default: return cudaErrorInvalidValue;
+  if (p.num_tokens == 0) return cudaSuccess;
+  const int32_t max_pos = p.max_position;
+  const int64_t *vpos = p.rope ? p.positions : nullptr;
+  SideStream *ss = nullptr;
+  if (p.num_tokens >= kRopeOverlapTokens && side_stream(&ss) == cudaSuccess) {
+    cudaError_t e;
+    if ((e = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
+    if ((e = launch_kv_store_values(p.value, p.value_stride, p.slot_mapping, p.num_tokens, p.hk,
+                                    p.d, p.v_cache, p.v_scale, p.num_blocks, p.block_size,
+                                    p.status, vpos, max_pos, ss->s, 1)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
+    const cudaError_t ek = launch_keys_any(p, stream);
+    // the join is waited for even when the keys failed to launch
+    if ((e = cudaStreamWaitEvent(stream, ss->join, 0)) != cudaSuccess) return e;
+    return ek;
   }
+  cudaError_t e = launch_keys_any(p, stream);
   if (e != cudaSuccess) return e;
   return launch_kv_store_values(p.value, p.value_stride, p.slot_mapping, p.num_tokens, p.hk, p.d,
-                                p.v_cache, p.v_scale, p.num_blocks, p.block_size, p.status,
-                                p.rope ? p.positions : nullptr, p.max_position, stream);
+                                p.v_cache, p.v_scale, p.num_blocks, p.block_size, p.status, vpos,
+                                max_pos, stream, 0);
 }
 
 }  // namespace paq8

@@ -67,6 +67,28 @@ struct KvNormRope {
 
 cudaError_t launch_kv_store_norm_rope(const KvNormRope &p, cudaStream_t stream);
 
+// The values of a store whose keys another kernel writes (the fused norm and
+// rotation store): kv_store's kernel, value warps only; with `positions`, a
+// token whose position is outside [0, max_position) is skipped.
+// blocks_per_sm > 0 caps its persistent grid at that many blocks per SM
+// (0: as many as are resident).
+cudaError_t launch_kv_store_values(const uint16_t *value, int64_t value_stride,
+                                   const int64_t *slot_mapping, int32_t num_tokens, int32_t hk,
+                                   int32_t d, int8_t *v_cache, uint16_t *v_scale,
+                                   int32_t num_blocks, int32_t block_size, uint32_t *status,
+                                   const int64_t *positions, int32_t max_position,
+                                   cudaStream_t stream, int32_t blocks_per_sm);
+
+// A high-priority side stream of the current device, with fork / join
+// events, for work that runs beside the caller's stream.  Created once per
+// device; calls from several host threads share it (correct, but their side
+// work then queues behind one another).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+cudaError_t side_stream(SideStream **out);
+
 cudaError_t launch_kv_store_f8v4(const uint16_t *key, int64_t key_stride, const uint16_t *value,
                                  int64_t value_stride, const int64_t *slot_mapping,
                                  int32_t num_tokens, int32_t hk, int32_t d, uint8_t *k_cache,

@@ -49,15 +49,29 @@ def _case(seed, hk, d, bs, n, rot, interleaved, norm, bad_pos=False, outliers=Fa
                 num_blocks=num_blocks, hk=hk, d=d, bs=bs, interleaved=interleaved)
 
 
-def _run_both(c, device, eps=1e-6):
+def _strided_key(k, device, pad):
+    """k [n, hk, d] on the device with a token stride of hk * d + pad
+    elements (pad = 1: rows that are not 16-byte aligned)."""
+    n, hk, d = k.shape
+    if pad == 0:
+        return k.to(device)
+    big = torch.zeros((n, hk * d + pad), dtype=k.dtype, device=device)
+    big[:, :hk * d] = k.reshape(n, hk * d).to(device)
+    return big.as_strided((n, hk, d), (hk * d + pad, d, 1))
+
+
+def _run_both(c, device, eps=1e-6, key_pad=0):
     kc, ks, vc, vs = inputs.empty_cache(c["num_blocks"], c["hk"], c["bs"], c["d"], device=device)
     status = torch.zeros(4, dtype=torch.int32, device=device)
     table = None if c["table"] is None else torch.from_numpy(c["table"]).to(device)
-    _lib.kv_store_norm_rope(c["k"].to(device), c["v"].to(device),
+    _lib.kv_store_norm_rope(_strided_key(c["k"], device, key_pad), c["v"].to(device),
                             torch.from_numpy(c["slots"]).to(device), kc, ks, vc, vs,
                             positions=torch.from_numpy(c["positions"]).to(device),
                             norm_weight=None if c["w"] is None else c["w"].to(device), eps=eps,
                             rope=table, interleaved=c["interleaved"], status=status)
+    # copies taken on the same stream right after the call: the store's work
+    # on any other stream has joined it by then
+    kc, ks, vc, vs = (t.clone() for t in (kc, ks, vc, vs))
     torch.cuda.synchronize()
     okc, oks, ovc, ovs = [t.numpy() for t in inputs.empty_cache(c["num_blocks"], c["hk"],
                                                                 c["bs"], c["d"])]
@@ -92,7 +106,24 @@ def _assert_same(g, o):
 def test_fused_store_is_bit_exact(d, bs, rot, interleaved, norm, cuda_device):
     c = _case(400 + d + rot + bs + int(interleaved), hk=3, d=d, bs=bs, n=157, rot=rot,
               interleaved=interleaved, norm=norm, outliers=True)
-    g, o = _run_both(c, cuda_device)
+    for key_pad in (0, 1):  # key rows 16-byte aligned or not
+        g, o = _run_both(c, cuda_device, key_pad=key_pad)
+        assert o[4] == 0
+        assert _lib.check_status(g[4]) == 0
+        _assert_same(g, o)
+
+
+@pytest.mark.parametrize("d,rot,interleaved,key_pad", [
+    (128, 128, False, 0), (128, 128, True, 0), (256, 192, False, 0), (64, 64, False, 0),
+    (128, 128, False, 1), (256, 256, True, 1)])
+def test_fused_store_large_batch_is_bit_exact(d, rot, interleaved, key_pad, cuda_device):
+    # enough tokens for one warp per token walking the kv heads (the
+    # population / prefill launch shape) rather than one per (token, head),
+    # and the values beside them on a second stream; key_pad 1: key rows
+    # that are not 16-byte aligned
+    c = _case(430 + d + rot + int(interleaved), hk=2, d=d, bs=16, n=40000, rot=rot,
+              interleaved=interleaved, norm=True, outliers=True)
+    g, o = _run_both(c, cuda_device, key_pad=key_pad)
     assert o[4] == 0
     assert _lib.check_status(g[4]) == 0
     _assert_same(g, o)
@@ -110,12 +141,26 @@ def test_fused_store_without_norm_or_rotation_equals_kv_store(cuda_device):
 
 def test_positions_outside_the_table_are_flagged_and_skipped(cuda_device):
     c = _case(411, hk=2, d=128, bs=16, n=90, rot=128, interleaved=False, norm=True, bad_pos=True)
-    g, o = _run_both(c, cuda_device)
-    assert o[4] >= 1
-    with pytest.raises(_lib.PagedAttentionError) as e:
-        _lib.check_status(g[4])
-    assert e.value.bits == _lib.DEV_BAD_POS
-    _assert_same(g, o)
+    for key_pad in (0, 1):
+        g, o = _run_both(c, cuda_device, key_pad=key_pad)
+        assert o[4] >= 1
+        with pytest.raises(_lib.PagedAttentionError) as e:
+            _lib.check_status(g[4])
+        assert e.value.bits == _lib.DEV_BAD_POS
+        _assert_same(g, o)
+
+
+def test_slots_outside_the_cache_are_flagged_and_skipped(cuda_device):
+    c = _case(412, hk=2, d=128, bs=16, n=90, rot=128, interleaved=True, norm=True)
+    nslots = c["num_blocks"] * c["bs"]
+    c["slots"][[5, 40]] = [nslots, nslots + 100]
+    for key_pad in (0, 1):
+        g, o = _run_both(c, cuda_device, key_pad=key_pad)
+        assert o[4] == 2
+        with pytest.raises(_lib.PagedAttentionError) as e:
+            _lib.check_status(g[4])
+        assert e.value.bits == _lib.DEV_BAD_SLOT
+        _assert_same(g, o)
 
 
 def test_attention_over_a_fused_store_cache(cuda_device):
