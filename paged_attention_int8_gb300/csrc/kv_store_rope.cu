@@ -6,28 +6,29 @@
 // are stored as kv_store stores them (kv_store.cu, values-only mode).
 //
 // Keys: one warp per unit = (token, run of its kv heads): all heads of a
-// token when they fit 2 KB of bf16 (fewer per unit otherwise), and one head
-// per unit for a batch too small to fill the GPU that way; one block per 8
-// units, so that the block scheduler balances the work.  Lane l holds
-// channels l, l + 32, ... (register j = channel l + 32 j), which is also the
-// q8 group layout: group j is register j across the 32 lanes.  The unit's
-// slot, position and cos / sin values are read once for all of its heads,
-// the next head's row is in flight while one is worked.
-//  * norm: each lane squares its first channel and adds the next ones with
-//    fused multiply-adds (the page's lane sums), the 32 lane sums are added
-//    by an xor butterfly (16, 8, 4, 2, 1); inv = 1 / sqrt(total / D + eps)
-//    with the square root and the reciprocal each rounded once in fp32
-//    (total / D is exact scaling by a power of two); y = bf16((x * inv) * w),
-//    two channels at a time in packed fp32 arithmetic;
+// token when they fit 2 KB of bf16 (fewer per unit otherwise), and as many
+// as one warp holds at once for a batch too small to fill the GPU that way;
+// one block per 8 units, so that the block scheduler balances the work.  A
+// warp holds two rows at once (head size up to 128: 16 lanes per row, lane
+// l' of a row holding channels l' + 16 j) or one (256: lane l holding
+// l + 32 j); the unit's slot, position and cos / sin values are read once
+// for all of its heads, the next rows are in flight while some are worked.
+//  * norm: the page's 32 lane sums (lane l: channel l squared, then the
+//    channels l + 32, l + 64, ... added by fused multiply-adds; with 16
+//    lanes per row each lane forms two of them), added by an xor butterfly
+//    (16, 8, 4, 2, 1); inv = 1 / sqrt(total / D + eps) with the square root
+//    and the reciprocal each rounded once in fp32 (total / D is exact
+//    scaling by a power of two); y = bf16((x * inv) * w), two channels at a
+//    time in packed fp32 arithmetic;
 //  * rotation: lead = fma(cos, y_lead, (-sin) * y_trail), trail = fma(sin,
 //    y_lead, cos * y_trail), fp32.  With split-half pairs over the whole row
 //    the partner of register j is register j +- J/2 of the same lane; with
-//    interleaved pairs it is lane l ^ 1 (one shuffle); other split-half
-//    rotary dims go through shared memory;
-//  * q8: the J group maxima by a reduce-scatter over the lanes (lane l ends
-//    with group l / (32 / J)), one scale and reciprocal per lane, broadcast
-//    back; the code of each value as in kv_store (the product with 1/s,
-//    exact near rounding ties).
+//    interleaved pairs it is the neighbouring lane (one shuffle); other
+//    split-half rotary dims go through shared memory;
+//  * q8: the group maxima by a reduce-scatter over the row's lanes (each
+//    lane ends with one group's), one scale and reciprocal per lane,
+//    broadcast back; the code of each value as in kv_store (the product with
+//    1/s, exact near rounding ties).
 // Every floating-point step uses an explicitly rounded intrinsic, so that no
 // contraction changes a bit: the codes are those of the CPU oracle.
 #include "common.cuh"
@@ -48,15 +49,30 @@ enum RopeMode : int {
   kRopeHalfPart = 3,     // split-half pairs (p, p + rot/2), rot < D
 };
 
-// Max of each of the J values m[j] over the 32 lanes, reduce-scattered:
-// returns the max of group (lane >> (5 - log2 J)), i.e. lanes
-// g * 32/J .. (g+1) * 32/J - 1 hold group g's.  At each of the first log2 J
-// steps a lane keeps half of its groups and sends the other half to its
-// partner; the remaining steps are a plain butterfly.
-template <int J>
-__device__ __forceinline__ float group_max_scatter(float (&m)[J], int lane) {
+// How a warp holds key rows of D channels: R rows at once, LR lanes per
+// row, lane l' (of the row's lanes) holding channels l' + LR j, j < J.  The
+// 32 per-lane sums of the norm (lane l: channels l, l + 32, ...) are then
+// the chains of registers j = k, k + R, k + 2R, ... of lane l' = l % LR for
+// k = l / LR, and q8 group g is registers R g .. R g + R - 1 across the
+// row's lanes.
+template <int D>
+struct RowLayout {
+  static constexpr int R = D <= 128 ? 2 : 1;  // rows per warp
+  static constexpr int LR = 32 / R;           // lanes per row
+  static constexpr int J = D / LR;            // channels per lane
+  static constexpr int G = D / 32;            // q8 groups per row
+  static constexpr int LG = LR / G;           // lanes per group after the reduce-scatter
+};
+
+// Max of each of the G values m[g] over the LR lanes of a row,
+// reduce-scattered: returns the max of group l' / (LR / G), i.e. the row's
+// lanes g * LR/G .. (g+1) * LR/G - 1 hold group g's.  At each of the first
+// log2 G steps a lane keeps half of its groups and sends the other half to
+// its partner; the remaining steps are a plain butterfly.
+template <int G, int LR>
+__device__ __forceinline__ float group_max_scatter(float (&m)[G], int lane) {
 #pragma unroll
-  for (int width = J, bit = 16; width > 1; width >>= 1, bit >>= 1) {
+  for (int width = G, bit = LR / 2; width > 1; width >>= 1, bit >>= 1) {
     const bool hi = (lane & bit) != 0;
 #pragma unroll
     for (int i = 0; i < width / 2; ++i) {
@@ -67,7 +83,8 @@ __device__ __forceinline__ float group_max_scatter(float (&m)[J], int lane) {
   }
   float r = m[0];
 #pragma unroll
-  for (int bit = 16 / J; bit > 0; bit >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, bit));
+  for (int bit = LR / (2 * G); bit > 0; bit >>= 1)
+    r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, bit));
   return r;
 }
 
@@ -80,15 +97,16 @@ struct TokenRope {
 };
 
 template <int D, int MODE>
-__device__ __forceinline__ void token_rope(TokenRope<D / 32> &tr, const float *rope, int64_t pos,
-                                           int rot, int lane) {
-  constexpr int J = D / 32;
+__device__ __forceinline__ void token_rope(TokenRope<RowLayout<D>::J> &tr, const float *rope,
+                                           int64_t pos, int rot, int lr) {
+  using L = RowLayout<D>;
+  constexpr int J = L::J;
   if constexpr (MODE != kRopeNone) {
     tr.row = rope + pos * rot;
     if constexpr (MODE == kRopeHalfFull) {
 #pragma unroll
       for (int j = 0; j < J / 2; ++j)
-        tr.cs[j] = *reinterpret_cast<const float2 *>(tr.row + 2 * (lane + 32 * j));
+        tr.cs[j] = *reinterpret_cast<const float2 *>(tr.row + 2 * (lr + L::LR * j));
 #pragma unroll
       for (int i = 0; i < J / 4; ++i) {
         tr.cos2[i] = f32x2_pack(tr.cs[2 * i].x, tr.cs[2 * i + 1].x);
@@ -98,7 +116,7 @@ __device__ __forceinline__ void token_rope(TokenRope<D / 32> &tr, const float *r
     } else if constexpr (MODE == kRopeInterleaved) {
 #pragma unroll
       for (int j = 0; j < J; ++j) {
-        const int c = lane + 32 * j;
+        const int c = lr + L::LR * j;
         tr.cs[j] = c < rot ? *reinterpret_cast<const float2 *>(tr.row + 2 * (c >> 1))
                            : make_float2(1.0f, 0.0f);
       }
@@ -123,25 +141,36 @@ __device__ __forceinline__ bool token_ok(int64_t slot, int64_t pos, bool has_rop
   return true;
 }
 
-// Norm, rotation and q8 of one key row y (register j = channel lane + 32 j),
-// stored at cache row krow.
+// Norm, rotation and q8 of the warp's R key rows (this lane: y, register j =
+// channel lr + LR j of its row), the row stored at cache row krow when live.
 template <int D, int MODE>
-__device__ __forceinline__ void norm_rope_row(float (&y)[D / 32], const uint64_t (&wt2)[D / 64],
-                                              bool norm, float eps, const TokenRope<D / 32> &tr,
-                                              int rot, float *row_s, int lane,
-                                              int8_t *__restrict__ k_cache,
-                                              uint16_t *__restrict__ k_scale, int64_t krow) {
-  constexpr int J = D / 32;
-  constexpr int kLanesPerGroup = 32 / J;
+__device__ __forceinline__ void norm_rope_rows(float (&y)[RowLayout<D>::J],
+                                               const uint64_t (&wt2)[RowLayout<D>::J / 2],
+                                               bool norm, float eps,
+                                               const TokenRope<RowLayout<D>::J> &tr, int rot,
+                                               float *row_s, int lane, bool live,
+                                               int8_t *__restrict__ k_cache,
+                                               uint16_t *__restrict__ k_scale, int64_t krow) {
+  using L = RowLayout<D>;
+  constexpr int J = L::J, R = L::R, LR = L::LR, G = L::G, LG = L::LG;
+  const int lr = lane % LR;
   // ---- weighted RMSNorm, output rounded to bf16
   if (norm) {
-    float acc = __fmul_rn(y[0], y[0]);
+    float acc[R];  // the per-lane sums of lanes lr + LR k
 #pragma unroll
-    for (int j = 1; j < J; ++j) acc = __fmaf_rn(y[j], y[j], acc);
+    for (int k = 0; k < R; ++k) {
+      acc[k] = __fmul_rn(y[k], y[k]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+      for (int j = k + R; j < J; j += R) acc[k] = __fmaf_rn(y[j], y[j], acc[k]);
+    }
+    // butterfly 16, 8, ..., 1 over the 32 sums: the steps of at least LR
+    // combine sums of one lane, the others go across the row's lanes
+    float t = acc[0];
+    if constexpr (R == 2) t = __fadd_rn(acc[0], acc[1]);
+#pragma unroll
+    for (int o = LR / 2; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
     const float inv =
-        __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(acc, 1.0f / static_cast<float>(D)), eps)));
+        __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(t, 1.0f / static_cast<float>(D)), eps)));
     const uint64_t inv2 = f32x2_pack(inv, inv);
 #pragma unroll
     for (int i = 0; i < J / 2; ++i) {  // two channels at a time
@@ -157,56 +186,56 @@ __device__ __forceinline__ void norm_rope_row(float (&y)[D / 32], const uint64_t
 
   // ---- rotation
   if constexpr (MODE == kRopeHalfFull) {
-    if constexpr (J == 2) {
-      const float lead = y[0], trail = y[1];
-      y[0] = __fmaf_rn(tr.cs[0].x, lead, __fmul_rn(-tr.cs[0].y, trail));
-      y[1] = __fmaf_rn(tr.cs[0].y, lead, __fmul_rn(tr.cs[0].x, trail));
-    } else {
 #pragma unroll
-      for (int i = 0; i < J / 4; ++i) {  // leads 2i, 2i+1 with trails 2i + J/2, 2i+1 + J/2
-        const uint64_t lead = f32x2_pack(y[2 * i], y[2 * i + 1]);
-        const uint64_t trail = f32x2_pack(y[2 * i + J / 2], y[2 * i + 1 + J / 2]);
-        const uint64_t ol = f32x2_fma(tr.cos2[i], lead, f32x2_mul(tr.nsin2[i], trail));
-        const uint64_t ot = f32x2_fma(tr.sin2[i], lead, f32x2_mul(tr.cos2[i], trail));
-        f32x2_unpack(ol, y[2 * i], y[2 * i + 1]);
-        f32x2_unpack(ot, y[2 * i + J / 2], y[2 * i + 1 + J / 2]);
-      }
+    for (int i = 0; i < J / 4; ++i) {  // leads 2i, 2i+1 with trails 2i + J/2, 2i+1 + J/2
+      const uint64_t lead = f32x2_pack(y[2 * i], y[2 * i + 1]);
+      const uint64_t trail = f32x2_pack(y[2 * i + J / 2], y[2 * i + 1 + J / 2]);
+      const uint64_t ol = f32x2_fma(tr.cos2[i], lead, f32x2_mul(tr.nsin2[i], trail));
+      const uint64_t ot = f32x2_fma(tr.sin2[i], lead, f32x2_mul(tr.cos2[i], trail));
+      f32x2_unpack(ol, y[2 * i], y[2 * i + 1]);
+      f32x2_unpack(ot, y[2 * i + J / 2], y[2 * i + 1 + J / 2]);
     }
   } else if constexpr (MODE == kRopeInterleaved) {
     const bool is_lead = (lane & 1) == 0;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const float other = __shfl_xor_sync(0xffffffffu, y[j], 1);
-      if (lane + 32 * j < rot)
+      if (lr + LR * j < rot)
         y[j] = is_lead ? __fmaf_rn(tr.cs[j].x, y[j], __fmul_rn(-tr.cs[j].y, other))
                        : __fmaf_rn(tr.cs[j].y, other, __fmul_rn(tr.cs[j].x, y[j]));
     }
   } else if constexpr (MODE == kRopeHalfPart) {
+    float *rs_row = row_s + (lane / LR) * D;
 #pragma unroll
-    for (int j = 0; j < J; ++j) row_s[lane + 32 * j] = y[j];
+    for (int j = 0; j < J; ++j) rs_row[lr + LR * j] = y[j];
     __syncwarp();
     const int pairs = rot >> 1;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      const int c = lane + 32 * j;
+      const int c = lr + LR * j;
       if (c < rot) {
         const bool is_lead = c < pairs;
         const int p = is_lead ? c : c - pairs;
         const float2 c2 = *reinterpret_cast<const float2 *>(tr.row + 2 * p);
-        const float other = row_s[is_lead ? c + pairs : c - pairs];
+        const float other = rs_row[is_lead ? c + pairs : c - pairs];
         y[j] = is_lead ? __fmaf_rn(c2.x, y[j], __fmul_rn(-c2.y, other))
                        : __fmaf_rn(c2.y, other, __fmul_rn(c2.x, y[j]));
       }
     }
-    __syncwarp();  // row_s is rewritten for the next row
+    __syncwarp();  // row_s is rewritten for the next rows
   }
 
-  // ---- q8 of each group j (register j across the lanes)
-  float m[J];
+  // ---- q8 of each group g (registers R g .. R g + R - 1 across the row's lanes)
+  float m[G];
 #pragma unroll
-  for (int j = 0; j < J; ++j) m[j] = fabsf(y[j]);
-  const float my_sc = group_scale(group_max_scatter<J>(m, lane));
+  for (int g = 0; g < G; ++g) {
+    m[g] = fabsf(y[R * g]);
+#pragma unroll
+    for (int r = 1; r < R; ++r) m[g] = fmaxf(m[g], fabsf(y[R * g + r]));
+  }
+  const float my_sc = group_scale(group_max_scatter<G, LR>(m, lane));
   const float my_rs = __frcp_rn(my_sc);
+  const int base = lane & ~(LR - 1);  // first lane of the row
   // c = the integer nearest to q = y * (1/s), taken exactly from one fused
   // multiply-add of 1.5 * 2^23 (its low byte is the code); d = q - c from a
   // second one.  Where |d| < 1/2 - 2^-15 the IEEE quotient y / s rounds to c
@@ -220,9 +249,11 @@ __device__ __forceinline__ void norm_rope_row(float (&y)[D / 32], const uint64_t
   float d[J], nc[J];
   bool near = false;
 #pragma unroll
-  for (int i = 0; i < J / 2; ++i) {
-    const uint64_t rs2 = f32x2_pack(__shfl_sync(0xffffffffu, my_rs, 2 * i * kLanesPerGroup),
-                                    __shfl_sync(0xffffffffu, my_rs, (2 * i + 1) * kLanesPerGroup));
+  for (int i = 0; i < J / 2; ++i) {  // registers 2i, 2i+1: groups (2i) / R, (2i+1) / R
+    const float rs_a = __shfl_sync(0xffffffffu, my_rs, base + (2 * i / R) * LG);
+    const float rs_b =
+        R == 2 ? rs_a : __shfl_sync(0xffffffffu, my_rs, base + ((2 * i + 1) / R) * LG);
+    const uint64_t rs2 = f32x2_pack(rs_a, rs_b);
     const uint64_t y2 = f32x2_pack(y[2 * i], y[2 * i + 1]);
     const uint64_t t2 = f32x2_fma(y2, rs2, shift2);      // 1.5 * 2^23 + c
     const uint64_t nc2 = f32x2_fma(t2, minus1, shift2);  // -c, exact
@@ -240,25 +271,31 @@ __device__ __forceinline__ void norm_rope_row(float (&y)[D / 32], const uint64_t
   // to (rare: the whole warp takes this branch together).
   if (__any_sync(0xffffffffu, near)) {
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const float sc = __shfl_sync(0xffffffffu, my_sc, j * kLanesPerGroup);
-      if (fabsf(d[j]) >= kFar) {
-        const float hh = __fsub_rn(copysignf(0.5f, d[j]), nc[j]);
-        tb[j] = tie_code_bits(y[j], sc, hh);
+    for (int g = 0; g < G; ++g) {
+      const float sc = __shfl_sync(0xffffffffu, my_sc, base + g * LG);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int j = R * g + r;
+        if (fabsf(d[j]) >= kFar) {
+          const float hh = __fsub_rn(copysignf(0.5f, d[j]), nc[j]);
+          tb[j] = tie_code_bits(y[j], sc, hh);
+        }
       }
     }
   }
-  int8_t *dst = k_cache + krow * D + lane;
+  if (live) {
+    int8_t *dst = k_cache + krow * D + lr;
 #pragma unroll
-  for (int j = 0; j < J; ++j) dst[32 * j] = static_cast<int8_t>(tb[j] & 0xffu);
-  // each group's first lane stores its scale
-  if (lane % kLanesPerGroup == 0)
-    k_scale[krow * J + lane / kLanesPerGroup] = __half_as_ushort(__float2half_rn(my_sc));
+    for (int j = 0; j < J; ++j) dst[LR * j] = static_cast<int8_t>(tb[j] & 0xffu);
+    // each group's first lane stores its scale
+    if (lr % LG == 0) k_scale[krow * G + lr / LG] = __half_as_ushort(__float2half_rn(my_sc));
+  }
 }
 
 // grid: one warp per unit (ceil(units / kRopeWarps) blocks, capped; the
 // warps then stride on); block: 32 x kRopeWarps; dynamic shared memory:
-// kRopeHalfPart, [kRopeWarps][D] fp32.
+// kRopeHalfPart, [kRopeWarps][R][D] fp32.  A warp works its unit's heads R
+// at a time, head h0 + R i + lane / LR in lanes LR (lane / LR) ...
 template <int D, int BS, int MODE>
 __global__ void __launch_bounds__(32 * kRopeWarps) kv_store_norm_rope_kernel(
     const uint16_t *__restrict__ key, int64_t key_stride, const int64_t *__restrict__ slot_mapping,
@@ -266,20 +303,23 @@ __global__ void __launch_bounds__(32 * kRopeWarps) kv_store_norm_rope_kernel(
     const uint16_t *__restrict__ norm_weight, float eps, const float *__restrict__ rope,
     int32_t max_position, int32_t rot, int8_t *__restrict__ k_cache,
     uint16_t *__restrict__ k_scale, int64_t num_slots, uint32_t *status) {
-  constexpr int J = D / 32;  // channels per lane, and q8 groups per row
+  using L = RowLayout<D>;
+  constexpr int J = L::J, R = L::R, LR = L::LR;
   extern __shared__ __align__(16) float rope_rows[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  float *row_s = rope_rows + warp * D;
+  const int lr = lane % LR;
+  const int my_row = lane / LR;
+  float *row_s = rope_rows + warp * R * D;
   const bool norm = norm_weight != nullptr;
   constexpr bool kHasRope = MODE != kRopeNone;
 
-  uint64_t wt2[J / 2];  // norm weights of channel pairs (2i, 2i + 1) of the lane
+  uint64_t wt2[J / 2];  // norm weights of the lane's channel pairs (registers 2i, 2i + 1)
   if (norm) {
 #pragma unroll
     for (int i = 0; i < J / 2; ++i)
-      wt2[i] = f32x2_pack(bf16_lo(norm_weight[lane + 64 * i]),
-                          bf16_lo(norm_weight[lane + 64 * i + 32]));
+      wt2[i] = f32x2_pack(bf16_lo(norm_weight[lr + LR * (2 * i)]),
+                          bf16_lo(norm_weight[lr + LR * (2 * i + 1)]));
   }
   const int heads_per = (hk + head_split - 1) / head_split;
   const int64_t units = static_cast<int64_t>(num_tokens) * head_split;
@@ -299,31 +339,37 @@ __global__ void __launch_bounds__(32 * kRopeWarps) kv_store_norm_rope_kernel(
     const int64_t pos = kHasRope && slot >= 0 && slot < num_slots ? positions[n] : 0;
     if (h0 >= h1 || !token_ok(slot, pos, kHasRope, h0, lane, num_slots, max_position, status))
       continue;
-    token_rope<D, MODE>(tr, rope, pos, rot, lane);
+    token_rope<D, MODE>(tr, rope, pos, rot, lr);
     const uint64_t us = static_cast<uint64_t>(slot);
     const int64_t blk = static_cast<int64_t>(us / BS), off = static_cast<int64_t>(us % BS);
-    const uint16_t *src = key + n * key_stride + lane;
+    const uint16_t *src = key + n * key_stride + lr;
     uint16_t nxt[J];
+    {
+      const int h = h0 + my_row;
 #pragma unroll
-    for (int j = 0; j < J; ++j) nxt[j] = src[static_cast<int64_t>(h0) * D + 32 * j];
+      for (int j = 0; j < J; ++j) nxt[j] = h < h1 ? src[static_cast<int64_t>(h) * D + LR * j] : 0;
+    }
 #pragma unroll 1
-    for (int h = h0; h < h1; ++h) {
+    for (int hb = h0; hb < h1; hb += R) {
+      const int h = hb + my_row;
       float y[J];
 #pragma unroll
       for (int j = 0; j < J; ++j) y[j] = bf16_lo(nxt[j]);
-      if (h + 1 < h1) {  // the next head's row, in flight while this one is worked
+      const int hn = h + R;
+      if (hb + R < h1) {  // the next rows, in flight while these are worked
 #pragma unroll
-        for (int j = 0; j < J; ++j) nxt[j] = src[static_cast<int64_t>(h + 1) * D + 32 * j];
+        for (int j = 0; j < J; ++j)
+          nxt[j] = hn < h1 ? src[static_cast<int64_t>(hn) * D + LR * j] : 0;
       }
-      norm_rope_row<D, MODE>(y, wt2, norm, eps, tr, rot, row_s, lane, k_cache, k_scale,
-                             (blk * hk + h) * BS + off);
+      norm_rope_rows<D, MODE>(y, wt2, norm, eps, tr, rot, row_s, lane, h < h1, k_cache, k_scale,
+                              (blk * hk + h) * BS + off);
     }
   }
 }
 
 template <int D, int BS, int MODE>
 static cudaError_t launch_keys(const KvNormRope &p, cudaStream_t stream) {
-  constexpr int smem = MODE == kRopeHalfPart ? kRopeWarps * D * 4 : 0;
+  constexpr int smem = MODE == kRopeHalfPart ? kRopeWarps * RowLayout<D>::R * D * 4 : 0;
   // the shared-memory carveout of the values kernel, so that the blocks of
   // both can be resident on one SM together
   static DeviceOnce carveout;
@@ -336,11 +382,12 @@ static cudaError_t launch_keys(const KvNormRope &p, cudaStream_t stream) {
   });
   if (e != cudaSuccess) return e;
   // units of a token's heads (as many as fit kRopeMaxBytes) when that makes
-  // enough units to fill the GPU; otherwise one head per unit
+  // enough units to fill the GPU; otherwise one warp's rows (R heads) per unit
   constexpr int kMaxHeads = kRopeMaxBytes / (2 * D);
   const int wide_split = (p.hk + kMaxHeads - 1) / kMaxHeads;
   const int64_t wide_units = static_cast<int64_t>(p.num_tokens) * wide_split;
-  const int head_split = wide_units >= kRopeWideUnits ? wide_split : p.hk;
+  constexpr int R = RowLayout<D>::R;
+  const int head_split = wide_units >= kRopeWideUnits ? wide_split : (p.hk + R - 1) / R;
   const int64_t units = static_cast<int64_t>(p.num_tokens) * head_split;
   const int64_t want = (units + kRopeWarps - 1) / kRopeWarps;
   const unsigned grid = static_cast<unsigned>(want < (1 << 30) ? want : (1 << 30));
