@@ -13,12 +13,17 @@
 //                                               (low nibble) and 2j + 1
 //   v_scale, v_zero fp16 [num_blocks][hk][bs]
 //
-// One warp per (32 consecutive tokens, kv head); lane = token.  Two tokens
-// whose slots share a nibble byte (offsets 2j, 2j + 1 of one page) and sit in
-// the same warp -- consecutive tokens of a prefill chunk -- are written
-// together by the even one; a token whose byte mate is not in the warp
-// updates its nibbles with 32-bit atomics (so a mate in another warp or from
-// an earlier call is never overwritten).
+// Work units: (32 consecutive tokens, kv head), once for the keys and once
+// for the values, one warp each (even warps keys, odd warps values).  Keys:
+// token by token, the lanes on consecutive D/32-channel pieces of the row
+// (one coalesced load and store per row, eight rows in flight).  Values:
+// lane = token.  Two tokens whose slots share a nibble byte (offsets 2j,
+// 2j + 1 of one page) and sit in the same warp -- consecutive tokens of a
+// prefill chunk -- are written together by the even one; a token whose byte
+// mate is not in the warp updates its nibbles with 32-bit atomics (so a mate
+// in another warp or from an earlier call is never overwritten).
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 #include "q8_quant.cuh"
@@ -121,40 +126,66 @@ __global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
   __shared__ uint32_t nib_s[kF8v4Warps][W][kNibStride];
   const int lane = threadIdx.x & 31;
   const int n_tblocks = (num_tokens + 31) / 32;
-  const int64_t units = static_cast<int64_t>(n_tblocks) * hk;
+  const int64_t units = static_cast<int64_t>(n_tblocks) * hk * 2;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kF8v4Warps;
+  const int bs_log2 = block_size == 32 ? 5 : 4;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * kF8v4Warps + (threadIdx.x >> 5); u < units;
        u += stride) {
-    const int h = static_cast<int>(u % hk);
-    const int64_t n = (u / hk) * 32 + lane;
+    const bool keys = (u & 1) == 0;
+    const int h = static_cast<int>((u >> 1) % hk);
+    const int64_t tb = (u >> 1) / hk;
+    const int64_t n = tb * 32 + lane;
     int64_t slot = n < num_tokens ? slot_mapping[n] : -1;
     if (slot >= num_slots) {
-      if (h == 0) flag_status(status, PA_DEV_BAD_SLOT);
+      if (h == 0 && !keys) flag_status(status, PA_DEV_BAD_SLOT);
       slot = -1;
     }
     const bool active = slot >= 0;
+
+    if (keys) {
+      // ---- keys: e4m3 of each value; token t of the block at a time, lane l
+      // on channels l * KC .. l * KC + KC - 1 (eight rows in flight)
+      constexpr int KC = D / 32;
+      using Piece = std::conditional_t<KC == 2, uint32_t, std::conditional_t<KC == 4, uint2, uint4>>;
+#pragma unroll 1
+      for (int t0 = 0; t0 < 32; t0 += 8) {
+        Piece a[8];
+        int64_t row[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int64_t st = __shfl_sync(0xffffffffu, slot, t0 + i);
+          row[i] = -1;
+          if (st >= 0) {
+            const int64_t nt = tb * 32 + t0 + i;
+            a[i] = *reinterpret_cast<const Piece *>(key + nt * key_stride +
+                                                     static_cast<int64_t>(h) * D + lane * KC);
+            row[i] = (((st >> bs_log2) * hk + h) << bs_log2) + (st & (block_size - 1));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (row[i] < 0) continue;
+          uint8_t *kd = k_cache + row[i] * D + lane * KC;
+          if constexpr (KC == 2) {
+            *reinterpret_cast<uint16_t *>(kd) =
+                static_cast<uint16_t>(f32x2_to_e4m3x2(bf16_lo(a[i]), bf16_hi(a[i])));
+          } else if constexpr (KC == 4) {
+            *reinterpret_cast<uint32_t *>(kd) =
+                f32x2_to_e4m3x2(bf16_lo(a[i].x), bf16_hi(a[i].x)) |
+                (f32x2_to_e4m3x2(bf16_lo(a[i].y), bf16_hi(a[i].y)) << 16);
+          } else {
+            *reinterpret_cast<uint2 *>(kd) =
+                make_uint2(f32x2_to_e4m3x2(bf16_lo(a[i].x), bf16_hi(a[i].x)) |
+                               (f32x2_to_e4m3x2(bf16_lo(a[i].y), bf16_hi(a[i].y)) << 16),
+                           f32x2_to_e4m3x2(bf16_lo(a[i].z), bf16_hi(a[i].z)) |
+                               (f32x2_to_e4m3x2(bf16_lo(a[i].w), bf16_hi(a[i].w)) << 16));
+          }
+        }
+      }
+      continue;
+    }
     const int64_t blk = active ? slot / block_size : 0, off = active ? slot % block_size : 0;
     const int64_t page = blk * hk + h;
-
-    // ---- keys: e4m3 of each value, one 16-byte store per 16 channels
-    if (active) {
-      const uint16_t *ks = key + n * key_stride + static_cast<int64_t>(h) * D;
-      uint8_t *kd = k_cache + (page * block_size + off) * D;
-#pragma unroll 4
-      for (int c = 0; c < D; c += 16) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(ks + c);
-        const uint4 b = *reinterpret_cast<const uint4 *>(ks + c + 8);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * i]), bf16_hi(w[2 * i]));
-          const uint32_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * i + 1]), bf16_hi(w[2 * i + 1]));
-          o[i] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4 *>(kd + c) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
 
     // ---- values: 4-bit codes with the row's scale and zero.  The nibble
     // words go through shared memory (word i of lane l at nib[i][l]), so that
@@ -266,7 +297,7 @@ cudaError_t launch_kv_store_f8v4(const uint16_t *key, int64_t key_stride, const 
     return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
   });
   if (e != cudaSuccess) return e;
-  const int64_t units = static_cast<int64_t>((num_tokens + 31) / 32) * hk;
+  const int64_t units = static_cast<int64_t>((num_tokens + 31) / 32) * hk * 2;
   const int64_t want = (units + kF8v4Warps - 1) / kF8v4Warps;
   const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
