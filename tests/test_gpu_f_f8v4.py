@@ -161,3 +161,40 @@ def test_f8v4_prefill_options(window, sink, causal, cuda_device):
         out, lse = g.gpu(num_splits=ns, sinks=sinks, window=window, causal=causal)
         H.compare(out, lse, ref_out, ref_lse, rows,
                   label=f"f8v4 prefill window={window} sink={sink} causal={causal} splits={ns}")
+
+
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 32), (256, 16)])
+def test_f8v4_store_padding_bad_slots_and_strided_rows(d, bs, cuda_device):
+    # padding rows, two slots past the cache (flagged, skipped for K and V),
+    # a run of consecutive slots then a shuffled tail, and key / value rows
+    # with a token stride past hk * D (16-byte aligned)
+    rng = np.random.default_rng(510 + d + bs)
+    n, hk, pad = 203, 3, 8
+    num_blocks = (n + bs - 1) // bs + 4
+    nslots = num_blocks * bs
+    slots = np.arange(n, dtype=np.int64)
+    tail = n // 3
+    slots[-tail:] = rng.permutation(np.arange(n - tail, nslots))[:tail]
+    slots[rng.choice(n, size=9, replace=False)] = -1
+    bad = rng.choice(np.flatnonzero(slots >= 0), size=2, replace=False)
+    slots[bad] = [nslots, nslots + 77]
+    rows = [torch.from_numpy(rng.standard_normal((n, hk * d + pad)) * 3.0).to(torch.bfloat16)
+            for _ in range(2)]
+    k, v = (r[:, :hk * d].reshape(n, hk, d) for r in rows)
+    kc, vc, vs, vz = inputs.empty_cache_f8v4(num_blocks, hk, bs, d, device=cuda_device)
+    status = torch.zeros(4, dtype=torch.int32, device=cuda_device)
+    kd, vd = (r.to(cuda_device).as_strided((n, hk, d), (hk * d + pad, d, 1)) for r in rows)
+    _lib.kv_store_f8v4(kd, vd, torch.from_numpy(slots).to(cuda_device), kc, vc, vs, vz,
+                       status=status)
+    okc, ovc, ovs, ovz = inputs.empty_cache_f8v4(num_blocks, hk, bs, d)
+    okc, ovc = okc.numpy(), ovc.numpy()
+    ovs, ovz = ovs.numpy().view(np.uint16), ovz.numpy().view(np.uint16)
+    assert oracle.kv_store_f8v4(inputs.bf16_bits(k.contiguous()), inputs.bf16_bits(v.contiguous()),
+                                slots, okc, ovc, ovs, ovz) == 2
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        _lib.check_status(status)
+    assert e.value.bits == _lib.DEV_BAD_SLOT
+    np.testing.assert_array_equal(kc.cpu().numpy(), okc)
+    np.testing.assert_array_equal(vc.cpu().numpy(), ovc)
+    np.testing.assert_array_equal(vs.cpu().numpy().view(np.uint16), ovs)
+    np.testing.assert_array_equal(vz.cpu().numpy().view(np.uint16), ovz)
