@@ -256,6 +256,7 @@ cudaError_t launch_paged_attention(const AttnLaunch &L, cudaStream_t stream) {
     SideStream *ss = nullptr;
     cudaError_t e = side_stream(&ss);
     if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(ss->mu);  // fork record .. join wait
     if ((e = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
     AttnArgs p = a;

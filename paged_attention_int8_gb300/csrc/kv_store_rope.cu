@@ -431,6 +431,7 @@ cudaError_t launch_kv_store_norm_rope(const KvNormRope &p, cudaStream_t stream) 
   const int64_t *vpos = p.rope ? p.positions : nullptr;
   SideStream *ss = nullptr;
   if (p.num_tokens >= kRopeOverlapTokens && side_stream(&ss) == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(ss->mu);  // fork record .. join wait
     cudaError_t e;
     if ((e = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;

@@ -81,11 +81,14 @@ cudaError_t launch_kv_store_values(const uint16_t *value, int64_t value_stride,
 
 // A high-priority side stream of the current device, with fork / join
 // events, for work that runs beside the caller's stream.  Created once per
-// device; calls from several host threads share it (correct, but their side
-// work then queues behind one another).
+// device; calls from several host threads share it: each holds `mu` from its
+// fork record to its join wait, so that another caller's record cannot come
+// between its record and its wait (their side work then queues behind one
+// another).
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
 };
 cudaError_t side_stream(SideStream **out);
 
