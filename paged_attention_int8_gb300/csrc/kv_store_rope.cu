@@ -39,7 +39,7 @@ namespace paq8 {
 
 constexpr int kRopeWarps = 8;
 constexpr int kRopeMaxBytes = 2048;          // bf16 keys of one unit, at most
-constexpr int64_t kRopeWideUnits = 16384;    // fewer wide units: one head per unit
+constexpr int64_t kRopeWideUnits = 16384;    // fewer wide units: one warp's rows per unit
 constexpr int32_t kRopeOverlapTokens = 4096;  // fewer tokens: keys, then values
 
 enum RopeMode : int {
