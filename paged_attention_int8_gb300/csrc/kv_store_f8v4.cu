@@ -207,14 +207,50 @@ __global__ void __launch_bounds__(32 * kF8v4Warps) kv_store_f8v4_kernel(
       }
       const float s = v4_step(lo, hi);
       const float rs = __frcp_rn(s);
-#pragma unroll 2
+      // The code of v = x - lo: c, the integer nearest to v * (1/s), from one
+      // fused multiply-add of 1.5 * 2^23 (its low nibble), and d = v * (1/s)
+      // - c from a second, two values at a time; values within 2^-15 of a
+      // tie take the IEEE quotient's code exactly (as v4_code).  No clamp is
+      // needed: 0 <= v <= RN(hi - lo), so 0 <= v * (1/s) < 15.00001.
+      constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+      constexpr float kFar = 0.5f - 0x1p-15f;
+      const uint64_t nlo2 = f32x2_pack(-lo, -lo), rs2 = f32x2_pack(rs, rs);
+      const uint64_t shift2 = f32x2_pack(kShift, kShift), minus1 = f32x2_pack(-1.0f, -1.0f);
+#pragma unroll 1
       for (int c = 0; c < D; c += 8) {
         const uint4 a = *reinterpret_cast<const uint4 *>(vs + c);
         const uint32_t w[4] = {a.x, a.y, a.z, a.w};
         uint32_t word = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          word |= v4_code((i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]), lo, s, rs) << (4 * i);
+        for (int half = 0; half < 2; ++half) {  // channels 4 half .. 4 half + 3
+          uint32_t tb[4];
+          float v[4], d[4], nc[4];
+          bool near = false;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint32_t ww = w[2 * half + i];
+            const uint64_t v2 = f32x2_add(f32x2_pack(bf16_lo(ww), bf16_hi(ww)), nlo2);  // x - lo
+            const uint64_t t2 = f32x2_fma(v2, rs2, shift2);      // 1.5 * 2^23 + c
+            const uint64_t nc2 = f32x2_fma(t2, minus1, shift2);  // -c, exact
+            const uint64_t d2 = f32x2_fma(v2, rs2, nc2);         // v * rs - c
+            float t0, t1;
+            f32x2_unpack(t2, t0, t1);
+            tb[2 * i] = __float_as_uint(t0);
+            tb[2 * i + 1] = __float_as_uint(t1);
+            f32x2_unpack(v2, v[2 * i], v[2 * i + 1]);
+            f32x2_unpack(d2, d[2 * i], d[2 * i + 1]);
+            f32x2_unpack(nc2, nc[2 * i], nc[2 * i + 1]);
+            near = near || fabsf(d[2 * i]) >= kFar || fabsf(d[2 * i + 1]) >= kFar;
+          }
+          if (near) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (fabsf(d[i]) >= kFar)
+                tb[i] = tie_code_bits(v[i], s, __fsub_rn(copysignf(0.5f, d[i]), nc[i]));
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) word |= (tb[i] & 0xfu) << (16 * half + 4 * i);
+        }
         nib[c / 8][lane] = word;
       }
       v_scale[page * block_size + off] = __half_as_ushort(__float2half_rn(s));
