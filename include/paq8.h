@@ -2,10 +2,16 @@
  * paq8 -- paged attention over a q8 KV cache, for NVIDIA GB300 (sm_103a).
  *
  * C ABI.  All tensors are caller-owned device buffers passed as plain
- * pointers; the library never allocates or frees device memory, never
- * synchronizes a stream (except pa_check_status), and launches every kernel
- * on the stream given.  `stream` is a cudaStream_t (NULL = the legacy default
- * stream).  bf16 and fp16 buffers are passed as raw 16-bit words.
+ * pointers; the library never allocates or frees device memory and never
+ * synchronizes a stream (except pa_check_status).  Each call's work is
+ * ordered on the stream given: its kernels run there, or -- the prefill
+ * kernel of a batch that mixes prefill and decode (not in
+ * pa_paged_attention_noalloc), the values of a fused store of 4096 tokens or
+ * more -- on an internal high-priority stream of the device that is forked
+ * from it and joined back to it inside the call (the pattern stream capture
+ * accepts).  `stream` is a cudaStream_t (NULL = the
+ * legacy default stream).  bf16 and fp16 buffers are passed as raw 16-bit
+ * words.
  *
  * The q8 format (page "shared/attention_kit.py", `quantize_q8` and the
  * `KVPrefix` docstring): int8 codes, one fp16 scale per (token, kv head,
